@@ -1,0 +1,204 @@
+"""CPU oracle for the routed-expert MXFP4 mixture-of-experts layer.
+
+TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import this module. The product
+path (the C-ABI library and its Python binding) never calls it, and this module
+imports nothing from the product package: it shares no code, table or helper
+with the CUDA kernels.
+
+What it computes, step by step, each in the plainest form (float64 numpy, one
+library matmul per projection):
+
+1. ``route``      stable counting sort of the routes r = t*k + j by expert.
+                  ("MXFP4 MoE decode kernels", Design, "Routing inside the
+                  kernel": routes are counting-sorted by local expert; routes
+                  to experts that are not present are skipped.)
+2. ``dequant``    w = E2M1(nibble) * 2^(E8M0 - 127), nibble 2i = low nibble of
+                  byte i, one scale per 32 values along the row.
+                  ("GLM-5.2 and GLM-5.3 (744B) in MXFP4 on Gaudi 2", What was
+                  built, "Byte-exact repack": OCP MXFP4, E2M1 low nibble first,
+                  E8M0 scales, blocks of 32; "MXFP4 MoE decode kernels", The
+                  bottleneck and Design, "Read the served layout":
+                  w13 u8 [E, 2I, K/2], s13 u8 [E, 2I, K/32], w2 u8 [E, K, I/2],
+                  s2 u8 [E, K, I/32].)
+3. w13 projection g = W_gate x, u = W_up x with the rows of each expert's w13
+   stored as [gate; up] ("GLM-5.2 and GLM-5.3", Why it needed a port, item 1;
+   "MXFP4 MoE decode kernels", Beyond gpt-oss: SiLU without bias for [gate; up]
+   row layouts).
+4. SwiGLU h = silu(g) * u, silu(z) = z / (1 + e^-z), then (default) one
+   rounding of h to bf16 ("MXFP4 MoE decode kernels", Parity: the reference is
+   CPU fp32 with dequantised weights and a bf16 intermediate).
+5. w2 projection o = W2 h.
+6. Weighted combine y_t = sum over slots j = 0..k-1 of w_tj * o_(t,j)
+   ("MXFP4 MoE decode kernels", Design, Fused epilogues: weighted sum per
+   token).
+
+All arithmetic is float64; products of E2M1 values, powers of two and bf16
+activations are exact there, so the only roundings are the sums (float64) and
+the optional bf16 rounding of h.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# --- E2M1 and E8M0 -----------------------------------------------------------
+# The 16 E2M1 codes in code order: bit 3 is the sign, bits 2..1 the exponent
+# (bias 1), bit 0 the mantissa; code 1 is the subnormal 0.5.
+E2M1_TABLE = np.array([
+    +0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+    -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0,
+], dtype=np.float64)
+
+SCALE_BLOCK = 32  # values per E8M0 scale along the row
+
+
+def e8m0_value(scale_bytes) -> np.ndarray:
+    """2^(s - 127) as float64; the byte 255 is NaN (OCP MX convention)."""
+    s = np.asarray(scale_bytes).astype(np.int64)
+    v = np.ldexp(np.ones(s.shape, dtype=np.float64), s - 127)
+    return np.where(s == 255, np.nan, v)
+
+
+def unpack_codes(packed) -> np.ndarray:
+    """uint8 [..., C/2] -> codes uint8 [..., C]; value 2i is the low nibble of byte i."""
+    p = np.asarray(packed, dtype=np.uint8)
+    codes = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    codes[..., 0::2] = p & 0x0F
+    codes[..., 1::2] = p >> 4
+    return codes
+
+
+def dequant(packed, scale) -> np.ndarray:
+    """Packed rows [..., N, C/2] with scales [..., N, C/32] -> float64 [..., N, C]."""
+    codes = unpack_codes(packed)
+    vals = E2M1_TABLE[codes]
+    factor = e8m0_value(scale)
+    if factor.shape[-1] * SCALE_BLOCK != vals.shape[-1]:
+        raise ValueError("scale count does not match the row length / 32")
+    return vals * np.repeat(factor, SCALE_BLOCK, axis=-1)
+
+
+# --- bf16 --------------------------------------------------------------------
+BF16_MAX = float.fromhex("0x1.fe0000p+127")  # (2 - 2^-7) * 2^127
+
+
+def bf16_bits_to_float(bits) -> np.ndarray:
+    """Raw bf16 bit patterns (uint16) -> float64 (exact)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return b.view(np.float32).astype(np.float64)
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bf16 value, ties to even.
+
+    bf16 keeps 8 significant bits: a finite x = m * 2^e (0.5 <= |m| < 1) is
+    rounded to a multiple of 2^(e-8), never finer than the smallest subnormal
+    2^-133. Results beyond the largest finite bf16 become +-inf.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    out = x.copy()
+    fin = np.isfinite(x)
+    xf = x[fin]
+    _, e = np.frexp(xf)
+    q = np.maximum(e - 8, -133)
+    y = np.ldexp(np.rint(np.ldexp(xf, -q)), q)
+    big = np.abs(y) > BF16_MAX
+    y[big] = np.copysign(np.inf, y[big])
+    out[fin] = y
+    return out
+
+
+def float_to_bf16_bits(x) -> np.ndarray:
+    """float64 -> bf16 bit patterns after round_to_bf16 (NaN -> 0x7FC0)."""
+    r = round_to_bf16(x)
+    bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    bits[np.isnan(r)] = 0x7FC0
+    return bits
+
+
+# --- routing -------------------------------------------------------------------
+def route(topk_ids, E: int) -> dict:
+    """Stable counting sort of routes by expert.
+
+    Route r = t*k + j (row-major over topk_ids). Negative ids are padding and
+    skipped; ids >= E are counted as invalid and skipped. Returns count[E],
+    offset[E+1] (exclusive prefix sum), list (route ids grouped by expert,
+    ascending r inside each group), invalid, and touched (experts with a
+    non-zero count, ascending).
+    """
+    flat = np.asarray(topk_ids).reshape(-1).tolist()
+    buckets = [[] for _ in range(E)]
+    invalid = 0
+    for r, e in enumerate(flat):
+        if e < 0:
+            continue
+        if e >= E:
+            invalid += 1
+            continue
+        buckets[e].append(r)
+    count = np.array([len(b) for b in buckets], dtype=np.int64)
+    offset = np.zeros(E + 1, dtype=np.int64)
+    offset[1:] = np.cumsum(count)
+    lst = np.array([r for b in buckets for r in b], dtype=np.int64)
+    touched = np.array([e for e in range(E) if buckets[e]], dtype=np.int64)
+    return dict(count=count, offset=offset, list=lst, invalid=invalid, touched=touched)
+
+
+# --- the layer -----------------------------------------------------------------
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def forward(hidden_bits, topk_ids, topk_weights, w13, s13, w2, s2,
+            intermediate: str = "bf16", tokens=None) -> np.ndarray:
+    """The MoE layer output y [T', K] in float64 (not rounded to bf16).
+
+    hidden_bits: bf16 bit patterns uint16 [T, K]; topk_ids int [T, k];
+    topk_weights float32 [T, k]; w13 uint8 [E, 2I, K/2]; s13 uint8 [E, 2I, K/32];
+    w2 uint8 [E, K, I/2]; s2 uint8 [E, K, I/32].
+    intermediate: "bf16" rounds h to bf16 once (the pages' reference), "fp32"
+    keeps it unrounded. tokens: optional list of token indices; each output
+    row depends only on its own token's routes, so a subset is computed the
+    same way on fewer routes.
+    """
+    if intermediate not in ("bf16", "fp32"):
+        raise ValueError(intermediate)
+    ids = np.asarray(topk_ids)
+    wts = np.asarray(topk_weights).astype(np.float64)
+    xs = bf16_bits_to_float(hidden_bits)
+    if tokens is not None:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        ids, wts, xs = ids[tokens], wts[tokens], xs[tokens]
+    T, k = ids.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    K = w2.shape[1]
+    rt = route(ids, E)
+    o = np.zeros((T * k, K), dtype=np.float64)
+    for e in rt["touched"].tolist():
+        r = rt["list"][rt["offset"][e]:rt["offset"][e + 1]]
+        x_e = xs[r // k]                              # [M_e, K]
+        W13 = dequant(w13[e], s13[e])                 # [2I, K], rows [gate; up]
+        g = x_e @ W13[:I].T
+        u = x_e @ W13[I:].T
+        h = silu(g) * u
+        if intermediate == "bf16":
+            h = round_to_bf16(h)
+        W2 = dequant(w2[e], s2[e])                    # [K, I]
+        o[r] = h @ W2.T
+    y = np.zeros((T, K), dtype=np.float64)
+    E_ok = (ids >= 0) & (ids < E)
+    for j in range(k):                                # slot order j = 0 .. k-1
+        rows = np.arange(T) * k + j
+        contrib = wts[:, j:j + 1] * o[rows]
+        y += np.where(E_ok[:, j:j + 1], contrib, 0.0)
+    return y
+
+
+def touched_bytes(topk_ids, E: int, K: int, I: int) -> int:
+    """Algorithmic HBM bytes of one call: packed bytes + scales of each touched
+    expert read once (3*I*K*(1/2 + 1/32) per expert)."""
+    n = len(route(topk_ids, E)["touched"])
+    return n * (3 * I * K // 2 + 3 * I * K // 32)

@@ -1,0 +1,18 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a); parity against the CPU oracle")
+
+
+@pytest.fixture(scope="session")
+def oracle():
+    from oracle import mxfp4_moe_oracle
+    return mxfp4_moe_oracle
