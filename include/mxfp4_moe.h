@@ -1,0 +1,134 @@
+/*
+ * mxfp4_moe.h -- C ABI of the routed-expert MXFP4 mixture-of-experts layer
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer reads each expert's weights in the served packed layout
+ * ("MXFP4 MoE decode kernels", Design, "Read the served layout"):
+ *   w13  uint8 [E, 2I, K/2]   two E2M1 values per byte, low nibble first
+ *   s13  uint8 [E, 2I, K/32]  one E8M0 scale per 32 values along K
+ *   w2   uint8 [E, K, I/2]
+ *   s2   uint8 [E, K, I/32]
+ * and computes, for every token t and slot j of its top-k routing,
+ *   g, u = split([gate; up] rows of dequant(w13[e])) . x_t     (fp32 accumulate)
+ *   h    = bf16( silu(g) * u )                                  (one bf16 rounding)
+ *   o    = dequant(w2[e]) . h                                   (fp32 accumulate)
+ *   y_t  = bf16( sum_{j=0..k-1} w_tj * o_(t,j) )                (slot order)
+ * where dequant(v) = E2M1(nibble) * 2^(E8M0 - 127) ("GLM-5.2 and GLM-5.3 (744B)
+ * in MXFP4 on Gaudi 2", What was built, "Byte-exact repack"; "MXFP4 MoE decode
+ * kernels", Design, "Unpack in registers" and "Fused epilogues"; Beyond
+ * gpt-oss, "mxk_w13x: SiLU without bias for [gate; up] row layouts").
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller (for
+ *    example a PyTorch CUDA tensor's data_ptr()), unless it is marked "host".
+ *    The library never allocates device memory, never frees, and never
+ *    synchronises the device: each call validates its arguments on the host,
+ *    enqueues its kernels on `stream` (a cudaStream_t passed as void*, NULL =
+ *    the legacy default stream) and returns.
+ *  - A non-zero return value is an mxfp4_moe_status code and means nothing
+ *    was enqueued (except MXFP4_MOE_ERR_CUDA, which reports a failed launch).
+ *  - Conditions only the device can see are written to `status` (device
+ *    int32[4]) by the enqueued work:
+ *       status[0] = number of routes whose expert id is >= E (skipped)
+ *       status[1] = number of distinct experts touched by the call
+ *       status[2], status[3] = 0 (reserved)
+ *    Negative expert ids are padding and are skipped silently.
+ *  - Every call is deterministic: repeating it on the same inputs gives
+ *    bit-identical outputs (no floating-point atomics anywhere).
+ */
+#ifndef MXFP4_MOE_H_
+#define MXFP4_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXFP4_MOE_OK = 0,
+  MXFP4_MOE_ERR_ARG = 1,        /* null pointer where one is required, negative size */
+  MXFP4_MOE_ERR_SHAPE = 2,      /* shape outside the supported limits listed below */
+  MXFP4_MOE_ERR_ALIGN = 3,      /* a pointer breaks its alignment rule */
+  MXFP4_MOE_ERR_WORKSPACE = 4,  /* workspace missing or smaller than mxfp4_moe_workspace_size */
+  MXFP4_MOE_ERR_CUDA = 5,       /* a CUDA runtime call failed (device query or launch) */
+  MXFP4_MOE_ERR_DEVICE = 6      /* current device is not an sm_103 GPU */
+} mxfp4_moe_status;
+
+/* Shape limits (checked on the host, MXFP4_MOE_ERR_SHAPE otherwise):
+ *   K % 32 == 0, I % 32 == 0, 32 <= K, I <= 16384
+ *   1 <= E <= 1024, 1 <= topk <= 32, topk <= E, 0 <= T
+ *   decode path: T <= 32 and T * topk <= 1024
+ *   prefill path: K % 64 == 0, I % 64 == 0 (tensor-core tiles), T * topk < 2^31 / K
+ * Alignment (MXFP4_MOE_ERR_ALIGN otherwise): w13, w2, hidden and out 16-byte
+ * aligned; workspace 256-byte aligned. Scale arrays have no alignment rule. */
+
+/* Bytes of device workspace a forward call with these sizes needs (either
+ * path). The first mxfp4_moe_workspace_size(...) bytes must be zero before
+ * the first call that uses a workspace; every completed call leaves the
+ * bookkeeping part zero again, so a workspace can be reused without clearing.
+ * Returns 0 for invalid sizes. */
+size_t mxfp4_moe_workspace_size(int T, int K, int I, int E, int topk);
+
+/* Routing / permute ("MXFP4 MoE decode kernels", Design, "Routing inside the
+ * kernel": a counting sort of the routes by expert; absent experts skipped).
+ * Route r = t * topk + j. Outputs:
+ *   expert_count  int32 [E]     routes per expert
+ *   expert_offset int32 [E+1]   exclusive prefix sum, expert_offset[E] = valid routes
+ *   route_list    int32 [T*topk] route ids grouped by expert in ascending
+ *                 expert order, ascending r inside a group; entries past
+ *                 expert_offset[E] are set to -1
+ *   status        int32 [4]     as above (may be NULL)
+ * topk_ids int32 [T, topk]. No workspace needed. */
+int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E,
+                    int32_t* expert_count, int32_t* expert_offset, int32_t* route_list,
+                    int32_t* status, void* stream);
+
+/* The MoE layer, y = sum_j w_tj * W2[e] silu(W_gate[e] x) * (W_up[e] x).
+ *   hidden        bf16  [T, K]
+ *   topk_ids      int32 [T, topk]   (negative = padding, >= E = invalid, both skipped)
+ *   topk_weights  fp32  [T, topk]
+ *   w13/s13/w2/s2 packed weights and scales, layouts in the file header
+ *   out           bf16  [T, K]      written completely (zero for tokens with no valid route)
+ *   status        int32 [4]         may be NULL
+ *   workspace     device scratch of at least mxfp4_moe_workspace_size(T,K,I,E,topk)
+ *                 bytes, zero before first use (see above); not shared by
+ *                 calls that may run concurrently
+ *   path          0 = automatic (decode for T <= 32, else prefill),
+ *                 1 = decode kernels, 2 = prefill (tensor-core grouped GEMM)
+ * T == 0 returns MXFP4_MOE_OK and enqueues nothing. */
+int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                      const uint8_t* w13, const uint8_t* s13,
+                      const uint8_t* w2, const uint8_t* s2,
+                      int T, int K, int I, int E, int topk,
+                      void* out, int32_t* status,
+                      void* workspace, size_t workspace_bytes,
+                      int path, void* stream);
+
+/* Dequantise packed rows to bf16 ("MXFP4 MoE decode kernels", Prefill:
+ * mxk_deq unpacks an expert's MXFP4 weights straight to bf16).
+ *   packed uint8 [rows, cols/2], scale uint8 [rows, cols/32] -> out bf16 [rows, cols]
+ * Each value is E2M1(nibble) * 2^(s - 127) rounded once to bf16, which is
+ * exact except that products beyond the bf16 range become +-inf and the
+ * scale byte 255 gives NaN. cols % 32 == 0; out 4-byte aligned. */
+int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
+                      void* out, void* stream);
+
+/* Profiling hook: when events (host array of n cudaEvent_t handles, n >= 3)
+ * is non-NULL, each later forward call on this process records events[0]
+ * before its first kernel and events[i] after its i-th kernel, on its stream.
+ * Pass NULL to turn it off. Not thread-safe; meant for benchmarks. */
+void mxfp4_moe_set_phase_events(void* const* events, int n);
+
+/* Static description of an error code (never NULL). */
+const char* mxfp4_moe_strerror(int code);
+
+/* Library ABI version: 100 * major + minor. */
+int mxfp4_moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_MOE_H_ */

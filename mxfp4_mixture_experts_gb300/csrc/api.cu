@@ -1,0 +1,248 @@
+// Host side of the C ABI declared in include/mxfp4_moe.h: argument checks,
+// workspace layout and kernel dispatch. Nothing here allocates, frees or
+// synchronises; every call only enqueues work on the caller's stream.
+#include <cuda_runtime.h>
+#include <mutex>
+#include <stdint.h>
+
+#include "../../include/mxfp4_moe.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "prefill.h"
+
+namespace {
+
+using namespace mxmoe;
+
+constexpr int kDecodeMaxT = 32;
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool ok = false;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+void* const* g_phase_events = nullptr;
+int g_phase_n = 0;
+
+// Checks the current device once (sm_103) and caches its SM count.
+int current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXFP4_MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MXFP4_MOE_ERR_CUDA;
+    d.probed = true;
+    d.ok = (major == 10 && minor == 3);
+    d.num_sms = sms;
+  }
+  if (!d.ok) return MXFP4_MOE_ERR_DEVICE;
+  *out = &d;
+  return MXFP4_MOE_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
+
+// Workspace layout. The bookkeeping that must be zero between calls comes
+// first; the scratch regions after it are overwritten by every call.
+struct Layout {
+  size_t item_ctr1, item_ctr2, tile_ctr, pf_ctr;          // zero-kept
+  size_t parts1, parts2, h, P, rcount, roffset, rlist, xp, hp;   // scratch
+  size_t total;
+};
+
+bool shape_ok(int T, int K, int I, int E, int topk) {
+  if (T < 0 || K < 32 || I < 32 || K > 16384 || I > 16384) return false;
+  if (K % 32 || I % 32) return false;
+  if (E < 1 || E > kMaxExperts || topk < 1 || topk > 32 || topk > E) return false;
+  if ((int64_t)T * topk * (int64_t)K >= ((int64_t)1 << 31)) return false;
+  return true;
+}
+
+Layout layout(int T, int K, int I, int E, int topk) {
+  Layout L;
+  const size_t R = (size_t)T * topk;
+  const size_t warps = (size_t)kMaxCtas * kDecodeWarpsPerCta;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
+  L.item_ctr1 = take(warps * sizeof(int));
+  L.item_ctr2 = take(warps * sizeof(int));
+  L.tile_ctr = take((size_t)(K / 16) * sizeof(int));
+  L.pf_ctr = take(prefill_counter_bytes(T, K, I, E, topk));
+  L.parts1 = take(warps * 2 * 128 * sizeof(float));
+  L.parts2 = take(warps * 2 * 128 * sizeof(float));
+  L.h = take(R * I * 2);
+  L.P = take(R * K * sizeof(float));
+  L.rcount = take((size_t)E * sizeof(int));
+  L.roffset = take((size_t)(E + 1) * sizeof(int));
+  L.rlist = take(R * sizeof(int));
+  L.xp = take(R * K * 2);
+  L.hp = take(R * I * 2);
+  L.total = o;
+  return L;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MXFP4_MOE_OK : MXFP4_MOE_ERR_CUDA; }
+
+void record_phase(int i, cudaStream_t s) {
+  if (g_phase_events != nullptr && i < g_phase_n)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_phase_events[i]), s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp4_moe_workspace_size(int T, int K, int I, int E, int topk) {
+  if (!shape_ok(T, K, I, E, topk)) return 0;
+  return layout(T, K, I, E, topk).total;
+}
+
+int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E, int32_t* expert_count,
+                    int32_t* expert_offset, int32_t* route_list, int32_t* status, void* stream) {
+  if (T < 0 || topk < 1 || topk > 32 || E < 1 || E > kMaxExperts) return MXFP4_MOE_ERR_SHAPE;
+  if (expert_count == nullptr || expert_offset == nullptr) return MXFP4_MOE_ERR_ARG;
+  if (T > 0 && (topk_ids == nullptr || route_list == nullptr)) return MXFP4_MOE_ERR_ARG;
+  if ((int64_t)T * topk >= ((int64_t)1 << 30)) return MXFP4_MOE_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  return cuda_status(launch_route(topk_ids, T * topk, E, expert_count, expert_offset, route_list,
+                                  status, static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                      const uint8_t* w13, const uint8_t* s13, const uint8_t* w2,
+                      const uint8_t* s2, int T, int K, int I, int E, int topk, void* out,
+                      int32_t* status, void* workspace, size_t workspace_bytes, int path,
+                      void* stream) {
+  if (!shape_ok(T, K, I, E, topk)) return MXFP4_MOE_ERR_SHAPE;
+  if (path < 0 || path > 2) return MXFP4_MOE_ERR_ARG;
+  if (T == 0) return MXFP4_MOE_OK;
+  if (!hidden || !topk_ids || !topk_weights || !w13 || !s13 || !w2 || !s2 || !out)
+    return MXFP4_MOE_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(w2, 16))
+    return MXFP4_MOE_ERR_ALIGN;
+  if (workspace == nullptr) return MXFP4_MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MXFP4_MOE_ERR_ALIGN;
+  const Layout L = layout(T, K, I, E, topk);
+  if (workspace_bytes < L.total) return MXFP4_MOE_ERR_WORKSPACE;
+  const bool decode = path == 1 || (path == 0 && T <= kDecodeMaxT);
+  if (decode && (T > kDecodeMaxT || T * topk > kDecodeMaxRoutes)) return MXFP4_MOE_ERR_SHAPE;
+  if (!decode && (K % 64 || I % 64)) return MXFP4_MOE_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int ctas = d->num_sms < kMaxCtas ? d->num_sms : kMaxCtas;
+
+  if (decode) {
+    DecodeArgs a = {};
+    a.ids = topk_ids;
+    a.wts = topk_weights;
+    a.T = T;
+    a.K = K;
+    a.I = I;
+    a.E = E;
+    a.topk = topk;
+    a.h = reinterpret_cast<uint16_t*>(ws + L.h);
+    a.P = reinterpret_cast<float*>(ws + L.P);
+    a.y = static_cast<uint16_t*>(out);
+    a.tile_ctr = reinterpret_cast<int*>(ws + L.tile_ctr);
+    a.status = status;
+    record_phase(0, s);
+    DecodeArgs a1 = a;
+    a1.x = static_cast<const uint16_t*>(hidden);
+    a1.wq = w13;
+    a1.wsc = s13;
+    a1.parts = reinterpret_cast<float*>(ws + L.parts1);
+    a1.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr1);
+    cudaError_t e = launch_decode(a1, 1, ctas, s, g_phase_events == nullptr);
+    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
+    record_phase(1, s);
+    DecodeArgs a2 = a;
+    a2.x = a.h;
+    a2.wq = w2;
+    a2.wsc = s2;
+    a2.parts = reinterpret_cast<float*>(ws + L.parts2);
+    a2.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr2);
+    e = launch_decode(a2, 2, ctas, s, g_phase_events == nullptr);
+    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
+    record_phase(2, s);
+    return MXFP4_MOE_OK;
+  }
+
+  PrefillArgs p = {};
+  p.hidden = static_cast<const uint16_t*>(hidden);
+  p.ids = topk_ids;
+  p.wts = topk_weights;
+  p.w13 = w13;
+  p.s13 = s13;
+  p.w2 = w2;
+  p.s2 = s2;
+  p.T = T;
+  p.K = K;
+  p.I = I;
+  p.E = E;
+  p.topk = topk;
+  p.y = static_cast<uint16_t*>(out);
+  p.status = status;
+  p.count = reinterpret_cast<int32_t*>(ws + L.rcount);
+  p.offset = reinterpret_cast<int32_t*>(ws + L.roffset);
+  p.list = reinterpret_cast<int32_t*>(ws + L.rlist);
+  p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  p.hp = reinterpret_cast<uint16_t*>(ws + L.hp);
+  p.P = reinterpret_cast<float*>(ws + L.P);
+  p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
+  p.num_sms = d->num_sms;
+  return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));
+}
+
+int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
+                      void* stream) {
+  if (rows < 0 || cols < 0) return MXFP4_MOE_ERR_ARG;
+  if (cols % 32) return MXFP4_MOE_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return MXFP4_MOE_OK;
+  if (!packed || !scale || !out) return MXFP4_MOE_ERR_ARG;
+  if (!aligned(packed, 16) || !aligned(out, 4)) return MXFP4_MOE_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  return cuda_status(launch_dequant(packed, scale, rows, cols, static_cast<uint16_t*>(out),
+                                    d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+void mxfp4_moe_set_phase_events(void* const* events, int n) {
+  if (events == nullptr || n < 3) {
+    g_phase_events = nullptr;
+    g_phase_n = 0;
+  } else {
+    g_phase_events = events;
+    g_phase_n = n;
+  }
+}
+
+const char* mxfp4_moe_strerror(int code) {
+  switch (code) {
+    case MXFP4_MOE_OK: return "ok";
+    case MXFP4_MOE_ERR_ARG: return "invalid argument (null pointer, negative size or bad path)";
+    case MXFP4_MOE_ERR_SHAPE: return "unsupported shape (see the limits in mxfp4_moe.h)";
+    case MXFP4_MOE_ERR_ALIGN: return "pointer alignment rule violated";
+    case MXFP4_MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MXFP4_MOE_ERR_CUDA: return "CUDA runtime error";
+    case MXFP4_MOE_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown error code";
+  }
+}
+
+int mxfp4_moe_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,159 @@
+// Device helpers shared by the kernels of the MXFP4 MoE library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mxmoe {
+
+constexpr int kScaleBlock = 32;        // E2M1 values per E8M0 scale
+constexpr int kMaxExperts = 1024;
+constexpr int kDecodeMaxTokens = 32;
+constexpr int kDecodeMaxRoutes = 1024;
+
+// ---------------------------------------------------------------------------
+// Small PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Read-only streaming load of 16 bytes: the data is used once, so it is not
+// kept in L1; L2 fetches 256-byte lines to keep DRAM bursts long.
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// 16-byte load through L1 (small operands reused by many warps of an SM).
+__device__ __forceinline__ uint4 ldg16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 16-byte load that skips L1, for data other SMs wrote during this kernel.
+__device__ __forceinline__ uint4 ldcg16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ldcg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Programmatic dependent launch: wait for the grid this one depends on / let
+// the next grid in the stream begin launching.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Exact bf16x2 product (inputs and results may be subnormal).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  // fma with a -0 addend returns the rounded product, sign of zero included
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// ---------------------------------------------------------------------------
+// E2M1 -> bf16
+//
+// An E2M1 code s.e1e0.m (sign bit 3) has magnitude (1 + m/2) * 2^(e-1) for
+// e > 0 and m/2 for e = 0. Writing (e1, e0, m) into bits 8..6 of a bf16 gives
+// exponent field e and leading mantissa bit m, i.e. exactly magnitude *
+// 2^-126 -- including the two e = 0 codes, which land on bf16 subnormals --
+// and the sign goes to bit 15. One exact bf16 multiply by 2^126 * 2^(s-127)
+// then gives E2M1 * 2^(s-127).
+//
+// e2m1_pair_raw<P>(w) takes nibbles P and P+4 of the 32-bit word w (bits
+// 4P..4P+3 and 4P+16..4P+19, which sit 16 bits apart) into the low and high
+// bf16 of the result.
+// ---------------------------------------------------------------------------
+template <int P>
+__device__ __forceinline__ uint32_t e2m1_pair_raw(uint32_t w) {
+  static_assert(P >= 0 && P < 4, "pair index");
+  constexpr int kMagShift = 6 - 4 * P;     // bits 4P..4P+2 -> 6..8
+  constexpr int kSignShift = 12 - 4 * P;   // bit 4P+3 -> 15
+  const uint32_t mag = kMagShift >= 0 ? (w << kMagShift) : (w >> (-kMagShift));
+  const uint32_t sgn = w << kSignShift;
+  return (mag & 0x01C001C0u) | (sgn & 0x80008000u);
+}
+
+// Multiplier pair for one E8M0 scale byte s. For s <= 128 a single exact
+// multiply by 2^(s-1) turns a raw pair into E2M1 * 2^(s-127). Larger bytes
+// need two steps (2^126, then 2^(s-127)); 255 is NaN.
+struct ScaleMul {
+  uint32_t m1;    // bf16x2
+  uint32_t m2;    // bf16x2, only used when two == true
+  bool two;
+};
+
+__device__ __forceinline__ ScaleMul scale_mul(uint32_t s) {
+  ScaleMul r;
+  if (s <= 128u) {
+    const uint32_t b = (s + 126u) << 7;            // bf16 bits of 2^(s-1)
+    r.m1 = b | (b << 16);
+    r.m2 = 0;
+    r.two = false;
+  } else {
+    r.m1 = 0x7E807E80u;                            // 2^126
+    const uint32_t b = (s == 255u) ? 0x7FC0u : (s << 7);   // 2^(s-127) or NaN
+    r.m2 = b | (b << 16);
+    r.two = true;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm) {
+  uint32_t v = bf16x2_mul(raw, sm.m1);
+  if (__builtin_expect(sm.two, 0)) v = bf16x2_mul(v, sm.m2);
+  return v;
+}
+
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+
+}  // namespace mxmoe

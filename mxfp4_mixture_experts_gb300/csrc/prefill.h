@@ -1,0 +1,34 @@
+// Prefill path (many tokens): route -> gather -> grouped GEMM1 (+SwiGLU) ->
+// grouped GEMM2 (+routing weight) -> slot-order combine.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mxmoe {
+
+struct PrefillArgs {
+  const uint16_t* hidden;   // bf16 [T, K]
+  const int32_t* ids;       // [T * topk]
+  const float* wts;         // [T * topk]
+  const uint8_t *w13, *s13, *w2, *s2;
+  int T, K, I, E, topk;
+  uint16_t* y;              // bf16 [T, K]
+  int32_t* status;
+  // workspace regions
+  int32_t* count;           // [E]
+  int32_t* offset;          // [E+1]
+  int32_t* list;            // [R]
+  uint16_t* xp;             // bf16 [R, K], rows in expert order
+  uint16_t* hp;             // bf16 [R, I], rows in expert order
+  float* P;                 // fp32 [R, K], rows in route order
+  int* counters;            // zero-kept scheduler counters
+  int num_sms;
+};
+
+size_t prefill_counter_bytes(int T, int K, int I, int E, int topk);
+cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, void* const* phase_events,
+                           int n_events);
+
+}  // namespace mxmoe

@@ -1,0 +1,120 @@
+// Standalone routing / permute kernel: stable counting sort of any number of
+// routes by expert, one 1024-thread CTA. Each warp owns a contiguous segment
+// of the routes; per-segment counts give every (segment, expert) its base, so
+// the placement pass runs in all 32 warps at once and stays in route order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxmoe {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+route_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ count,
+             int32_t* __restrict__ offset, int32_t* __restrict__ list, int32_t* status) {
+  extern __shared__ int sm[];
+  int* seg = sm;                        // [32][E] per-segment counts, then bases
+  int* off = seg + kRouteWarps * E;     // [E+1]
+  __shared__ int s_inv, s_nd;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = lanemask_lt();
+
+  grid_dependency_wait();
+  for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) seg[i] = 0;
+  if (tid == 0) s_inv = 0;
+  __syncthreads();
+
+  const int rb = (int)((int64_t)R * warp / kRouteWarps);
+  const int re = (int)((int64_t)R * (warp + 1) / kRouteWarps);
+  int* myseg = seg + warp * E;
+  int inv = 0;
+  for (int base = rb; base < re; base += 32) {
+    const int r = base + lane;
+    const int e = r < re ? ids[r] : -1;
+    const bool ok = e >= 0 && e < E;
+    if (r < re && e >= E) ++inv;
+    const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+    if (ok && (grp & lt) == 0) myseg[e] += __popc(grp);
+    __syncwarp();
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) inv += __shfl_xor_sync(0xffffffffu, inv, o);
+  if (lane == 0 && inv) atomicAdd(&s_inv, inv);
+  __syncthreads();
+
+  // per expert: exclusive prefix over segments, total in off[e] (temporarily)
+  for (int e = tid; e < E; e += kRouteThreads) {
+    int run = 0;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int c = seg[w * E + e];
+      seg[w * E + e] = run;
+      run += c;
+    }
+    off[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0, nd = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? off[e] : 0;
+      int x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (e < E) {
+        count[e] = c;
+        off[e] = carry + x - c;
+      }
+      carry += __shfl_sync(0xffffffffu, x, 31);
+      nd += __popc(__ballot_sync(0xffffffffu, c > 0));
+    }
+    if (lane == 0) {
+      off[E] = carry;
+      s_nd = nd;
+    }
+  }
+  __syncthreads();
+
+  for (int base = rb; base < re; base += 32) {
+    const int r = base + lane;
+    const int e = r < re ? ids[r] : -1;
+    const bool ok = e >= 0 && e < E;
+    const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : E + lane);
+    const int rank = __popc(grp & lt);
+    const int before = ok ? myseg[e] : 0;
+    __syncwarp();
+    if (ok) {
+      list[off[e] + before + rank] = r;
+      if (rank == 0) myseg[e] = before + __popc(grp);
+    }
+    __syncwarp();
+  }
+  for (int e = tid; e <= E; e += kRouteThreads) offset[e] = off[e];
+  for (int p = off[E] + tid; p < R; p += kRouteThreads) list[p] = -1;
+  if (tid == 0 && status != nullptr) {
+    status[0] = s_inv;
+    status[1] = s_nd;
+    status[2] = 0;
+    status[3] = 0;
+  }
+}
+
+cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
+                         int32_t* list, int32_t* status, cudaStream_t stream) {
+  static size_t granted = 48 * 1024;
+  const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + E + 1);
+  if (smem > granted) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    granted = smem;
+  }
+  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, count, offset, list, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mxmoe

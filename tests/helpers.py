@@ -1,0 +1,56 @@
+"""Test helpers: seeded cases on the device, oracle calls on host copies,
+and the comparison metrics (no arithmetic of the layer itself)."""
+import numpy as np
+import torch
+
+from mxfp4_mixture_experts_gb300 import synth
+from oracle import mxfp4_moe_oracle as O
+
+TOL_REL_L2 = 3e-3   # output gate, rel_l2 over the compared rows, vs both oracle modes
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / den) if den > 0 else float(np.linalg.norm(got))
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def oracle_rows(case: synth.Case, tokens=None, intermediate="bf16"):
+    """Oracle output rows for `tokens` (all if None). Only the experts those
+    tokens use are copied to the host, relabelled 0..n-1 (the oracle is pinned
+    invariant under expert relabelling); padding stays -1 and ids >= E stay
+    invalid."""
+    ids = case.topk_ids.cpu().numpy().astype(np.int64)
+    tok = np.arange(ids.shape[0]) if tokens is None else np.asarray(tokens)
+    sub = ids[tok]
+    E = case.shape.E
+    valid = (sub >= 0) & (sub < E)
+    used = np.unique(sub[valid])
+    n_e = max(len(used), 1)
+    remap = np.full(E, -1, dtype=np.int64)
+    remap[used] = np.arange(len(used))
+    sub_ids = np.where(valid, remap[np.clip(sub, 0, E - 1)], np.where(sub >= E, n_e, -1))
+    if len(used):
+        idx = torch.as_tensor(used, dtype=torch.long)
+        pick = lambda w: w.index_select(0, idx.to(w.device)).cpu().numpy()
+    else:
+        pick = lambda w: np.zeros((1,) + tuple(w.shape[1:]), dtype=np.uint8)
+    w13, s13, w2, s2 = pick(case.w13), pick(case.s13), pick(case.w2), pick(case.s2)
+    hb = case.hidden.cpu().view(torch.int16).numpy().view(np.uint16)[tok]
+    wts = case.topk_weights.cpu().numpy()[tok]
+    return O.forward(hb, sub_ids, wts, w13, s13, w2, s2, intermediate=intermediate)
+
+
+def compare(y_gpu: torch.Tensor, case: synth.Case, tokens=None):
+    """(rel_l2 vs bf16-intermediate oracle, rel_l2 vs fp32-intermediate, max abs err)."""
+    got = bf16_to_f64(y_gpu)
+    if tokens is not None:
+        got = got[np.asarray(tokens)]
+    ref_a = oracle_rows(case, tokens, "bf16")
+    ref_b = oracle_rows(case, tokens, "fp32")
+    return rel_l2(got, ref_a), rel_l2(got, ref_b), float(np.abs(got - ref_a).max())

@@ -1,0 +1,122 @@
+"""The C-ABI library loads, exports what include/mxfp4_moe.h declares, and
+rejects bad arguments on the host before touching the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4_moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_mixture_experts_gb300 import moe
+    return moe.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mxfp4_moe_route", "mxfp4_moe_forward", "mxfp4_moe_dequant",
+              "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from mxfp4_mixture_experts_gb300 import moe
+    out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", out))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(L, n)
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    c = tmp_path / "t.c"
+    c.write_text('#include "mxfp4_moe.h"\nint main(void){return mxfp4_moe_version()>0?0:1;}\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", "-I", os.path.dirname(HEADER),
+                        str(c), "-o", str(tmp_path / "t.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_version_and_strerror(L):
+    from mxfp4_mixture_experts_gb300 import moe
+    assert moe.version() == 100
+    for code in range(7):
+        assert len(moe.strerror(code)) > 0
+    assert moe.strerror(99) == "unknown error code"
+
+
+def test_workspace_size(L):
+    from mxfp4_mixture_experts_gb300 import moe
+    a = moe.workspace_size(32, 2880, 2880, 128, 4)
+    b = moe.workspace_size(1, 2880, 2880, 128, 4)
+    assert a > b > 0
+    assert a % 256 == 0
+    assert moe.workspace_size(1, 2881, 2880, 128, 4) == 0      # K not a multiple of 32
+    assert moe.workspace_size(1, 2880, 2880, 2048, 4) == 0     # E above the limit
+    assert moe.workspace_size(1, 2880, 2880, 8, 9) == 0        # topk > E
+    assert moe.workspace_size(-1, 2880, 2880, 8, 2) == 0
+
+
+VP = ctypes.c_void_p
+
+
+def fwd(L, **kw):
+    a = dict(hidden=VP(0x10000), ids=VP(0x20000), wts=VP(0x30000), w13=VP(0x40000),
+             s13=VP(0x50000), w2=VP(0x60000), s2=VP(0x70000), T=4, K=64, I=64, E=4, topk=2,
+             out=VP(0x80000), status=None, ws=VP(0x100000), ws_bytes=1 << 40, path=1,
+             stream=None)
+    a.update(kw)
+    return L.mxfp4_moe_forward(a["hidden"], a["ids"], a["wts"], a["w13"], a["s13"], a["w2"],
+                               a["s2"], a["T"], a["K"], a["I"], a["E"], a["topk"], a["out"],
+                               a["status"], a["ws"], a["ws_bytes"], a["path"], a["stream"])
+
+
+def test_forward_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    assert fwd(L, hidden=None) == m.ERR_ARG
+    assert fwd(L, w2=None) == m.ERR_ARG
+    assert fwd(L, out=None) == m.ERR_ARG
+    assert fwd(L, path=3) == m.ERR_ARG
+    assert fwd(L, K=65) == m.ERR_SHAPE
+    assert fwd(L, I=48) == m.ERR_SHAPE
+    assert fwd(L, topk=0) == m.ERR_SHAPE
+    assert fwd(L, topk=5) == m.ERR_SHAPE          # topk > E
+    assert fwd(L, E=0) == m.ERR_SHAPE
+    assert fwd(L, T=-1) == m.ERR_SHAPE
+    assert fwd(L, T=33, path=1) == m.ERR_SHAPE    # decode limited to 32 tokens
+    assert fwd(L, K=96, I=96, T=40, path=2) == m.ERR_SHAPE   # prefill needs multiples of 64
+    assert fwd(L, hidden=VP(0x10008)) == m.ERR_ALIGN
+    assert fwd(L, w13=VP(0x40004)) == m.ERR_ALIGN
+    assert fwd(L, out=VP(0x80002)) == m.ERR_ALIGN
+    assert fwd(L, ws=VP(0x100080)) == m.ERR_ALIGN
+    assert fwd(L, ws=None) == m.ERR_WORKSPACE
+    need = L.mxfp4_moe_workspace_size(4, 64, 64, 4, 2)
+    assert fwd(L, ws_bytes=need - 1) == m.ERR_WORKSPACE
+    assert fwd(L, T=0) == m.OK                    # nothing to do, nothing enqueued
+
+
+def test_route_and_dequant_reject_bad_arguments(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    r = L.mxfp4_moe_route(VP(0x1000), 4, 0, 8, VP(0x2000), VP(0x3000), VP(0x4000), None, None)
+    assert r == m.ERR_SHAPE
+    r = L.mxfp4_moe_route(VP(0x1000), 4, 2, 8, None, VP(0x3000), VP(0x4000), None, None)
+    assert r == m.ERR_ARG
+    r = L.mxfp4_moe_route(None, 4, 2, 8, VP(0x2000), VP(0x3000), VP(0x4000), None, None)
+    assert r == m.ERR_ARG
+    assert L.mxfp4_moe_dequant(VP(0x1000), VP(0x2000), 4, 48, VP(0x3000), None) == m.ERR_SHAPE
+    assert L.mxfp4_moe_dequant(VP(0x1008), VP(0x2000), 4, 64, VP(0x3000), None) == m.ERR_ALIGN
+    assert L.mxfp4_moe_dequant(None, VP(0x2000), 4, 64, VP(0x3000), None) == m.ERR_ARG
+    assert L.mxfp4_moe_dequant(VP(0x1000), VP(0x2000), 0, 64, VP(0x3000), None) == m.OK

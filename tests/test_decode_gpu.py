@@ -1,0 +1,171 @@
+"""Decode path (1..32 tokens) vs the CPU oracle.
+
+Small shapes span several row tiles, a ragged k-step and several stream-K
+splits, and are compared on every output element; the four workload shapes
+are run at full size (the launch configuration the benchmark times) and
+compared on sampled tokens the oracle computes one by one, plus properties
+that hold at any size (touched-expert count, finiteness)."""
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_mixture_experts_gb300 import synth
+from helpers import TOL_REL_L2, compare, bf16_to_f64, oracle_rows, rel_l2
+from oracle import mxfp4_moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_mixture_experts_gb300 import moe
+    return moe
+
+
+def run(moe, case, path=1, workspace=None, status=None):
+    g = case.to("cuda")
+    y = moe.forward(g.hidden, g.topk_ids, g.topk_weights, g.w13, g.s13, g.w2, g.s2,
+                    workspace=workspace, status=status, path=path)
+    torch.cuda.synchronize()
+    return y
+
+
+def assert_close(y, case, tokens=None):
+    ra, rb, mx = compare(y, case, tokens)
+    assert ra <= TOL_REL_L2 and rb <= TOL_REL_L2, (ra, rb, mx)
+    return ra, rb, mx
+
+
+SMALL = synth.custom_shape(K=320, I=96, E=8, topk=3, name="small")   # 10 k-blocks: ragged step
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 9, 17, 32])
+def test_small_all_elements(moe, T):
+    case = synth.make_case(SMALL, T, seed=T)
+    y = run(moe, case)
+    assert_close(y, case)
+
+
+@pytest.mark.parametrize("K,I,E,k", [(32, 32, 2, 1), (64, 64, 4, 4), (2880, 2880, 3, 2),
+                                     (7168, 64, 5, 3), (96, 2048, 6, 2)])
+def test_shapes_all_elements(moe, K, I, E, k):
+    shape = synth.custom_shape(K=K, I=I, E=E, topk=k)
+    case = synth.make_case(shape, 3, seed=K + I)
+    assert_close(run(moe, case), case)
+
+
+def test_hot_routing_many_token_groups(moe):
+    """Every token on the same experts: 32 tokens per expert = 4 token groups."""
+    case = synth.make_case(SMALL, 32, seed=11)
+    ids, w = synth.hot_routing(32, SMALL.topk, SMALL.E, first=2)
+    case.topk_ids, case.topk_weights = torch.from_numpy(ids), torch.from_numpy(w)
+    assert_close(run(moe, case), case)
+
+
+def test_padding_invalid_and_duplicates(moe):
+    case = synth.make_case(SMALL, 6, seed=12)
+    ids = case.topk_ids.clone()
+    ids[0, 1] = -1          # padding
+    ids[1, :] = -1          # a token with no route at all -> zero row
+    ids[2, 2] = 99          # invalid: counted, skipped
+    ids[3, 1] = ids[3, 0]   # the same expert twice for one token
+    case.topk_ids = ids
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    y = run(moe, case, status=status)
+    assert int(status[0]) == 1
+    assert torch.all(y[1] == 0)
+    rt = O.route(ids.numpy(), SMALL.E)
+    assert int(status[1]) == len(rt["touched"])
+    assert_close(y, case)
+
+
+def test_nothing_routed_gives_zeros(moe):
+    case = synth.make_case(SMALL, 4, seed=13)
+    case.topk_ids = torch.full_like(case.topk_ids, -1)
+    y = run(moe, case)
+    assert torch.all(y == 0)
+
+
+def test_wide_scale_range(moe):
+    """Scale bytes from 100 to 140 (outputs spanning ~12 orders of magnitude
+    per block), so the exact scale multiply matters."""
+    case = synth.make_case(SMALL, 5, seed=14)
+    gen = torch.Generator().manual_seed(5)
+    for name in ("s13", "s2"):
+        t = getattr(case, name)
+        setattr(case, name, torch.randint(100, 141, t.shape, generator=gen, dtype=torch.uint8))
+    assert_close(run(moe, case), case)
+
+
+def test_scale_255_is_nan(moe):
+    case = synth.make_case(SMALL, 2, seed=15)
+    e = int(case.topk_ids[0, 0])
+    case.s2 = case.s2.clone()
+    case.s2[e, 7, 0] = 255           # one w2 block of expert e -> NaN in output row 7
+    y = run(moe, case)
+    assert torch.isnan(y[0, 7]).item()
+    assert not torch.isnan(y[0, 8]).item()
+
+
+def test_deterministic_and_chain_independent(moe):
+    case = synth.make_case(SMALL, 17, seed=16)
+    other = synth.make_case(SMALL, 9, seed=17)
+    ws = moe.new_workspace(32, SMALL.K, SMALL.I, SMALL.E, SMALL.topk)
+    y1 = run(moe, case, workspace=ws).clone()
+    run(moe, other, workspace=ws)
+    y2 = run(moe, case, workspace=ws).clone()
+    y3 = run(moe, case, workspace=ws).clone()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+
+
+def test_negative_control_swapped_gate_up(moe):
+    """The test has power: feeding [up; gate] instead of [gate; up] fails the
+    gate by far on the workloads' statistics."""
+    case = synth.make_case(synth.custom_shape(512, 256, 4, 2), 4, seed=18)
+    I = 256
+    sw = synth.Case(case.shape, case.T, case.hidden, case.topk_ids, case.topk_weights,
+                    torch.cat([case.w13[:, I:], case.w13[:, :I]], 1).contiguous(),
+                    torch.cat([case.s13[:, I:], case.s13[:, :I]], 1).contiguous(),
+                    case.w2, case.s2, case.logits)
+    y = run(moe, sw)
+    ra, _, _ = compare(y, case)
+    assert ra > 0.1
+
+
+FULL = [("single32", 1), ("gptoss128", 1), ("gptoss128", 4), ("gptoss128", 16),
+        ("gptoss128", 32), ("glm256", 1), ("glm256", 8), ("glm256", 32), ("widek256", 1),
+        ("widek256", 2), ("widek256", 4), ("widek256", 8), ("widek256", 16), ("widek256", 32)]
+
+
+@pytest.fixture(scope="module")
+def full_weights():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            cache[name] = synth.draw_weights_cuda(synth.SHAPES[name], seed=0, layer=0)
+        return cache[name]
+    yield get
+    cache.clear()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,T", FULL)
+def test_full_size_sampled_tokens(moe, full_weights, name, T):
+    shape = synth.SHAPES[name]
+    rng = np.random.default_rng(0)
+    hidden, logits, ids, w = synth.draw_activations(shape, T, np.random.Generator(np.random.PCG64(T)))
+    w13, s13, w2, s2 = full_weights(name)
+    case = synth.Case(shape, T, hidden, ids, w, w13, s13, w2, s2, logits)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    y = run(moe, case, status=status)
+    assert torch.isfinite(y).all()
+    rt = O.route(ids.numpy(), shape.E)
+    assert int(status[1]) == len(rt["touched"]) and int(status[0]) == 0
+    tokens = sorted({0, T - 1})
+    assert_close(y, case, tokens)
