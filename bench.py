@@ -439,6 +439,27 @@ def run_reference(args, dist: Dist):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """`--profile-case NAME:T`: warm-up + steps forward calls of one layer of a
+    workload, no timing; the command profilers (ncu) run."""
+    from mxfp4_mixture_experts_gb300 import moe
+    name, T = args.profile_case.split(":")
+    T = int(T)
+    shape = synth.SHAPES[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hidden, _, ids, w = synth.draw_activations(shape, T, np.random.Generator(np.random.PCG64(T)))
+    w13, s13, w2, s2 = synth.draw_weights_cuda(shape, seed=0, layer=0, device=dev)
+    hidden, ids, w = hidden.to(dev), ids.to(dev), w.to(dev)
+    ws = moe.new_workspace(T, shape.K, shape.I, shape.E, shape.topk, dev)
+    out = torch.empty(T, shape.K, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup + args.steps):
+        moe.forward(hidden, ids, w, w13, s13, w2, s2, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "calls": args.warmup + args.steps,
+                      "touched_experts": touched_experts(ids, shape.E)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,7 +468,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gptoss128", choices=["gptoss128", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None,
+                    help="NAME:T -- run warmup+steps calls of one layer, untimed (for ncu)")
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     dist = Dist()

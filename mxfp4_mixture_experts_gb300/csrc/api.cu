@@ -21,6 +21,7 @@ struct DeviceInfo {
   bool probed = false;
   bool ok = false;
   int num_sms = 0;
+  int max_smem = 0;   // opt-in dynamic shared memory per block
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -35,14 +36,16 @@ int current_device(DeviceInfo** out) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceInfo& d = g_dev[dev];
   if (!d.probed) {
-    int major = 0, minor = 0, sms = 0;
+    int major = 0, minor = 0, sms = 0, smem = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
       return MXFP4_MOE_ERR_CUDA;
     d.probed = true;
     d.ok = (major == 10 && minor == 3);
     d.num_sms = sms;
+    d.max_smem = smem;
   }
   if (!d.ok) return MXFP4_MOE_ERR_DEVICE;
   *out = &d;
@@ -159,6 +162,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a.y = static_cast<uint16_t*>(out);
     a.tile_ctr = reinterpret_cast<int*>(ws + L.tile_ctr);
     a.status = status;
+    a.smem_bytes = (size_t)d->max_smem;
     record_phase(0, s);
     DecodeArgs a1 = a;
     a1.x = static_cast<const uint16_t*>(hidden);

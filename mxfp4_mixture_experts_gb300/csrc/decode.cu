@@ -53,6 +53,9 @@ struct DecodeCtx {
   RouteTables tb;
   const int* gbase;   // [nD+1] token-group prefix over touched experts
   int nD, NT, S, nblk, rows_per_e, row_bytes, G;
+  // activation rows staged in shared memory: list positions [p_lo, p_lo + nrows)
+  const char* stage;
+  int p_lo, nrows, stage_stride;
 };
 
 __device__ __forceinline__ void cursor_load_expert(Cursor& c, const DecodeCtx& x) {
@@ -139,27 +142,68 @@ __device__ __forceinline__ void load_slot(Slot& sl, const Cursor& c, const Decod
   }
 }
 
-// B source row (bf16) for token column g of the item, or null when the column
-// is padding.
+// Pairs of one 16-byte chunk of 8 consecutive activations x[8i..8i+7]:
+// (x[8i+p], x[8i+p+4]) for p = 0..3, matching e2m1_pair_raw<p> of word i.
+__device__ __forceinline__ uint4 chunk_to_pairs(uint4 v) {
+  return make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
+                    prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+}
+
+// Global source row of list position p (a token row of hidden, or a route row of h).
 template <int PHASE>
-__device__ __forceinline__ const uint16_t* b_row(const Cursor& c, const DecodeCtx& x, int g) {
+__device__ __forceinline__ const uint16_t* src_row(const DecodeCtx& x, int p) {
   const DecodeArgs& a = *x.a;
-  const int j = c.gr * kGroup + g;
-  if (j >= x.tb.cnt[c.e]) return nullptr;
-  const int r = x.tb.lst[x.tb.off[c.e] + j];
+  const int r = x.tb.lst[p];
   if (PHASE == 1) return a.x + (int64_t)(r / a.topk) * a.K;
   return a.x + (int64_t)r * a.I;
+}
+
+// Shared-memory layout of a staged row: block b (32 values) takes 64 bytes,
+// its 16-byte chunk i (pairs of x[32b+8i .. 32b+8i+7]) sits at position
+// i ^ (b & 3), so the four lanes of a quad (consecutive blocks) and two quads
+// (row stride = 64 mod 128 bytes) hit distinct banks.
+__device__ __forceinline__ int stage_offset(int b, int i) { return b * 64 + ((i ^ (b & 3)) << 4); }
+
+// B fragment pairs of token column g for block b, in [word i][pair p] order.
+template <int PHASE>
+__device__ __forceinline__ void load_b(uint32_t (&bp)[16], const Cursor& c, const DecodeCtx& x,
+                                       int g, int b) {
+  const int j = c.gr * kGroup + g;
+  if (b < x.nblk && j < x.tb.cnt[c.e]) {
+    const int p = x.tb.off[c.e] + j;
+    const int idx = p - x.p_lo;
+    if (idx >= 0 && idx < x.nrows) {
+      const char* row = x.stage + (size_t)idx * x.stage_stride;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + stage_offset(b, i));
+        bp[4 * i + 0] = v.x;
+        bp[4 * i + 1] = v.y;
+        bp[4 * i + 2] = v.z;
+        bp[4 * i + 3] = v.w;
+      }
+    } else {
+      // row not staged (shared memory full): read it from L2 and permute here
+      const uint4* src = reinterpret_cast<const uint4*>(src_row<PHASE>(x, p) + b * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = chunk_to_pairs(ldcg16(src + i));
+        bp[4 * i + 0] = v.x;
+        bp[4 * i + 1] = v.y;
+        bp[4 * i + 2] = v.z;
+        bp[4 * i + 3] = v.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q) bp[q] = 0;
+  }
 }
 
 template <int WI>
 __device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wa, uint32_t wb,
                                          const ScaleMul& ma, const ScaleMul& mb,
-                                         const uint32_t (&xw)[16]) {
-  // B pairs of word WI: (x[8WI+p], x[8WI+p+4]) for p = 0..3
-  const uint32_t b0 = prmt(xw[4 * WI + 0], xw[4 * WI + 2], 0x5410u);
-  const uint32_t b1 = prmt(xw[4 * WI + 0], xw[4 * WI + 2], 0x7632u);
-  const uint32_t b2 = prmt(xw[4 * WI + 1], xw[4 * WI + 3], 0x5410u);
-  const uint32_t b3 = prmt(xw[4 * WI + 1], xw[4 * WI + 3], 0x7632u);
+                                         const uint32_t (&bp)[16]) {
   const uint32_t a0 = apply_scale(e2m1_pair_raw<0>(wa), ma);
   const uint32_t a1 = apply_scale(e2m1_pair_raw<1>(wa), ma);
   const uint32_t a2 = apply_scale(e2m1_pair_raw<2>(wa), ma);
@@ -169,37 +213,20 @@ __device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wa, uint32_t 
   const uint32_t c2 = apply_scale(e2m1_pair_raw<2>(wb), mb);
   const uint32_t c3 = apply_scale(e2m1_pair_raw<3>(wb), mb);
   // A rows: g -> word wa, g+8 -> word wb; logical k (2t,2t+1) then (2t+8,2t+9)
-  mma_bf16_16816(acc, a0, c0, a1, c1, b0, b1);
-  mma_bf16_16816(acc, a2, c2, a3, c3, b2, b3);
+  mma_bf16_16816(acc, a0, c0, a1, c1, bp[4 * WI + 0], bp[4 * WI + 1]);
+  mma_bf16_16816(acc, a2, c2, a3, c3, bp[4 * WI + 2], bp[4 * WI + 3]);
 }
 
 template <int PHASE>
 __device__ __forceinline__ void compute_step(float (&acc)[4], const Slot& sl, const Cursor& c,
                                              const DecodeCtx& x, int g, int t) {
-  const int b = c.s * 4 + t;
-  uint32_t xw[16];
-  const uint16_t* src = (b < x.nblk) ? b_row<PHASE>(c, x, g) : nullptr;
-  if (src != nullptr) {
-    const uint4* p = reinterpret_cast<const uint4*>(src + b * 32);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      // x / h rows may have been written by the kernel this one waited on:
-      // read them through L2 only.
-      const uint4 v = ldcg16(p + q);
-      xw[4 * q + 0] = v.x;
-      xw[4 * q + 1] = v.y;
-      xw[4 * q + 2] = v.z;
-      xw[4 * q + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) xw[q] = 0;
-  }
+  uint32_t bp[16];
+  load_b<PHASE>(bp, c, x, g, c.s * 4 + t);
   const ScaleMul ma = scale_mul(sl.s0), mb = scale_mul(sl.s1);
-  mma_word<0>(acc, sl.w0.x, sl.w1.x, ma, mb, xw);
-  mma_word<1>(acc, sl.w0.y, sl.w1.y, ma, mb, xw);
-  mma_word<2>(acc, sl.w0.z, sl.w1.z, ma, mb, xw);
-  mma_word<3>(acc, sl.w0.w, sl.w1.w, ma, mb, xw);
+  mma_word<0>(acc, sl.w0.x, sl.w1.x, ma, mb, bp);
+  mma_word<1>(acc, sl.w0.y, sl.w1.y, ma, mb, bp);
+  mma_word<2>(acc, sl.w0.z, sl.w1.z, ma, mb, bp);
+  mma_word<3>(acc, sl.w0.w, sl.w1.w, ma, mb, bp);
 }
 
 // Balanced split of U units over NW warps: warp v gets q = U / NW units plus
@@ -353,15 +380,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   const int g = lane >> 2, t = lane & 3;
   const int NW = gridDim.x * kDecWarps;
   const int v = blockIdx.x * kDecWarps + warp;
+  const int64_t cta_ub = range_begin(blockIdx.x * kDecWarps, U, NW);
+  const int64_t cta_ue = range_begin((blockIdx.x + 1) * kDecWarps, U, NW);
+  if (cta_ub >= cta_ue) return;     // the whole CTA has no work (U < number of warps)
   const int64_t ub = range_begin(v, U, NW);
   const int64_t ue = range_begin(v + 1, U, NW);
-  if (ub >= ue) {
-    if (PHASE == 2) grid_dependency_wait();
-    return;
+
+  // Activation rows this CTA can need: every route of the touched experts its
+  // unit range covers (a contiguous stretch of the route list).
+  {
+    const Cursor c0 = cursor_at(cta_ub, x);
+    const Cursor c1 = cursor_at(cta_ue - 1, x);
+    const int e0 = tb.touched[c0.d], e1 = tb.touched[c1.d];
+    x.p_lo = tb.off[e0];
+    const int need = tb.off[e1] + tb.cnt[e1] - x.p_lo;
+    x.stage_stride = ((kred * 2 + 127) / 128) * 128 + 64;
+    const size_t tables = decode_smem_bytes(a.T, a.topk, E);
+    const size_t stage_at = (tables + 127) / 128 * 128;
+    x.stage = reinterpret_cast<const char*>(smem) + stage_at;
+    const int fit = (int)((a.smem_bytes - stage_at) / x.stage_stride);
+    x.nrows = need < fit ? need : fit;
   }
 
-  Cursor lc = cursor_at(ub, x);    // loader
-  Cursor cc = lc;                  // consumer
+  Cursor lc = ub < ue ? cursor_at(ub, x) : cursor_at(cta_ub, x);    // loader
+  Cursor cc = lc;                                                    // consumer
   Slot ring[kPrefetch];
 #pragma unroll
   for (int q = 0; q < kPrefetch; ++q) {
@@ -371,6 +413,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
     }
   }
   if (PHASE == 2) grid_dependency_wait();   // h is ready from here on
+
+  // stage: 16-byte chunks, permuted into MMA pair order
+  {
+    char* st = const_cast<char*>(x.stage);
+    const int chunks = kred / 8;
+    const int total = x.nrows * chunks;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int row = i / chunks, c16 = i - row * chunks;
+      const uint4 v4 = ldcg16(src_row<PHASE>(x, x.p_lo + row) + c16 * 8);
+      *reinterpret_cast<uint4*>(st + (size_t)row * x.stage_stride + stage_offset(c16 >> 2, c16 & 3)) =
+          chunk_to_pairs(v4);
+    }
+  }
+  __syncthreads();
+  if (ub >= ue) return;
 
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   bool seg_from_start = (cc.s == 0);   // current segment began at step 0 of its item
@@ -431,11 +488,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_con
   }
 }
 
-size_t decode_smem_bytes(int T, int topk, int E) {
-  const int R = T * topk;
-  return sizeof(int) * (size_t)(E /*cnt*/ + (E + 1) /*off*/ + E /*run*/ + E /*touched*/ + R /*lst*/ +
-                                4 /*misc*/ + (E + 1) /*gbase*/);
-}
 
 // Raises a kernel's dynamic shared-memory limit only when a launch needs more
 // than was granted before (per process; one device per process is assumed for
@@ -451,7 +503,7 @@ static cudaError_t ensure_smem(K kernel, size_t bytes, size_t& granted) {
 cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, cudaStream_t stream,
                           bool pdl) {
   static size_t granted1 = 0, granted2 = 0;
-  const size_t smem = decode_smem_bytes(a.T, a.topk, a.E);
+  const size_t smem = a.smem_bytes;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(kDecThreads);

@@ -22,12 +22,19 @@ struct DecodeArgs {
   int* item_ctr;          // [warps], zero between calls
   int* tile_ctr;          // [K / 16], zero between calls (phase 2)
   int32_t* status;        // [4] or null (phase 1 writes it)
+  size_t smem_bytes;      // dynamic shared memory of the launch (tables + staged rows)
 };
 
 constexpr int kDecodeWarpsPerCta = 16;
 constexpr int kMaxCtas = 256;            // grid cap; sizes the stream-K bookkeeping
 
-size_t decode_smem_bytes(int T, int topk, int E);
+// Shared-memory routing tables of a decode CTA (the staged activation rows
+// follow them, 128-byte aligned).
+__host__ __device__ inline size_t decode_smem_bytes(int T, int topk, int E) {
+  const int R = T * topk;
+  return sizeof(int) * (size_t)(E /*cnt*/ + (E + 1) /*off*/ + E /*run*/ + E /*touched*/ +
+                                R /*lst*/ + 4 /*misc*/ + (E + 1) /*gbase*/);
+}
 cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, cudaStream_t stream,
                           bool pdl);
 
