@@ -59,10 +59,10 @@ typedef enum {
 /* Shape limits (checked on the host, MXFP4_MOE_ERR_SHAPE otherwise):
  *   K % 32 == 0, I % 32 == 0, 32 <= K, I <= 16384
  *   1 <= E <= 1024, 1 <= topk <= 32, topk <= E, 0 <= T
- *   decode path: T <= 32 and T * topk <= 1024
+ *   decode path: T <= 32 and T * topk <= 1024 (the shared-memory tables must fit)
  *   prefill path: K % 64 == 0, I % 64 == 0 (tensor-core tiles), T * topk < 2^31 / K
- * Alignment (MXFP4_MOE_ERR_ALIGN otherwise): w13, w2, hidden and out 16-byte
- * aligned; workspace 256-byte aligned. Scale arrays have no alignment rule. */
+ * Alignment (MXFP4_MOE_ERR_ALIGN otherwise): w13, s13, w2, s2, hidden and out
+ * 16-byte aligned; workspace 256-byte aligned. */
 
 /* Bytes of device workspace a forward call with these sizes needs (either
  * path). The first mxfp4_moe_workspace_size(...) bytes must be zero before

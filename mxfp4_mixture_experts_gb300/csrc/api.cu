@@ -1,6 +1,8 @@
 // Host side of the C ABI declared in include/mxfp4_moe.h: argument checks,
 // workspace layout and kernel dispatch. Nothing here allocates, frees or
 // synchronises; every call only enqueues work on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -28,6 +30,37 @@ std::mutex g_dev_mu;
 
 void* const* g_phase_events = nullptr;
 int g_phase_n = 0;
+
+// cuTensorMapEncodeTiled, fetched from the driver at first use (no link-time
+// dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+bool get_encoder() {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_encode_tiled != nullptr) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// Packed weights viewed as a 2-D byte tensor [rows][row_bytes]; tiles of 16
+// rows x 128 bytes land in shared memory with the 128-byte swizzle; reads past
+// the end of a row return zeros.
+bool weight_tensor_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows) {
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, 16};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Checks the current device once (sm_103) and caches its SM count.
 int current_device(DeviceInfo** out) {
@@ -75,15 +108,15 @@ bool shape_ok(int T, int K, int I, int E, int topk) {
 Layout layout(int T, int K, int I, int E, int topk) {
   Layout L;
   const size_t R = (size_t)T * topk;
-  const size_t warps = (size_t)kMaxCtas * kDecodeWarpsPerCta;
+  const size_t ctas = (size_t)kMaxCtas;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
-  L.item_ctr1 = take(warps * sizeof(int));
-  L.item_ctr2 = take(warps * sizeof(int));
+  L.item_ctr1 = take(ctas * sizeof(int));
+  L.item_ctr2 = take(ctas * sizeof(int));
   L.tile_ctr = take((size_t)(K / 16) * sizeof(int));
   L.pf_ctr = take(prefill_counter_bytes(T, K, I, E, topk));
-  L.parts1 = take(warps * 2 * 128 * sizeof(float));
-  L.parts2 = take(warps * 2 * 128 * sizeof(float));
+  L.parts1 = take(ctas * 2 * 256 * sizeof(float));
+  L.parts2 = take(ctas * 2 * 256 * sizeof(float));
   L.h = take(R * I * 2);
   L.P = take(R * K * sizeof(float));
   L.rcount = take((size_t)E * sizeof(int));
@@ -133,7 +166,8 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   if (T == 0) return MXFP4_MOE_OK;
   if (!hidden || !topk_ids || !topk_weights || !w13 || !s13 || !w2 || !s2 || !out)
     return MXFP4_MOE_ERR_ARG;
-  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(w2, 16))
+  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(s13, 16) || !aligned(s2, 16))
     return MXFP4_MOE_ERR_ALIGN;
   if (workspace == nullptr) return MXFP4_MOE_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return MXFP4_MOE_ERR_ALIGN;
@@ -162,7 +196,11 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a.y = static_cast<uint16_t*>(out);
     a.tile_ctr = reinterpret_cast<int*>(ws + L.tile_ctr);
     a.status = status;
-    a.smem_bytes = (size_t)d->max_smem;
+    if (!get_encoder()) return MXFP4_MOE_ERR_CUDA;
+    CUtensorMap map1, map2;
+    if (!weight_tensor_map(&map1, w13, (uint64_t)K / 2, (uint64_t)E * 2 * I) ||
+        !weight_tensor_map(&map2, w2, (uint64_t)I / 2, (uint64_t)E * K))
+      return MXFP4_MOE_ERR_CUDA;
     record_phase(0, s);
     DecodeArgs a1 = a;
     a1.x = static_cast<const uint16_t*>(hidden);
@@ -170,7 +208,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a1.wsc = s13;
     a1.parts = reinterpret_cast<float*>(ws + L.parts1);
     a1.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr1);
-    cudaError_t e = launch_decode(a1, 1, ctas, s, g_phase_events == nullptr);
+    cudaError_t e = launch_decode(a1, 1, ctas, d->max_smem, map1, s, g_phase_events == nullptr);
     if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     record_phase(1, s);
     DecodeArgs a2 = a;
@@ -179,7 +217,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a2.wsc = s2;
     a2.parts = reinterpret_cast<float*>(ws + L.parts2);
     a2.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr2);
-    e = launch_decode(a2, 2, ctas, s, g_phase_events == nullptr);
+    e = launch_decode(a2, 2, ctas, d->max_smem, map2, s, g_phase_events == nullptr);
     if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     record_phase(2, s);
     return MXFP4_MOE_OK;

@@ -3,510 +3,637 @@
 //
 // Two launches per layer call:
 //   phase 1 (w13): per touched expert, gate and up rows are streamed once,
-//                  dequantised in registers, multiplied with the expert's
-//                  tokens on the tensor cores (mma.sync m16n8k16, fp32
-//                  accumulators) and finished with SwiGLU -> bf16 h [R, I];
+//                  decoded in registers, multiplied with the expert's tokens
+//                  on the tensor cores and finished with SwiGLU -> bf16 h [R, I];
 //   phase 2 (w2):  per touched expert, the w2 rows are streamed the same way
 //                  against h, scaled by the routing weight into fp32 route
-//                  outputs P [R, K]; the last contribution to each 16-row
+//                  outputs P [R, K]; the last contribution to each 32-row
 //                  output tile sums the k slots of every token in slot order
 //                  and writes bf16 y [T, K].
 //
-// Work decomposition. A work *item* is (touched expert d, row tile nt, token
-// group gr): 16 weight rows against up to 8 of the expert's tokens (phase 1:
-// gate rows nt*8..nt*8+7 and the matching up rows, so SwiGLU sees gate and up
-// of one output in the same thread; phase 2: w2 rows nt*16..nt*16+15). An item
-// has S = ceil(K_red/128) *steps*; in one step a warp consumes 4 scale blocks
-// (lane t of each quad owns one 32-value block of one gate/w2 row and of the
-// paired up/w2 row). Items are ordered (d, nt, gr) and their steps are dealt to
-// warps in equal contiguous ranges ("stream-K"), so every warp streams the same
-// number of bytes whatever the routing. An item cut between warps is finished
-// by whichever of its warps arrives last (an integer counter per item): it adds
-// the fp32 partials in fixed warp order, so the result is deterministic.
+// CTA = 1 producer warp + 8 consumer warps, one CTA per SM.
+//  * The producer streams weight tiles with 2-D TMA (cp.async.bulk.tensor,
+//    128-byte swizzle) into a ring of shared-memory stages, and each item's
+//    E8M0 scale rows with 1-D bulk copies; mbarriers track both.
+//  * Consumers decode E2M1 with the hardware e2m1x2 -> f16x2 conversion
+//    (exact), run one m16n8k16 f16 MMA pair per 32-value scale block into a
+//    fresh fp32 fragment and fold it into the accumulator with one FFMA by
+//    2^(s-127) (exact for every scale byte, 0 and 255 included).
+//  * Activations (hidden rows for phase 1, h rows for phase 2) are staged once
+//    per CTA in shared memory as f16 after an exact power-of-two prescale per
+//    row (max |x| lands in [2^14, 2^15)); the epilogue multiplies it back.
 //
-// Register dequantisation (see e2m1_pair_raw): nibbles p and p+4 of a 32-bit
-// word become one bf16x2 A-fragment register, so lane t's physical k indices
-// in a step are a fixed permutation of its block; the B fragment (activations)
-// is gathered in the same permutation with byte permutes.
+// Work decomposition. An *item* is (touched expert d, row tile nt, token
+// group gr): 32 weight rows against up to 8 of the expert's tokens (phase 1:
+// gate rows 16nt..16nt+15 and the matching up rows; phase 2: w2 rows
+// 32nt..32nt+31). Its K range is cut into *chunks* of 32 scale blocks (one
+// pipeline stage each). The (item, chunk) units are dealt to CTAs in equal
+// contiguous ranges, so every SM streams the same number of bytes whatever
+// the routing; an item cut between CTAs is finished by whichever CTA arrives
+// last (an integer counter per item), adding the fp32 partials in fixed CTA
+// order, so the result is deterministic.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "route.cuh"
 #include "kernels.h"
 
 namespace mxmoe {
 
-constexpr int kDecWarps = 16;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kPrefetch = 4;       // steps of weight bytes in flight per warp
-constexpr int kGroup = 8;          // tokens per mma n-tile
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kGroup = 8;            // tokens per mma n-tile
+constexpr int kItemRows = 32;        // weight rows per item (two m16 tiles)
+constexpr int kChunkBlocks = 32;     // scale blocks per stage (4 TMA columns of 128 B)
+constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 16 KB
+constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 128 bytes
+constexpr int kScaleSlots = 3;
+constexpr int kBarConsumers = 1;     // named barrier id of the consumer warps
+
+__host__ __device__ inline size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+// Shared-memory plan (byte offsets from a 1024-byte aligned base).
+struct DecodeSmem {
+  size_t stage, scale, scale_slot, bars, red, fin, flags, ints, row_sh, xs, total;
+};
+
+__host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, int I, int E,
+                                                       int topk, int stages, int rows_cap,
+                                                       int xs_rows, int xs_stride) {
+  DecodeSmem m;
+  const int kred = phase == 1 ? K : I;
+  const int nblk = kred / kScaleBlock;
+  const int R = T * topk;
+  size_t o = 0;
+  m.stage = o;
+  o += (size_t)stages * kStageBytes;
+  m.scale_slot = round_up((size_t)kItemRows * nblk, 128);
+  m.scale = o;
+  o += kScaleSlots * m.scale_slot;
+  m.bars = o;
+  o += round_up((size_t)(2 * stages + 2 * kScaleSlots) * 8, 16);
+  m.red = o;
+  o += (size_t)kConsumerWarps * 2 * 32 * 4 * sizeof(float);
+  m.fin = o;
+  o += 256 * sizeof(float);
+  m.flags = o;
+  o += 16;
+  m.ints = o;
+  o += (size_t)(5 * E + R + 6) * sizeof(int);
+  m.row_sh = o;
+  o += (size_t)rows_cap * sizeof(int);
+  o = round_up(o, 128);
+  m.xs = o;
+  o += (size_t)xs_rows * xs_stride;
+  m.total = o;
+  return m;
+}
 
 struct Cursor {
-  int s;    // step inside the item
-  int nt;   // row tile
-  int gr;   // token group
-  int d;    // index into the touched-expert list
-  int ng;   // token groups of expert d
-  int e;    // expert id
+  int nt, gr, d, ng, e;
 };
 
-struct DecodeCtx {
-  const DecodeArgs* a;
+struct Ctx {
   RouteTables tb;
-  const int* gbase;   // [nD+1] token-group prefix over touched experts
-  int nD, NT, S, nblk, rows_per_e, row_bytes, G;
-  // activation rows staged in shared memory: list positions [p_lo, p_lo + nrows)
-  const char* stage;
-  int p_lo, nrows, stage_stride;
+  const int* gbase;
+  int nD, NT, G;
 };
 
-__device__ __forceinline__ void cursor_load_expert(Cursor& c, const DecodeCtx& x) {
+__device__ __forceinline__ void cursor_expert(Cursor& c, const Ctx& x) {
   if (c.d < x.nD) {
     c.e = x.tb.touched[c.d];
     c.ng = (x.tb.cnt[c.e] + kGroup - 1) / kGroup;
   }
 }
 
-// Position of global unit u (item u / S, step u % S).
-__device__ __forceinline__ Cursor cursor_at(int64_t u, const DecodeCtx& x) {
+// Item index -> (d, nt, gr); items of expert d start at NT * gbase[d].
+__device__ __forceinline__ Cursor cursor_of_item(int64_t item, const Ctx& x) {
   Cursor c;
-  const int64_t item = u / x.S;
-  c.s = (int)(u - item * x.S);
-  // items of expert d start at NT * gbase[d]; find d by binary search
-  int lo = 0, hi = x.nD;   // invariant: NT*gbase[lo] <= item < NT*gbase[hi]
+  int lo = 0, hi = x.nD;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
     if ((int64_t)x.NT * x.gbase[mid] <= item) lo = mid; else hi = mid;
   }
   c.d = lo;
-  cursor_load_expert(c, x);
+  cursor_expert(c, x);
   const int local = (int)(item - (int64_t)x.NT * x.gbase[lo]);
   c.nt = local / c.ng;
   c.gr = local - c.nt * c.ng;
   return c;
 }
 
-__device__ __forceinline__ void cursor_next(Cursor& c, const DecodeCtx& x) {
-  if (++c.s == x.S) {
-    c.s = 0;
-    if (++c.gr == c.ng) {
-      c.gr = 0;
-      if (++c.nt == x.NT) {
-        c.nt = 0;
-        ++c.d;
-        cursor_load_expert(c, x);
-      }
+__device__ __forceinline__ void cursor_next_item(Cursor& c, const Ctx& x) {
+  if (++c.gr == c.ng) {
+    c.gr = 0;
+    if (++c.nt == x.NT) {
+      c.nt = 0;
+      ++c.d;
+      cursor_expert(c, x);
     }
   }
 }
 
-__device__ __forceinline__ int64_t cursor_item(const Cursor& c, const DecodeCtx& x) {
-  return (int64_t)x.NT * x.gbase[c.d] + (int64_t)c.nt * c.ng + c.gr;
-}
-
-// Weight rows of the item for this lane's quad row g: first row (gate / w2
-// row g) and second row (up / w2 row g+8).
-template <int PHASE>
-__device__ __forceinline__ void item_rows(const Cursor& c, const DecodeCtx& x, int g,
-                                          int64_t& r0, int64_t& r1) {
-  const DecodeArgs& a = *x.a;
-  if (PHASE == 1) {
-    r0 = (int64_t)c.e * (2 * a.I) + c.nt * 8 + g;
-    r1 = r0 + a.I;
-  } else {
-    r0 = (int64_t)c.e * a.K + c.nt * 16 + g;
-    r1 = r0 + 8;
-  }
-}
-
-struct Slot {
-  uint4 w0, w1;
-  uint32_t s0, s1;
-};
-
-template <int PHASE>
-__device__ __forceinline__ void load_slot(Slot& sl, const Cursor& c, const DecodeCtx& x, int g,
-                                          int t) {
-  const int b = c.s * 4 + t;
-  if (b < x.nblk) {
-    int64_t r0, r1;
-    item_rows<PHASE>(c, x, g, r0, r1);
-    const DecodeArgs& a = *x.a;
-    sl.w0 = ldg_stream16(a.wq + r0 * x.row_bytes + b * 16);
-    sl.w1 = ldg_stream16(a.wq + r1 * x.row_bytes + b * 16);
-    sl.s0 = ldg_u8(a.wsc + r0 * x.nblk + b);
-    sl.s1 = ldg_u8(a.wsc + r1 * x.nblk + b);
-  } else {
-    sl.w0 = make_uint4(0, 0, 0, 0);
-    sl.w1 = make_uint4(0, 0, 0, 0);
-    sl.s0 = 127;
-    sl.s1 = 127;
-  }
-}
-
-// Pairs of one 16-byte chunk of 8 consecutive activations x[8i..8i+7]:
-// (x[8i+p], x[8i+p+4]) for p = 0..3, matching e2m1_pair_raw<p> of word i.
-__device__ __forceinline__ uint4 chunk_to_pairs(uint4 v) {
-  return make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
-                    prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
-}
-
-// Global source row of list position p (a token row of hidden, or a route row of h).
-template <int PHASE>
-__device__ __forceinline__ const uint16_t* src_row(const DecodeCtx& x, int p) {
-  const DecodeArgs& a = *x.a;
-  const int r = x.tb.lst[p];
-  if (PHASE == 1) return a.x + (int64_t)(r / a.topk) * a.K;
-  return a.x + (int64_t)r * a.I;
-}
-
-// Shared-memory layout of a staged row: block b (32 values) takes 64 bytes,
-// its 16-byte chunk i (pairs of x[32b+8i .. 32b+8i+7]) sits at position
-// i ^ (b & 3), so the four lanes of a quad (consecutive blocks) and two quads
-// (row stride = 64 mod 128 bytes) hit distinct banks.
-__device__ __forceinline__ int stage_offset(int b, int i) { return b * 64 + ((i ^ (b & 3)) << 4); }
-
-// B fragment pairs of token column g for block b, in [word i][pair p] order.
-template <int PHASE>
-__device__ __forceinline__ void load_b(uint32_t (&bp)[16], const Cursor& c, const DecodeCtx& x,
-                                       int g, int b) {
-  const int j = c.gr * kGroup + g;
-  if (b < x.nblk && j < x.tb.cnt[c.e]) {
-    const int p = x.tb.off[c.e] + j;
-    const int idx = p - x.p_lo;
-    if (idx >= 0 && idx < x.nrows) {
-      const char* row = x.stage + (size_t)idx * x.stage_stride;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = *reinterpret_cast<const uint4*>(row + stage_offset(b, i));
-        bp[4 * i + 0] = v.x;
-        bp[4 * i + 1] = v.y;
-        bp[4 * i + 2] = v.z;
-        bp[4 * i + 3] = v.w;
-      }
-    } else {
-      // row not staged (shared memory full): read it from L2 and permute here
-      const uint4* src = reinterpret_cast<const uint4*>(src_row<PHASE>(x, p) + b * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 v = chunk_to_pairs(ldcg16(src + i));
-        bp[4 * i + 0] = v.x;
-        bp[4 * i + 1] = v.y;
-        bp[4 * i + 2] = v.z;
-        bp[4 * i + 3] = v.w;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int q = 0; q < 16; ++q) bp[q] = 0;
-  }
-}
-
-template <int WI>
-__device__ __forceinline__ void mma_word(float (&acc)[4], uint32_t wa, uint32_t wb,
-                                         const ScaleMul& ma, const ScaleMul& mb,
-                                         const uint32_t (&bp)[16]) {
-  const uint32_t a0 = apply_scale(e2m1_pair_raw<0>(wa), ma);
-  const uint32_t a1 = apply_scale(e2m1_pair_raw<1>(wa), ma);
-  const uint32_t a2 = apply_scale(e2m1_pair_raw<2>(wa), ma);
-  const uint32_t a3 = apply_scale(e2m1_pair_raw<3>(wa), ma);
-  const uint32_t c0 = apply_scale(e2m1_pair_raw<0>(wb), mb);
-  const uint32_t c1 = apply_scale(e2m1_pair_raw<1>(wb), mb);
-  const uint32_t c2 = apply_scale(e2m1_pair_raw<2>(wb), mb);
-  const uint32_t c3 = apply_scale(e2m1_pair_raw<3>(wb), mb);
-  // A rows: g -> word wa, g+8 -> word wb; logical k (2t,2t+1) then (2t+8,2t+9)
-  mma_bf16_16816(acc, a0, c0, a1, c1, bp[4 * WI + 0], bp[4 * WI + 1]);
-  mma_bf16_16816(acc, a2, c2, a3, c3, bp[4 * WI + 2], bp[4 * WI + 3]);
-}
-
-template <int PHASE>
-__device__ __forceinline__ void compute_step(float (&acc)[4], const Slot& sl, const Cursor& c,
-                                             const DecodeCtx& x, int g, int t) {
-  uint32_t bp[16];
-  load_b<PHASE>(bp, c, x, g, c.s * 4 + t);
-  const ScaleMul ma = scale_mul(sl.s0), mb = scale_mul(sl.s1);
-  mma_word<0>(acc, sl.w0.x, sl.w1.x, ma, mb, bp);
-  mma_word<1>(acc, sl.w0.y, sl.w1.y, ma, mb, bp);
-  mma_word<2>(acc, sl.w0.z, sl.w1.z, ma, mb, bp);
-  mma_word<3>(acc, sl.w0.w, sl.w1.w, ma, mb, bp);
-}
-
-// Balanced split of U units over NW warps: warp v gets q = U / NW units plus
-// one more if v < U % NW, in order. Warps left empty (U < NW) are all at the
-// end, so the warps covering one item are always consecutive and non-empty.
-__device__ __forceinline__ int64_t range_begin(int v, int64_t U, int NW) {
-  const int64_t q = U / NW, rem = U % NW;
+// Balanced split of U units over n CTAs (first U % n CTAs get one more).
+__device__ __forceinline__ int64_t range_begin(int v, int64_t U, int n) {
+  const int64_t q = U / n, rem = U % n;
   return (int64_t)v * q + (v < rem ? v : rem);
 }
-__device__ __forceinline__ int warp_of_unit(int64_t u, int64_t U, int NW) {
-  const int64_t q = U / NW, rem = U % NW;
+__device__ __forceinline__ int owner_of_unit(int64_t u, int64_t U, int n) {
+  const int64_t q = U / n, rem = U % n;
   if (u < rem * (q + 1)) return (int)(u / (q + 1));
   return (int)(rem + (u - rem * (q + 1)) / q);
 }
 
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+// First weight row of TMA box h (0, 1) of an item.
+template <int PHASE>
+__device__ __forceinline__ int box_row(const Cursor& c, const DecodeArgs& a, int h) {
+  if (PHASE == 1) return c.e * (2 * a.I) + h * a.I + c.nt * 16;
+  return c.e * a.K + c.nt * kItemRows + h * 16;
+}
 
-// Item epilogue, phase 1: SwiGLU of (gate, up) and bf16 store into h.
-__device__ __forceinline__ void finish_w13(const float (&acc)[4], const Cursor& c,
-                                           const DecodeCtx& x, int g, int t) {
-  const DecodeArgs& a = *x.a;
-  const int n = c.nt * 8 + g;
-  const int ntok = min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup);
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int col = 2 * t + q;
-    if (col < ntok) {
-      const int r = x.tb.lst[x.tb.off[c.e] + c.gr * kGroup + col];
-      const float hv = silu_f32(acc[q]) * acc[2 + q];
-      reinterpret_cast<uint16_t*>(a.h)[(int64_t)r * a.I + n] = f32_to_bf16_rne(hv);
-    }
+// Scale rows of an item into [32][nblk]: phase 1 two runs of 16 rows (gate,
+// up), phase 2 one run of 32 rows.
+template <int PHASE>
+__device__ __forceinline__ void issue_scales(const Cursor& c, const DecodeArgs& a, int nblk,
+                                             uint8_t* dst, uint64_t* bar) {
+  const uint32_t run = 16u * nblk;
+  mbar_arrive_expect_tx(bar, 2 * run);
+  if (PHASE == 1) {
+    bulk_load(dst, a.wsc + (size_t)box_row<1>(c, a, 0) * nblk, run, bar);
+    bulk_load(dst + run, a.wsc + (size_t)box_row<1>(c, a, 1) * nblk, run, bar);
+  } else {
+    bulk_load(dst, a.wsc + (size_t)box_row<2>(c, a, 0) * nblk, 2 * run, bar);
   }
 }
 
-// Item epilogue, phase 2: weighted route outputs, then (last contribution to
-// the row tile) the slot-order combine into y.
-__device__ __forceinline__ void finish_w2(const float (&acc)[4], const Cursor& c,
-                                          const DecodeCtx& x, int g, int t, int lane) {
-  const DecodeArgs& a = *x.a;
-  const int m0 = c.nt * 16;
-  const int ntok = min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup);
+// Activation row (bf16) of route-list position q.
+template <int PHASE>
+__device__ __forceinline__ const uint16_t* act_row(const DecodeArgs& a, const RouteTables& tb,
+                                                   int q) {
+  const int r = tb.lst[q];
+  if (PHASE == 1) return a.x + (size_t)(r / a.topk) * a.K;
+  return a.x + (size_t)r * a.I;
+}
+
+__device__ __forceinline__ float pow2f(int e) {   // 2^e, -126 <= e <= 127
+  return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
+// 8 bf16 (one uint4) times a power of two -> 8 f16, round to nearest even.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float mul) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int col = 2 * t + q;
-    if (col < ntok) {
-      const int r = x.tb.lst[x.tb.off[c.e] + c.gr * kGroup + col];
-      const float w = a.wts[r];
-      a.P[(int64_t)r * a.K + m0 + g] = w * acc[q];
-      a.P[(int64_t)r * a.K + m0 + g + 8] = w * acc[2 + q];
-    }
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * mul;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * mul;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
   }
-  __syncwarp();
-  __threadfence();
-  int old = 0;
-  if (lane == 0) old = atomicAdd(&a.tile_ctr[c.nt], 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old != x.G - 1) return;
-  __threadfence();
-  const int k = a.topk;
-  for (int idx = lane; idx < a.T * 16; idx += 32) {
-    const int tok = idx >> 4;
-    const int m = m0 + (idx & 15);
-    float s = 0.0f;
-    for (int j = 0; j < k; ++j) {
-      const int r = tok * k + j;
-      const int e = a.ids[r];
-      if (e >= 0 && e < a.E) s += ldcg_f32(a.P + (int64_t)r * a.K + m);
-    }
-    a.y[(int64_t)tok * a.K + m] = f32_to_bf16_rne(s);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// Epilogue of one item from the 256 reduced values (thread o = consumer
+// thread ctid holds output (tile tt, lane l, element q): MMA row
+// tt*16 + l/4 + 8*(q/2), token column 2*(l%4) + q%2). All 256 consumer
+// threads call it.
+template <int PHASE>
+__device__ void finish_item(float v, const Cursor& c, const Ctx& x, const DecodeArgs& a,
+                            float* fin, int ctid, int p_lo, int n_sh, const int* row_sh,
+                            int* flags) {
+  const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
+  const int g = l >> 2, t = l & 3;
+  const int col = 2 * t + (q & 1);
+  const int ntok = min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup);
+  const int qpos = x.tb.off[c.e] + c.gr * kGroup + col;   // route-list position of the column
+  float colmul = 1.0f;
+  int r = -1;
+  if (col < ntok) {
+    r = x.tb.lst[qpos];
+    const int idx = qpos - p_lo;
+    colmul = pow2f(idx >= 0 && idx < n_sh ? row_sh[idx] : 0);
   }
-  __syncwarp();
-  if (lane == 0) a.tile_ctr[c.nt] = 0;
+  if (PHASE == 1) {
+    fin[ctid] = v;
+    named_barrier(kBarConsumers, kConsumerThreads);
+    if (q < 2 && col < ntok) {
+      const float gate = fin[ctid] * colmul, up = fin[ctid + 2] * colmul;
+      const int n = c.nt * 16 + tt * 8 + g;
+      a.h[(size_t)r * a.I + n] = f32_to_bf16_rne(silu_f32(gate) * up);
+    }
+  } else {
+    const int m = c.nt * kItemRows + tt * 16 + g + 8 * (q >> 1);
+    if (col < ntok) a.P[(size_t)r * a.K + m] = a.wts[r] * (v * colmul);
+    __threadfence();
+    named_barrier(kBarConsumers, kConsumerThreads);
+    if (ctid == 0) flags[0] = atomicAdd(&a.tile_ctr[c.nt], 1);
+    named_barrier(kBarConsumers, kConsumerThreads);
+    if (flags[0] != x.G - 1) return;
+    __threadfence();
+    const int k = a.topk, m0 = c.nt * kItemRows;
+    for (int idx = ctid; idx < a.T * kItemRows; idx += kConsumerThreads) {
+      const int tok = idx / kItemRows, mm = m0 + idx % kItemRows;
+      float s = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int rr = tok * k + j;
+        const int e = a.ids[rr];
+        if (e >= 0 && e < a.E) s += ldcg_f32(a.P + (size_t)rr * a.K + mm);
+      }
+      a.y[(size_t)tok * a.K + mm] = f32_to_bf16_rne(s);
+    }
+    if (ctid == 0) a.tile_ctr[c.nt] = 0;
+  }
 }
 
 template <int PHASE>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs args) {
-  extern __shared__ int smem[];
-  const DecodeArgs& a = args;
-  const int E = a.E;
-  const int R = a.T * a.topk;
+__global__ void __launch_bounds__(kThreads, 1)
+decode_kernel(const __grid_constant__ DecodeParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const DecodeArgs& a = P.a;
+  const int E = a.E, R = a.T * a.topk;
+  const int kred = PHASE == 1 ? a.K : a.I;
+  const int nblk = kred / kScaleBlock;
+  const int NC = (nblk + kChunkBlocks - 1) / kChunkBlocks;
+  const int S = P.stages;
+  const DecodeSmem M = decode_smem_plan(PHASE, a.T, a.K, a.I, E, a.topk, S, P.rows_cap,
+                                        P.xs_rows_cap, P.xs_stride);
+  uint8_t* stage_base = smem + M.stage;
+  uint8_t* scale_base = smem + M.scale;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + M.bars);   // [S]
+  uint64_t* empty = full + S;                                     // [S]
+  uint64_t* sfull = empty + S;                                    // [kScaleSlots]
+  uint64_t* sempty = sfull + kScaleSlots;                         // [kScaleSlots]
+  float* red = reinterpret_cast<float*>(smem + M.red);            // [8][2][32][4]
+  float* fin = reinterpret_cast<float*>(smem + M.fin);            // [256]
+  int* flags = reinterpret_cast<int*>(smem + M.flags);
   RouteTables tb;
-  tb.cnt = smem;
+  tb.cnt = reinterpret_cast<int*>(smem + M.ints);
   tb.off = tb.cnt + E;
   tb.run = tb.off + E + 1;
   tb.touched = tb.run + E;
   tb.lst = tb.touched + E;
   tb.misc = tb.lst + R;
-  int* gbase = tb.misc + 4;   // [E+1]
+  int* gbase = tb.misc + 4;                                        // [E+1]
+  int* row_sh = reinterpret_cast<int*>(smem + M.row_sh);          // [rows_cap]
+  uint8_t* xs_base = smem + M.xs;
+  const int xs_stride = P.xs_stride;
 
-  // Phase 1 reads inputs that the previous kernel in the stream may produce;
-  // phase 2 only needs h after the wait (its routing and weight prefetch use
-  // inputs that were complete before phase 1 started).
-  if (PHASE == 1) grid_dependency_wait();
-  cta_route_small(a.ids, R, E, tb);
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  if (PHASE == 1) grid_dependency_wait();   // inputs may come from the previous kernel
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kScaleSlots; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sempty[i], kConsumerWarps);
+    }
+    fence_barrier_init();
+    prefetch_tensormap(&P.tmap);
+  }
+  cta_route_small(a.ids, R, E, tb);   // ends with __syncthreads
   const int nD = tb.misc[0];
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  if (tid < 32) {
     int carry = 0;
     for (int base = 0; base < nD; base += 32) {
       const int d = base + lane;
       const int ng = d < nD ? (tb.cnt[tb.touched[d]] + kGroup - 1) / kGroup : 0;
-      int xs = ng;
+      int xsum = ng;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, xs, o);
-        if (lane >= o) xs += y;
+        const int y = __shfl_up_sync(0xffffffffu, xsum, o);
+        if (lane >= o) xsum += y;
       }
-      if (d < nD) gbase[d] = carry + xs - ng;
-      carry += __shfl_sync(0xffffffffu, xs, 31);
+      if (d < nD) gbase[d] = carry + xsum - ng;
+      carry += __shfl_sync(0xffffffffu, xsum, 31);
     }
     if (lane == 0) gbase[nD] = carry;
   }
   __syncthreads();
   launch_dependents();
 
-  DecodeCtx x;
-  x.a = &a;
+  Ctx x;
   x.tb = tb;
   x.gbase = gbase;
   x.nD = nD;
   x.G = gbase[nD];
-  x.NT = PHASE == 1 ? a.I / 8 : a.K / 16;
-  const int kred = PHASE == 1 ? a.K : a.I;
-  x.nblk = kred / kScaleBlock;
-  x.S = (x.nblk + 3) / 4;
-  x.rows_per_e = PHASE == 1 ? 2 * a.I : a.K;
-  x.row_bytes = kred / 2;
+  x.NT = PHASE == 1 ? a.I / 16 : a.K / kItemRows;
 
-  if (PHASE == 1 && blockIdx.x == 0 && threadIdx.x == 0 && a.status != nullptr) {
+  if (PHASE == 1 && blockIdx.x == 0 && tid == 0 && a.status != nullptr) {
     a.status[0] = tb.misc[1];
     a.status[1] = nD;
     a.status[2] = 0;
     a.status[3] = 0;
   }
 
-  const int64_t U = (int64_t)x.NT * x.G * x.S;
+  const int64_t U = (int64_t)x.NT * x.G * NC;
   if (U == 0) {
-    // no valid route at all: y is zero
-    if (PHASE == 2) {
+    if (PHASE == 2) {   // no valid route at all: y is zero
       grid_dependency_wait();
       const int64_t n = (int64_t)a.T * a.K;
-      for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+      for (int64_t i = blockIdx.x * (int64_t)blockDim.x + tid; i < n;
            i += (int64_t)gridDim.x * blockDim.x)
         a.y[i] = 0;
     }
     return;
   }
+  const int nCta = gridDim.x;
+  const int64_t cub = range_begin(blockIdx.x, U, nCta);
+  const int64_t cue = range_begin(blockIdx.x + 1, U, nCta);
+  if (cub >= cue) return;
+  const int64_t i_first = cub / NC, i_last = (cue - 1) / NC;
 
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
+  // ======================= producer warp =======================
+  if (warp == 0) {
+    if (lane == 0) {
+      Cursor c = cursor_of_item(i_first, x);
+      int64_t item = i_first;
+      int k = 0, seq = 0;
+      bool ok = true;
+      for (int64_t u = cub; u < cue && ok; ++u) {
+        const int64_t it = u / NC;
+        const int ch = (int)(u - it * NC);
+        if (it != item) {
+          cursor_next_item(c, x);
+          item = it;
+        }
+        if (u == cub || ch == 0) {
+          const int slot = seq % kScaleSlots;
+          if (seq >= kScaleSlots) ok = mbar_wait(&sempty[slot], ((seq / kScaleSlots) - 1) & 1);
+          if (!ok) break;
+          issue_scales<PHASE>(c, a, nblk, scale_base + slot * M.scale_slot, &sfull[slot]);
+          ++seq;
+        }
+        const int st = k % S;
+        if (k >= S) ok = mbar_wait(&empty[st], ((k / S) - 1) & 1);
+        if (!ok) break;
+        uint8_t* dst = stage_base + (size_t)st * kStageBytes;
+        // columns of 8 blocks that start inside the row (a partial last
+        // column reads zeros past the row end)
+        const int ncols = min(4, (nblk - ch * kChunkBlocks + 7) / 8);
+        mbar_arrive_expect_tx(&full[st], ncols * 2 * kBoxBytes);
+        const int x0 = ch * kChunkBlocks * 16;
+        for (int col = 0; col < ncols; ++col) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(dst + (col * 2 + h) * kBoxBytes, &P.tmap, x0 + col * 128,
+                        box_row<PHASE>(c, a, h), &full[st]);
+        }
+        ++k;
+      }
+      if (!ok && a.status != nullptr) atomicOr(&a.status[2], 1);
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  const int cw = warp - 1;        // consumer warp 0..7
+  const int ctid = tid - 32;      // 0..255
   const int g = lane >> 2, t = lane & 3;
-  const int NW = gridDim.x * kDecWarps;
-  const int v = blockIdx.x * kDecWarps + warp;
-  const int64_t cta_ub = range_begin(blockIdx.x * kDecWarps, U, NW);
-  const int64_t cta_ue = range_begin((blockIdx.x + 1) * kDecWarps, U, NW);
-  if (cta_ub >= cta_ue) return;     // the whole CTA has no work (U < number of warps)
-  const int64_t ub = range_begin(v, U, NW);
-  const int64_t ue = range_begin(v + 1, U, NW);
 
-  // Activation rows this CTA can need: every route of the touched experts its
-  // unit range covers (a contiguous stretch of the route list).
-  {
-    const Cursor c0 = cursor_at(cta_ub, x);
-    const Cursor c1 = cursor_at(cta_ue - 1, x);
-    const int e0 = tb.touched[c0.d], e1 = tb.touched[c1.d];
-    x.p_lo = tb.off[e0];
-    const int need = tb.off[e1] + tb.cnt[e1] - x.p_lo;
-    x.stage_stride = ((kred * 2 + 127) / 128) * 128 + 64;
-    const size_t tables = decode_smem_bytes(a.T, a.topk, E);
-    const size_t stage_at = (tables + 127) / 128 * 128;
-    x.stage = reinterpret_cast<const char*>(smem) + stage_at;
-    const int fit = (int)((a.smem_bytes - stage_at) / x.stage_stride);
-    x.nrows = need < fit ? need : fit;
-  }
+  // activation rows this CTA can need: every route of the touched experts
+  // its unit range covers (a contiguous stretch of the route list)
+  const Cursor c_first = cursor_of_item(i_first, x);
+  const Cursor c_last = cursor_of_item(i_last, x);
+  const int p_lo = tb.off[c_first.e];
+  const int p_need = tb.off[c_last.e] + tb.cnt[c_last.e] - p_lo;
+  const int n_sh = min(p_need, P.rows_cap);
+  const int xs_rows = min(n_sh, P.xs_rows_cap);
 
-  Cursor lc = ub < ue ? cursor_at(ub, x) : cursor_at(cta_ub, x);    // loader
-  Cursor cc = lc;                                                    // consumer
-  Slot ring[kPrefetch];
+  if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
+  for (int r = cw; r < n_sh; r += kConsumerWarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r));
+    uint32_t emax = 0;
+    for (int c16 = lane; c16 < kred / 8; c16 += 32) {
+      const uint4 v = ldcg16(src + c16);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int q = 0; q < kPrefetch; ++q) {
-    if (ub + q < ue) {
-      load_slot<PHASE>(ring[q], lc, x, g, t);
-      cursor_next(lc, x);
-    }
-  }
-  if (PHASE == 2) grid_dependency_wait();   // h is ready from here on
-
-  // stage: 16-byte chunks, permuted into MMA pair order
-  {
-    char* st = const_cast<char*>(x.stage);
-    const int chunks = kred / 8;
-    const int total = x.nrows * chunks;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-      const int row = i / chunks, c16 = i - row * chunks;
-      const uint4 v4 = ldcg16(src_row<PHASE>(x, x.p_lo + row) + c16 * 8);
-      *reinterpret_cast<uint4*>(st + (size_t)row * x.stage_stride + stage_offset(c16 >> 2, c16 & 3)) =
-          chunk_to_pairs(v4);
-    }
-  }
-  __syncthreads();
-  if (ub >= ue) return;
-
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  bool seg_from_start = (cc.s == 0);   // current segment began at step 0 of its item
-  bool first_seg = true;               // current segment is this warp's first
-  for (int64_t u = ub; u < ue; u += kPrefetch) {
-#pragma unroll
-    for (int q = 0; q < kPrefetch; ++q) {
-      if (u + q < ue) {
-        compute_step<PHASE>(acc, ring[q], cc, x, g, t);
-        if (u + q + kPrefetch < ue) {
-          load_slot<PHASE>(ring[q], lc, x, g, t);
-          cursor_next(lc, x);
-        }
-        const bool item_end = (cc.s == x.S - 1);
-        const bool range_end = (u + q + 1 == ue);
-        if (item_end || range_end) {
-          const bool whole = seg_from_start && item_end;
-          if (whole) {
-            if (PHASE == 1) finish_w13(acc, cc, x, g, t);
-            else finish_w2(acc, cc, x, g, t, lane);
-          } else {
-            // partial item: publish, count, and let the last arrival finish
-            const int64_t item = cursor_item(cc, x);
-            const int va = warp_of_unit(item * x.S, U, NW);
-            const int vb = warp_of_unit(item * x.S + x.S - 1, U, NW);
-            const int slot = first_seg ? 0 : 1;
-            float4* mine = reinterpret_cast<float4*>(a.parts + ((int64_t)v * 2 + slot) * 128);
-            mine[lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            __syncwarp();
-            __threadfence();
-            int old = 0;
-            if (lane == 0) old = atomicAdd(&a.item_ctr[va], 1);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == vb - va) {
-              __threadfence();
-              float tot[4] = {0.f, 0.f, 0.f, 0.f};
-              const bool va_first = range_begin(va, U, NW) == item * x.S;
-              for (int w = va; w <= vb; ++w) {
-                const int sl = (w == va && !va_first) ? 1 : 0;
-                const uint4 pv = ldcg16(a.parts + ((int64_t)w * 2 + sl) * 128 + lane * 4);
-                tot[0] += __uint_as_float(pv.x);
-                tot[1] += __uint_as_float(pv.y);
-                tot[2] += __uint_as_float(pv.z);
-                tot[3] += __uint_as_float(pv.w);
-              }
-              if (PHASE == 1) finish_w13(tot, cc, x, g, t);
-              else finish_w2(tot, cc, x, g, t, lane);
-              if (lane == 0) a.item_ctr[va] = 0;
-            }
-          }
-          acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-          seg_from_start = true;
-          first_seg = false;
-        }
-        cursor_next(cc, x);
+      for (int i = 0; i < 4; ++i) {
+        emax = max(emax, (w[i] >> 7) & 0xFFu);
+        emax = max(emax, (w[i] >> 23) & 0xFFu);
       }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+    if (lane == 0) {
+      // max |x| * 2^-sh in [2^14, 2^15): exact in f16 down to 2^-31 of the max
+      const int sh = emax == 0 ? 0 : (int)emax - 127 - 14;
+      row_sh[r] = max(-100, min(100, sh));
+    }
   }
+  named_barrier(kBarConsumers, kConsumerThreads);
+  for (int i = ctid; i < xs_rows * (kred / 8); i += kConsumerThreads) {
+    const int r = i / (kred / 8), c16 = i - r * (kred / 8);
+    const uint4 v = ldcg16(reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r)) + c16);
+    *reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride + c16 * 16) =
+        bf16x8_to_f16x8(v, pow2f(-row_sh[r]));
+  }
+  named_barrier(kBarConsumers, kConsumerThreads);
+
+  Cursor c = c_first;
+  int64_t item = i_first;
+  int k = 0, seq = 0;
+  float acc[2][4];
+  bool special = false;          // the item has E8M0 bytes 0 or 255
+  const uint8_t* sc = nullptr;   // scale rows of the item [32][nblk]
+  const uint8_t* brow = nullptr; // staged f16 row of this lane's token column
+  const uint16_t* bglob = nullptr;   // or its global bf16 row (not staged)
+  float bmul = 1.0f;
+  bool item_start = true;
+  bool ok = true;
+  // lane-constant parts of the A addresses: tile tt, rows g / g+8
+  int aoff0[2], aoff1[2], soff0[2], soff1[2];
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt) {
+    if (PHASE == 1) {
+      aoff0[tt] = 0 * kBoxBytes + (tt * 8 + g) * 128;
+      aoff1[tt] = 1 * kBoxBytes + (tt * 8 + g) * 128;
+      soff0[tt] = (tt * 8 + g) * nblk;
+      soff1[tt] = (16 + tt * 8 + g) * nblk;
+    } else {
+      aoff0[tt] = tt * kBoxBytes + g * 128;
+      aoff1[tt] = tt * kBoxBytes + (g + 8) * 128;
+      soff0[tt] = (tt * 16 + g) * nblk;
+      soff1[tt] = (tt * 16 + g + 8) * nblk;
+    }
+  }
+
+  for (int64_t u = cub; u < cue; ++u) {
+    const int64_t it = u / NC;
+    const int ch = (int)(u - it * NC);
+    if (it != item) {
+      cursor_next_item(c, x);
+      item = it;
+    }
+    if (item_start) {
+      const int slot = seq % kScaleSlots;
+      ok = ok && mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
+      sc = scale_base + slot * M.scale_slot;
+      int bad = 0;
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
+      for (int i = ctid; i < (kItemRows * nblk) / 4; i += kConsumerThreads) {
+        const uint32_t w = sw[i];
+        const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;     // some byte == 0
+        const uint32_t f = (~w - 0x01010101u) & w & 0x80808080u;     // some byte == 0xFF
+        bad |= (z | f) != 0u;
+      }
+      special = named_barrier_or(kBarConsumers, kConsumerThreads, bad != 0);
+      const int ntok = min(kGroup, tb.cnt[c.e] - c.gr * kGroup);
+      brow = nullptr;
+      bglob = nullptr;
+      if (g < ntok) {
+        const int qpos = tb.off[c.e] + c.gr * kGroup + g;
+        const int r = qpos - p_lo;
+        if (r >= 0 && r < xs_rows) {
+          brow = xs_base + (size_t)r * xs_stride;
+        } else {
+          bglob = act_row<PHASE>(a, tb, qpos);
+          bmul = pow2f(-(r >= 0 && r < n_sh ? row_sh[r] : 0));
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[tt][q] = 0.f;
+      item_start = false;
+    }
+
+    const int st = k % S;
+    ok = ok && mbar_wait(&full[st], (k / S) & 1);
+    const uint8_t* stg = stage_base + (size_t)st * kStageBytes;
+    const int b_lo = ch * kChunkBlocks;
+    const int b_hi = min(kChunkBlocks, nblk - b_lo);
+    const int bi_end = min(b_hi, cw * 4 + 4);
+    for (int bi = cw * 4; bi < bi_end; ++bi) {
+      const int b = b_lo + bi;
+      // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
+      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+      if (brow != nullptr) {
+        bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
+      } else if (bglob != nullptr) {
+        bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
+      }
+      // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
+      const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
+        e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
+        mma_f16_16816(d, a0, c0, a1, c1, bv.x, bv.y);
+        mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
+        const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
+        const float f0 = special ? e8m0_to_f32(sb0) : e8m0_to_f32_normal(sb0);
+        const float f1 = special ? e8m0_to_f32(sb1) : e8m0_to_f32_normal(sb1);
+        acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
+        acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
+        acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
+        acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    ++k;
+
+    const bool item_end = (ch == NC - 1) || (u + 1 == cue);
+    if (!item_end) continue;
+
+    // ---- item end: reduce the 8 warps' fragments, then finish or publish
+    float* my = red + ((size_t)cw * 2 * 32 + lane) * 4;
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+      *reinterpret_cast<float4*>(my + tt * 32 * 4) =
+          make_float4(acc[tt][0], acc[tt][1], acc[tt][2], acc[tt][3]);
+    named_barrier(kBarConsumers, kConsumerThreads);
+    float v = 0.f;
+    {
+      const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
+      for (int w = 0; w < kConsumerWarps; ++w) v += red[(((size_t)w * 2 + tt) * 32 + l) * 4 + q];
+    }
+    const bool whole = (ch == NC - 1) && (item * NC >= cub);
+    if (whole) {
+      finish_item<PHASE>(v, c, x, a, fin, ctid, p_lo, n_sh, row_sh, flags);
+    } else {
+      // partial item: publish, count, and let the last CTA to arrive finish it
+      const int va = owner_of_unit(item * NC, U, nCta);
+      const int vb = owner_of_unit(item * NC + NC - 1, U, nCta);
+      const int slot = (item == i_first) ? 0 : 1;
+      a.parts[((size_t)blockIdx.x * 2 + slot) * 256 + ctid] = v;
+      __threadfence();
+      named_barrier(kBarConsumers, kConsumerThreads);
+      if (ctid == 0) flags[1] = atomicAdd(&a.item_ctr[va], 1);
+      named_barrier(kBarConsumers, kConsumerThreads);
+      if (flags[1] == vb - va) {
+        __threadfence();
+        const bool va_first = range_begin(va, U, nCta) == item * NC;
+        float tot = 0.f;
+        for (int w = va; w <= vb; ++w) {
+          const int sl = (w == va && !va_first) ? 1 : 0;
+          tot += ldcg_f32(a.parts + ((size_t)w * 2 + sl) * 256 + ctid);
+        }
+        finish_item<PHASE>(tot, c, x, a, fin, ctid, p_lo, n_sh, row_sh, flags);
+        if (ctid == 0) a.item_ctr[va] = 0;
+      }
+    }
+    named_barrier(kBarConsumers, kConsumerThreads);
+    if (lane == 0) mbar_arrive(&sempty[seq % kScaleSlots]);
+    ++seq;
+    item_start = true;
+  }
+  if (!ok && lane == 0 && a.status != nullptr) atomicOr(&a.status[2], 1);
 }
 
+size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int stages) {
+  return decode_smem_plan(phase, T, K, I, E, topk, stages, T * topk, 0, 0).total + 1024;
+}
 
-// Raises a kernel's dynamic shared-memory limit only when a launch needs more
-// than was granted before (per process; one device per process is assumed for
-// the cache, a second device simply repeats the call).
-template <typename K>
-static cudaError_t ensure_smem(K kernel, size_t bytes, size_t& granted) {
+template <typename Kern>
+static cudaError_t ensure_smem(Kern kernel, size_t bytes, size_t& granted) {
   if (bytes <= 48 * 1024 || bytes <= granted) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) granted = bytes;
   return e;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, cudaStream_t stream,
-                          bool pdl) {
+cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_smem,
+                          const CUtensorMap& tmap, cudaStream_t stream, bool pdl) {
   static size_t granted1 = 0, granted2 = 0;
-  const size_t smem = a.smem_bytes;
+  DecodeParams p;
+  p.tmap = tmap;
+  p.a = a;
+  const int kred = phase == 1 ? a.K : a.I;
+  const int R = a.T * a.topk;
+  p.rows_cap = R;
+  p.xs_stride = (int)round_up((size_t)kred * 2, 128) + 64;
+  // deepest pipeline (up to 6 stages) that still leaves room for a few rows
+  int stages = 6;
+  size_t fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
+  const size_t want_rows = (size_t)(R < 8 ? R : 8) * p.xs_stride;
+  while (stages > 3 && fixed + want_rows > (size_t)max_smem) {
+    --stages;
+    fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
+  }
+  if (fixed > (size_t)max_smem) return cudaErrorInvalidValue;
+  p.stages = stages;
+  size_t rows = ((size_t)max_smem - fixed) / p.xs_stride;
+  if (rows > (size_t)R) rows = R;
+  p.xs_rows_cap = (int)rows;
+  const size_t smem = fixed + rows * p.xs_stride;
+
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(kDecThreads);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -517,11 +644,11 @@ cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, cudaStrea
   if (phase == 1) {
     cudaError_t e = ensure_smem(decode_kernel<1>, smem, granted1);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<1>, a);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<1>, p);
   }
   cudaError_t e = ensure_smem(decode_kernel<2>, smem, granted2);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<2>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<2>, p);
 }
 
 }  // namespace mxmoe

@@ -1,11 +1,24 @@
 // Packed MXFP4 rows -> bf16 ("MXFP4 MoE decode kernels", Prefill: mxk_deq
-// unpacks an expert's weights straight to bf16). It uses the same register
-// decode and exact scale multiply as the decode and prefill kernels, so the
-// bit-exact test of this entry point also pins their dequantisation.
+// unpacks an expert's weights straight to bf16). It uses the same
+// conversion as the decode kernels -- hardware e2m1x2 -> f16x2, then an exact
+// fp32 multiply by 2^(s-127) -- so the bit-exact test of this entry point also
+// pins their dequantisation. Every product is representable in fp32 (E2M1 has
+// two significant bits), so the only rounding is the final fp32 -> bf16 one,
+// which is exact except where the product leaves the bf16 range.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mxmoe {
+
+__device__ __forceinline__ uint32_t f16x2_scale_to_bf16x2(uint32_t h2, float s) {
+  float lo, hi;
+  asm("{\n .reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  uint32_t o;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o) : "f"(hi * s), "f"(lo * s));
+  return o;
+}
 
 // One thread per 32-value scale block: 16 packed bytes + 1 scale byte -> 64 B.
 __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ packed,
@@ -18,20 +31,17 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const uint4 v = *reinterpret_cast<const uint4*>(packed + i * 16);
-    const ScaleMul sm = scale_mul(scale[i]);
+    const float s = e8m0_to_f32(scale[i]);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t* o = out + i * 16;   // 32 bf16 = 16 words
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(w[q]), sm);   // (n0, n4)
-      const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(w[q]), sm);   // (n1, n5)
-      const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(w[q]), sm);   // (n2, n6)
-      const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(w[q]), sm);   // (n3, n7)
-      // back to natural order: (n0,n1), (n2,n3), (n4,n5), (n6,n7)
-      o[4 * q + 0] = prmt(p0, p1, 0x5410u);
-      o[4 * q + 1] = prmt(p2, p3, 0x5410u);
-      o[4 * q + 2] = prmt(p0, p1, 0x7632u);
-      o[4 * q + 3] = prmt(p2, p3, 0x7632u);
+      uint32_t h0, h1, h2, h3;   // byte j of word q -> values 8q+2j, 8q+2j+1
+      e2m1x8_to_f16x2(w[q], h0, h1, h2, h3);
+      o[4 * q + 0] = f16x2_scale_to_bf16x2(h0, s);
+      o[4 * q + 1] = f16x2_scale_to_bf16x2(h1, s);
+      o[4 * q + 2] = f16x2_scale_to_bf16x2(h2, s);
+      o[4 * q + 3] = f16x2_scale_to_bf16x2(h3, s);
     }
   }
 }

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the kernel translation units and the C-ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -18,25 +19,31 @@ struct DecodeArgs {
   uint16_t* h;            // phase 1 output, bf16 [R, I]
   float* P;               // phase 2 weighted route outputs, fp32 [R, K]
   uint16_t* y;            // phase 2 output, bf16 [T, K]
-  float* parts;           // stream-K partials [warps][2][128]
-  int* item_ctr;          // [warps], zero between calls
+  float* parts;           // stream-K partials [CTAs][2][256]
+  int* item_ctr;          // [CTAs], zero between calls
   int* tile_ctr;          // [K / 16], zero between calls (phase 2)
   int32_t* status;        // [4] or null (phase 1 writes it)
-  size_t smem_bytes;      // dynamic shared memory of the launch (tables + staged rows)
 };
 
-constexpr int kDecodeWarpsPerCta = 16;
 constexpr int kMaxCtas = 256;            // grid cap; sizes the stream-K bookkeeping
 
-// Shared-memory routing tables of a decode CTA (the staged activation rows
-// follow them, 128-byte aligned).
-__host__ __device__ inline size_t decode_smem_bytes(int T, int topk, int E) {
-  const int R = T * topk;
-  return sizeof(int) * (size_t)(E /*cnt*/ + (E + 1) /*off*/ + E /*run*/ + E /*touched*/ +
-                                R /*lst*/ + 4 /*misc*/ + (E + 1) /*gbase*/);
-}
-cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, cudaStream_t stream,
-                          bool pdl);
+// Kernel parameter block of one decode phase: the weight tensor map (TMA
+// descriptor, 64-byte aligned) and the launch-time shared-memory plan.
+struct DecodeParams {
+  CUtensorMap tmap;       // packed weights of the phase as 2-D u8 [rows][row bytes]
+  DecodeArgs a;
+  int stages;             // weight pipeline depth (16 KB stages)
+  int rows_cap;           // activation rows whose prescale is tracked (>= routes)
+  int xs_rows_cap;        // activation rows staged in shared memory
+  int xs_stride;          // bytes per staged row (f16), = 64 mod 128
+};
+
+// Shared-memory plan of a decode phase for a given stage count; returns the
+// bytes needed before the staged activation rows (and their offset).
+size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int stages);
+
+cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_smem,
+                          const CUtensorMap& tmap, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);

@@ -100,6 +100,7 @@ def test_forward_rejects_bad_arguments_without_a_gpu(L):
     assert fwd(L, K=96, I=96, T=40, path=2) == m.ERR_SHAPE   # prefill needs multiples of 64
     assert fwd(L, hidden=VP(0x10008)) == m.ERR_ALIGN
     assert fwd(L, w13=VP(0x40004)) == m.ERR_ALIGN
+    assert fwd(L, s2=VP(0x70001)) == m.ERR_ALIGN
     assert fwd(L, out=VP(0x80002)) == m.ERR_ALIGN
     assert fwd(L, ws=VP(0x100080)) == m.ERR_ALIGN
     assert fwd(L, ws=None) == m.ERR_WORKSPACE
