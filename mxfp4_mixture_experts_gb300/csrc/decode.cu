@@ -247,6 +247,54 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
   }
 }
 
+// One stage (chunk) of the current item for one consumer warp: its 4 scale
+// blocks bi = 4cw .. 4cw+3 (those below nb), both m16 tiles. FAST: the item
+// has no E8M0 byte 0 or 255, so 2^(s-127) is a single shift. GLOB: some lane's
+// token row is not staged and is read (and converted) from global memory.
+template <bool FAST, bool GLOB>
+__device__ __forceinline__ void consume_stage(float (&acc)[2][4], const uint8_t* stg,
+                                              const uint8_t* sc, int b_lo, int nb, int cw,
+                                              int g, int t, const int (&aoff0)[2],
+                                              const int (&aoff1)[2], const int (&soff0)[2],
+                                              const int (&soff1)[2], const uint8_t* brow,
+                                              const uint16_t* bglob, float bmul) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int bi = cw * 4 + j;
+    if (bi < nb) {
+      const int b = b_lo + bi;
+      // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
+      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+      if (brow != nullptr) {
+        bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
+      } else if (GLOB && bglob != nullptr) {
+        bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
+      }
+      // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
+      const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
+        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
+        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+        e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
+        e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
+        float d[4];
+        // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
+        mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
+        mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
+        const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
+        const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
+        const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
+        acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
+        acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
+        acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
+        acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
+      }
+    }
+  }
+}
+
 template <int PHASE>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
@@ -354,16 +402,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   if (warp == 0) {
     if (lane == 0) {
       Cursor c = cursor_of_item(i_first, x);
-      int64_t item = i_first;
-      int k = 0, seq = 0;
+      int ch = (int)(cub - i_first * NC);
+      int k = 0, seq = 0, st = 0;
+      uint32_t phase = 0;      // parity of the current pass over the stages
       bool ok = true;
       for (int64_t u = cub; u < cue && ok; ++u) {
-        const int64_t it = u / NC;
-        const int ch = (int)(u - it * NC);
-        if (it != item) {
-          cursor_next_item(c, x);
-          item = it;
-        }
         if (u == cub || ch == 0) {
           const int slot = seq % kScaleSlots;
           if (seq >= kScaleSlots) ok = mbar_wait(&sempty[slot], ((seq / kScaleSlots) - 1) & 1);
@@ -371,8 +414,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           issue_scales<PHASE>(c, a, nblk, scale_base + slot * M.scale_slot, &sfull[slot]);
           ++seq;
         }
-        const int st = k % S;
-        if (k >= S) ok = mbar_wait(&empty[st], ((k / S) - 1) & 1);
+        if (k >= S) ok = mbar_wait(&empty[st], phase ^ 1u);
         if (!ok) break;
         uint8_t* dst = stage_base + (size_t)st * kStageBytes;
         // columns of 8 blocks that start inside the row (a partial last
@@ -387,6 +429,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         box_row<PHASE>(c, a, h), &full[st]);
         }
         ++k;
+        if (++st == S) {
+          st = 0;
+          phase ^= 1u;
+        }
+        if (++ch == NC) {
+          ch = 0;
+          cursor_next_item(c, x);
+        }
       }
       if (!ok && a.status != nullptr) atomicOr(&a.status[2], 1);
     }
@@ -408,11 +458,18 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   const int xs_rows = min(n_sh, P.xs_rows_cap);
 
   if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
+  // One warp per row: load the bf16 row once (kept raw in shared memory when
+  // the row is staged), take the largest exponent, then convert in place to
+  // f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact in f16 down to 2^-31 of
+  // the row maximum.
   for (int r = cw; r < n_sh; r += kConsumerWarps) {
     const uint4* src = reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r));
+    uint4* dst = reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride);
+    const bool staged = r < xs_rows;
     uint32_t emax = 0;
     for (int c16 = lane; c16 < kred / 8; c16 += 32) {
       const uint4 v = ldcg16(src + c16);
+      if (staged) dst[c16] = v;
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -422,24 +479,20 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-    if (lane == 0) {
-      // max |x| * 2^-sh in [2^14, 2^15): exact in f16 down to 2^-31 of the max
-      const int sh = emax == 0 ? 0 : (int)emax - 127 - 14;
-      row_sh[r] = max(-100, min(100, sh));
+    const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
+    if (lane == 0) row_sh[r] = sh;
+    if (staged) {
+      __syncwarp();
+      const float mul = pow2f(-sh);
+      for (int c16 = lane; c16 < kred / 8; c16 += 32) dst[c16] = bf16x8_to_f16x8(dst[c16], mul);
     }
-  }
-  named_barrier(kBarConsumers, kConsumerThreads);
-  for (int i = ctid; i < xs_rows * (kred / 8); i += kConsumerThreads) {
-    const int r = i / (kred / 8), c16 = i - r * (kred / 8);
-    const uint4 v = ldcg16(reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r)) + c16);
-    *reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride + c16 * 16) =
-        bf16x8_to_f16x8(v, pow2f(-row_sh[r]));
   }
   named_barrier(kBarConsumers, kConsumerThreads);
 
   Cursor c = c_first;
   int64_t item = i_first;
-  int k = 0, seq = 0;
+  int st = 0, seq = 0;
+  uint32_t phase = 0;
   float acc[2][4];
   bool special = false;          // the item has E8M0 bytes 0 or 255
   const uint8_t* sc = nullptr;   // scale rows of the item [32][nblk]
@@ -465,13 +518,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     }
   }
 
+  int ch = (int)(cub - i_first * NC);
+  bool glob = false;
   for (int64_t u = cub; u < cue; ++u) {
-    const int64_t it = u / NC;
-    const int ch = (int)(u - it * NC);
-    if (it != item) {
-      cursor_next_item(c, x);
-      item = it;
-    }
     if (item_start) {
       const int slot = seq % kScaleSlots;
       ok = ok && mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
@@ -498,6 +547,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           bmul = pow2f(-(r >= 0 && r < n_sh ? row_sh[r] : 0));
         }
       }
+      glob = __any_sync(0xffffffffu, bglob != nullptr);
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
@@ -505,49 +555,28 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       item_start = false;
     }
 
-    const int st = k % S;
-    ok = ok && mbar_wait(&full[st], (k / S) & 1);
+    ok = ok && mbar_wait(&full[st], phase);
     const uint8_t* stg = stage_base + (size_t)st * kStageBytes;
     const int b_lo = ch * kChunkBlocks;
-    const int b_hi = min(kChunkBlocks, nblk - b_lo);
-    const int bi_end = min(b_hi, cw * 4 + 4);
-    for (int bi = cw * 4; bi < bi_end; ++bi) {
-      const int b = b_lo + bi;
-      // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
-      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-      if (brow != nullptr) {
-        bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
-      } else if (bglob != nullptr) {
-        bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
-      }
-      // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
-      const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
-        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-        e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
-        e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
-        mma_f16_16816(d, a0, c0, a1, c1, bv.x, bv.y);
-        mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
-        const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
-        const float f0 = special ? e8m0_to_f32(sb0) : e8m0_to_f32_normal(sb0);
-        const float f1 = special ? e8m0_to_f32(sb1) : e8m0_to_f32_normal(sb1);
-        acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
-        acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
-        acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
-        acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
-      }
-    }
+    const int nb = min(kChunkBlocks, nblk - b_lo);
+    if (!special && !glob)
+      consume_stage<true, false>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
+    else if (!special)
+      consume_stage<true, true>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
+    else
+      consume_stage<false, true>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
-    ++k;
+    if (++st == S) {
+      st = 0;
+      phase ^= 1u;
+    }
 
     const bool item_end = (ch == NC - 1) || (u + 1 == cue);
-    if (!item_end) continue;
+    if (!item_end) {
+      ++ch;
+      continue;
+    }
 
     // ---- item end: reduce the 8 warps' fragments, then finish or publish
     float* my = red + ((size_t)cw * 2 * 32 + lane) * 4;
@@ -590,6 +619,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     if (lane == 0) mbar_arrive(&sempty[seq % kScaleSlots]);
     ++seq;
     item_start = true;
+    ch = 0;
+    ++item;
+    cursor_next_item(c, x);
   }
   if (!ok && lane == 0 && a.status != nullptr) atomicOr(&a.status[2], 1);
 }
