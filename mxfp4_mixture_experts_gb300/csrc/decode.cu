@@ -11,7 +11,7 @@
 //                  output tile sums the k slots of every token in slot order
 //                  and writes bf16 y [T, K].
 //
-// CTA = 1 producer warp + 8 consumer warps, one CTA per SM.
+// CTA = 1 producer warp + 12 consumer warps, one CTA per SM.
 //  * The producer streams weight tiles with 2-D TMA (cp.async.bulk.tensor,
 //    128-byte swizzle) into a ring of shared-memory stages, and each item's
 //    E8M0 scale rows with 1-D bulk copies; mbarriers track both.
@@ -26,7 +26,7 @@
 // Work decomposition. An *item* is (touched expert d, row tile nt, token
 // group gr): 32 weight rows against up to 8 of the expert's tokens (phase 1:
 // gate rows 16nt..16nt+15 and the matching up rows; phase 2: w2 rows
-// 32nt..32nt+31). Its K range is cut into *chunks* of 32 scale blocks (one
+// 32nt..32nt+31). Its K range is cut into *chunks* of 24 scale blocks (one
 // pipeline stage each). The (item, chunk) units are dealt to CTAs in equal
 // contiguous ranges, so every SM streams the same number of bytes whatever
 // the routing; an item cut between CTAs is finished by whichever CTA arrives
@@ -40,13 +40,14 @@
 
 namespace mxmoe {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 12;   // 13 warps: at most 4 per SM sub-partition, 128 registers each
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kGroup = 8;            // tokens per mma n-tile
 constexpr int kItemRows = 32;        // weight rows per item (two m16 tiles)
-constexpr int kChunkBlocks = 32;     // scale blocks per stage (4 TMA columns of 128 B)
-constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 16 KB
+constexpr int kChunkBlocks = 24;     // scale blocks per stage (3 TMA columns of 128 B)
+constexpr int kWarpBlocks = kChunkBlocks / kConsumerWarps;   // blocks per consumer warp per stage
+constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 12 KB
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 128 bytes
 constexpr int kScaleSlots = 3;
 constexpr int kBarConsumers = 1;     // named barrier id of the consumer warps
@@ -203,10 +204,11 @@ template <int PHASE>
 __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const DecodeArgs& a,
                             float* fin, int ctid, int p_lo, int n_sh, const int* row_sh,
                             int* flags) {
-  const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
+  const bool own = ctid < 256;     // threads 256.. only join the barriers
+  const int tt = (ctid >> 7) & 1, l = (ctid >> 2) & 31, q = ctid & 3;
   const int g = l >> 2, t = l & 3;
   const int col = 2 * t + (q & 1);
-  const int ntok = min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup);
+  const int ntok = own ? min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup) : 0;
   const int qpos = x.tb.off[c.e] + c.gr * kGroup + col;   // route-list position of the column
   float colmul = 1.0f;
   int r = -1;
@@ -216,7 +218,7 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
     colmul = pow2f(idx >= 0 && idx < n_sh ? row_sh[idx] : 0);
   }
   if (PHASE == 1) {
-    fin[ctid] = v;
+    if (own) fin[ctid] = v;
     named_barrier(kBarConsumers, kConsumerThreads);
     if (q < 2 && col < ntok) {
       const float gate = fin[ctid] * colmul, up = fin[ctid + 2] * colmul;
@@ -247,10 +249,48 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
   }
 }
 
-// One stage (chunk) of the current item for one consumer warp: its 4 scale
-// blocks bi = 4cw .. 4cw+3 (those below nb), both m16 tiles. FAST: the item
-// has no E8M0 byte 0 or 255, so 2^(s-127) is a single shift. GLOB: some lane's
-// token row is not staged and is read (and converted) from global memory.
+// One scale block b of the current item for one consumer warp, both m16 tiles.
+// FAST: no E8M0 byte 0 or 255 in the item, so 2^(s-127) is a single shift.
+// GLOB: this warp has a lane whose token row is read (and converted) from
+// global memory instead of the staged copy.
+template <bool FAST, bool GLOB>
+__device__ __forceinline__ void consume_block(float (&acc)[2][4], const uint8_t* stg,
+                                              const uint8_t* sc, int b, int bi, int g, int t,
+                                              const int (&aoff0)[2], const int (&aoff1)[2],
+                                              const int (&soff0)[2], const int (&soff1)[2],
+                                              const uint8_t* brow, const uint16_t* bglob,
+                                              float bmul) {
+  // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
+  uint4 bv = make_uint4(0u, 0u, 0u, 0u);
+  if (brow != nullptr) {
+    bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
+  } else if (GLOB && bglob != nullptr) {
+    bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
+  }
+  // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
+  const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
+#pragma unroll
+  for (int tt = 0; tt < 2; ++tt) {
+    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
+    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+    e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
+    e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
+    float d[4];
+    // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
+    mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
+    mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
+    const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
+    const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
+    const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
+    acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
+    acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
+    acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
+    acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
+  }
+}
+
+// One stage (chunk) for one consumer warp: its kWarpBlocks scale blocks.
 template <bool FAST, bool GLOB>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][4], const uint8_t* stg,
                                               const uint8_t* sc, int b_lo, int nb, int cw,
@@ -258,40 +298,18 @@ __device__ __forceinline__ void consume_stage(float (&acc)[2][4], const uint8_t*
                                               const int (&aoff1)[2], const int (&soff0)[2],
                                               const int (&soff1)[2], const uint8_t* brow,
                                               const uint16_t* bglob, float bmul) {
+  const int bi0 = cw * kWarpBlocks;
+  if (nb == kChunkBlocks) {      // full chunk: no guards, so the blocks interleave
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int bi = cw * 4 + j;
-    if (bi < nb) {
-      const int b = b_lo + bi;
-      // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
-      uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-      if (brow != nullptr) {
-        bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
-      } else if (GLOB && bglob != nullptr) {
-        bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
-      }
-      // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
-      const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
+    for (int j = 0; j < kWarpBlocks; ++j)
+      consume_block<FAST, GLOB>(acc, stg, sc, b_lo + bi0 + j, bi0 + j, g, t, aoff0, aoff1, soff0,
+                                soff1, brow, bglob, bmul);
+  } else {
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
-        uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-        e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
-        e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
-        float d[4];
-        // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
-        mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
-        mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
-        const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
-        const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
-        const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
-        acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
-        acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
-        acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
-        acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
-      }
-    }
+    for (int j = 0; j < kWarpBlocks; ++j)
+      if (bi0 + j < nb)
+        consume_block<FAST, GLOB>(acc, stg, sc, b_lo + bi0 + j, bi0 + j, g, t, aoff0, aoff1,
+                                  soff0, soff1, brow, bglob, bmul);
   }
 }
 
@@ -315,7 +333,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   uint64_t* empty = full + S;                                     // [S]
   uint64_t* sfull = empty + S;                                    // [kScaleSlots]
   uint64_t* sempty = sfull + kScaleSlots;                         // [kScaleSlots]
-  float* red = reinterpret_cast<float*>(smem + M.red);            // [8][2][32][4]
+  float* red = reinterpret_cast<float*>(smem + M.red);            // [warps][2][32][4]
   float* fin = reinterpret_cast<float*>(smem + M.fin);            // [256]
   int* flags = reinterpret_cast<int*>(smem + M.flags);
   RouteTables tb;
@@ -419,7 +437,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         uint8_t* dst = stage_base + (size_t)st * kStageBytes;
         // columns of 8 blocks that start inside the row (a partial last
         // column reads zeros past the row end)
-        const int ncols = min(4, (nblk - ch * kChunkBlocks + 7) / 8);
+        const int ncols = min(kChunkBlocks / 8, (nblk - ch * kChunkBlocks + 7) / 8);
         mbar_arrive_expect_tx(&full[st], ncols * 2 * kBoxBytes);
         const int x0 = ch * kChunkBlocks * 16;
         for (int col = 0; col < ncols; ++col) {
@@ -586,7 +604,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           make_float4(acc[tt][0], acc[tt][1], acc[tt][2], acc[tt][3]);
     named_barrier(kBarConsumers, kConsumerThreads);
     float v = 0.f;
-    {
+    if (ctid < 256) {
       const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
       for (int w = 0; w < kConsumerWarps; ++w) v += red[(((size_t)w * 2 + tt) * 32 + l) * 4 + q];
     }
@@ -598,7 +616,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       const int va = owner_of_unit(item * NC, U, nCta);
       const int vb = owner_of_unit(item * NC + NC - 1, U, nCta);
       const int slot = (item == i_first) ? 0 : 1;
-      a.parts[((size_t)blockIdx.x * 2 + slot) * 256 + ctid] = v;
+      if (ctid < 256) a.parts[((size_t)blockIdx.x * 2 + slot) * 256 + ctid] = v;
       __threadfence();
       named_barrier(kBarConsumers, kConsumerThreads);
       if (ctid == 0) flags[1] = atomicAdd(&a.item_ctr[va], 1);
@@ -607,7 +625,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         __threadfence();
         const bool va_first = range_begin(va, U, nCta) == item * NC;
         float tot = 0.f;
-        for (int w = va; w <= vb; ++w) {
+        for (int w = va; w <= vb && ctid < 256; ++w) {
           const int sl = (w == va && !va_first) ? 1 : 0;
           tot += ldcg_f32(a.parts + ((size_t)w * 2 + sl) * 256 + ctid);
         }
@@ -648,8 +666,8 @@ cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_s
   const int R = a.T * a.topk;
   p.rows_cap = R;
   p.xs_stride = (int)round_up((size_t)kred * 2, 128) + 64;
-  // deepest pipeline (up to 6 stages) that still leaves room for a few rows
-  int stages = 6;
+  // deepest pipeline (up to 8 stages) that still leaves room for a few rows
+  int stages = 8;
   size_t fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
   const size_t want_rows = (size_t)(R < 8 ? R : 8) * p.xs_stride;
   while (stages > 3 && fixed + want_rows > (size_t)max_smem) {
