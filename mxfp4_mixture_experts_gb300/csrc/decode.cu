@@ -79,7 +79,7 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, 
   m.fin = o;
   o += 256 * sizeof(float);
   m.flags = o;
-  o += 16;
+  o += 32;   // int flags[4] + a 16-byte zero chunk
   m.ints = o;
   o += (size_t)(5 * E + R + 6) * sizeof(int);
   m.row_sh = o;
@@ -249,67 +249,79 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
   }
 }
 
-// One scale block b of the current item for one consumer warp, both m16 tiles.
-// FAST: no E8M0 byte 0 or 255 in the item, so 2^(s-127) is a single shift.
-// GLOB: this warp has a lane whose token row is read (and converted) from
-// global memory instead of the staged copy.
-template <bool FAST, bool GLOB>
-__device__ __forceinline__ void consume_block(float (&acc)[2][4], const uint8_t* stg,
-                                              const uint8_t* sc, int b, int bi, int g, int t,
-                                              const int (&aoff0)[2], const int (&aoff1)[2],
-                                              const int (&soff0)[2], const int (&soff1)[2],
-                                              const uint8_t* brow, const uint16_t* bglob,
-                                              float bmul) {
-  // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7, f16
-  uint4 bv = make_uint4(0u, 0u, 0u, 0u);
-  if (brow != nullptr) {
-    bv = *reinterpret_cast<const uint4*>(brow + b * 64 + t * 16);
-  } else if (GLOB && bglob != nullptr) {
-    bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
-  }
-  // A: word t of block b in each row (box column bi/8, 128-byte swizzle)
-  const uint8_t* colp = stg + (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
-#pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(colp + aoff0[tt]);
-    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(colp + aoff1[tt]);
-    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-    e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
-    e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
-    float d[4];
-    // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
-    mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
-    mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
-    const uint32_t sb0 = sc[soff0[tt] + b], sb1 = sc[soff1[tt] + b];
-    const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
-    const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
-    acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
-    acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
-    acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
-    acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
-  }
-}
+// Lane-constant shared-memory offsets of the consumer warp's kWarpBlocks
+// blocks (bi = cw * kWarpBlocks + j) inside a stage / an item.
+struct LaneOffsets {
+  int a[kWarpBlocks][2][2];   // A word: [j][tile][row g | row g + 8], from the stage base
+  int s[kWarpBlocks][2][2];   // scale byte: [j][tile][row], from the item's scale rows + b_lo
+  int b[kWarpBlocks];         // B chunk: from the token row + 64 * b_lo
+};
 
-// One stage (chunk) for one consumer warp: its kWarpBlocks scale blocks.
+// One stage (chunk) of the current item for one consumer warp, both m16 tiles.
+// FAST: the item has no E8M0 byte 0 or 255, so 2^(s-127) is a single shift.
+// GLOB: some lane's token row is read (and converted) from global memory.
 template <bool FAST, bool GLOB>
 __device__ __forceinline__ void consume_stage(float (&acc)[2][4], const uint8_t* stg,
                                               const uint8_t* sc, int b_lo, int nb, int cw,
-                                              int g, int t, const int (&aoff0)[2],
-                                              const int (&aoff1)[2], const int (&soff0)[2],
-                                              const int (&soff1)[2], const uint8_t* brow,
-                                              const uint16_t* bglob, float bmul) {
-  const int bi0 = cw * kWarpBlocks;
-  if (nb == kChunkBlocks) {      // full chunk: no guards, so the blocks interleave
+                                              int t, const LaneOffsets& lo, const uint8_t* brow,
+                                              const uint8_t* zero16, const uint16_t* bglob,
+                                              float bmul) {
 #pragma unroll
-    for (int j = 0; j < kWarpBlocks; ++j)
-      consume_block<FAST, GLOB>(acc, stg, sc, b_lo + bi0 + j, bi0 + j, g, t, aoff0, aoff1, soff0,
-                                soff1, brow, bglob, bmul);
-  } else {
+  for (int j = 0; j < kWarpBlocks; ++j) {
+    if (nb < kChunkBlocks && cw * kWarpBlocks + j >= nb) break;
+    // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7 (f16); padding
+    // columns read a zero chunk
+    uint4 bv;
+    if (GLOB && bglob != nullptr) {
+      const int b = b_lo + cw * kWarpBlocks + j;
+      bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
+    } else {
+      const uint8_t* bp = brow != nullptr ? brow + b_lo * 64 + lo.b[j] : zero16;
+      bv = *reinterpret_cast<const uint4*>(bp);
+    }
 #pragma unroll
-    for (int j = 0; j < kWarpBlocks; ++j)
-      if (bi0 + j < nb)
-        consume_block<FAST, GLOB>(acc, stg, sc, b_lo + bi0 + j, bi0 + j, g, t, aoff0, aoff1,
-                                  soff0, soff1, brow, bglob, bmul);
+    for (int tt = 0; tt < 2; ++tt) {
+      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(stg + lo.a[j][tt][0]);
+      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(stg + lo.a[j][tt][1]);
+      const uint32_t sb0 = sc[b_lo + lo.s[j][tt][0]], sb1 = sc[b_lo + lo.s[j][tt][1]];
+      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+      e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
+      e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
+      float d[4];
+      // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
+      mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
+      mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
+      const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
+      const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
+      acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
+      acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
+      acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
+      acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
+    }
+  }
+}
+
+// All chunks [ch, ch_end) of one item: wait for each stage, consume, release.
+template <bool FAST, bool GLOB>
+__device__ __forceinline__ void consume_item(float (&acc)[2][4], uint8_t* stage_base,
+                                             uint64_t* full, uint64_t* empty, int S, int& st,
+                                             uint32_t& phase, bool& ok, const uint8_t* sc,
+                                             int ch, int ch_end, int nblk, int cw, int t,
+                                             int lane, const LaneOffsets& lo,
+                                             const uint8_t* brow, const uint8_t* zero16,
+                                             const uint16_t* bglob, float bmul) {
+  for (; ch < ch_end; ++ch) {
+    if (ok) ok = mbar_wait(&full[st], phase);
+    const int b_lo = ch * kChunkBlocks;
+    consume_stage<FAST, GLOB>(acc, stage_base + st * kStageBytes, sc, b_lo,
+                              min(kChunkBlocks, nblk - b_lo), cw, t, lo, brow, zero16, bglob,
+                              bmul);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+    if (++st == S) {
+      st = 0;
+      phase ^= 1u;
+    }
   }
 }
 
@@ -317,8 +329,9 @@ template <int PHASE>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base (128-byte swizzled TMA tiles); offsetting the array
+  // keeps the compiler's knowledge that these are shared-memory addresses
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const DecodeArgs& a = P.a;
   const int E = a.E, R = a.T * a.topk;
   const int kred = PHASE == 1 ? a.K : a.I;
@@ -352,6 +365,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   const int warp = tid >> 5, lane = tid & 31;
 
   if (PHASE == 1) grid_dependency_wait();   // inputs may come from the previous kernel
+  if (tid < 8) flags[tid] = 0;
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
@@ -511,92 +525,80 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   int64_t item = i_first;
   int st = 0, seq = 0;
   uint32_t phase = 0;
-  float acc[2][4];
-  bool special = false;          // the item has E8M0 bytes 0 or 255
-  const uint8_t* sc = nullptr;   // scale rows of the item [32][nblk]
-  const uint8_t* brow = nullptr; // staged f16 row of this lane's token column
-  const uint16_t* bglob = nullptr;   // or its global bf16 row (not staged)
-  float bmul = 1.0f;
-  bool item_start = true;
   bool ok = true;
-  // lane-constant parts of the A addresses: tile tt, rows g / g+8
-  int aoff0[2], aoff1[2], soff0[2], soff1[2];
+  float acc[2][4];
+  LaneOffsets lo;
 #pragma unroll
-  for (int tt = 0; tt < 2; ++tt) {
-    if (PHASE == 1) {
-      aoff0[tt] = 0 * kBoxBytes + (tt * 8 + g) * 128;
-      aoff1[tt] = 1 * kBoxBytes + (tt * 8 + g) * 128;
-      soff0[tt] = (tt * 8 + g) * nblk;
-      soff1[tt] = (16 + tt * 8 + g) * nblk;
-    } else {
-      aoff0[tt] = tt * kBoxBytes + g * 128;
-      aoff1[tt] = tt * kBoxBytes + (g + 8) * 128;
-      soff0[tt] = (tt * 16 + g) * nblk;
-      soff1[tt] = (tt * 16 + g + 8) * nblk;
+  for (int j = 0; j < kWarpBlocks; ++j) {
+    const int bi = cw * kWarpBlocks + j;
+    const int colsw = (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+      if (PHASE == 1) {   // box 0 = gate rows, box 1 = up rows; tile tt = rows tt*8 ..
+        lo.a[j][tt][0] = colsw + (tt * 8 + g) * 128;
+        lo.a[j][tt][1] = colsw + kBoxBytes + (tt * 8 + g) * 128;
+        lo.s[j][tt][0] = (tt * 8 + g) * nblk + bi;
+        lo.s[j][tt][1] = (16 + tt * 8 + g) * nblk + bi;
+      } else {            // box tt = rows 16tt .. 16tt+15
+        lo.a[j][tt][0] = colsw + tt * kBoxBytes + g * 128;
+        lo.a[j][tt][1] = colsw + tt * kBoxBytes + (g + 8) * 128;
+        lo.s[j][tt][0] = (tt * 16 + g) * nblk + bi;
+        lo.s[j][tt][1] = (tt * 16 + g + 8) * nblk + bi;
+      }
     }
+    lo.b[j] = bi * 64 + t * 16;
   }
+  const uint8_t* zero16 = reinterpret_cast<const uint8_t*>(flags + 4);   // B chunk of padding columns
 
   int ch = (int)(cub - i_first * NC);
-  bool glob = false;
-  for (int64_t u = cub; u < cue; ++u) {
-    if (item_start) {
-      const int slot = seq % kScaleSlots;
-      ok = ok && mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
-      sc = scale_base + slot * M.scale_slot;
-      int bad = 0;
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
-      for (int i = ctid; i < (kItemRows * nblk) / 4; i += kConsumerThreads) {
-        const uint32_t w = sw[i];
-        const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;     // some byte == 0
-        const uint32_t f = (~w - 0x01010101u) & w & 0x80808080u;     // some byte == 0xFF
-        bad |= (z | f) != 0u;
-      }
-      special = named_barrier_or(kBarConsumers, kConsumerThreads, bad != 0);
-      const int ntok = min(kGroup, tb.cnt[c.e] - c.gr * kGroup);
-      brow = nullptr;
-      bglob = nullptr;
-      if (g < ntok) {
-        const int qpos = tb.off[c.e] + c.gr * kGroup + g;
-        const int r = qpos - p_lo;
-        if (r >= 0 && r < xs_rows) {
-          brow = xs_base + (size_t)r * xs_stride;
-        } else {
-          bglob = act_row<PHASE>(a, tb, qpos);
-          bmul = pow2f(-(r >= 0 && r < n_sh ? row_sh[r] : 0));
-        }
-      }
-      glob = __any_sync(0xffffffffu, bglob != nullptr);
-#pragma unroll
-      for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) acc[tt][q] = 0.f;
-      item_start = false;
+  int64_t u = cub;
+  while (u < cue) {
+    // ---- item start: its scales, the special-byte flag, this lane's B row
+    const int slot = seq % kScaleSlots;
+    if (ok) ok = mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
+    const uint8_t* sc = scale_base + slot * M.scale_slot;
+    int bad = 0;
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
+    for (int i = ctid; i < (kItemRows * nblk) / 4; i += kConsumerThreads) {
+      const uint32_t w = sw[i];
+      const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;     // some byte == 0
+      const uint32_t f = (~w - 0x01010101u) & w & 0x80808080u;     // some byte == 0xFF
+      bad |= (z | f) != 0u;
     }
-
-    ok = ok && mbar_wait(&full[st], phase);
-    const uint8_t* stg = stage_base + (size_t)st * kStageBytes;
-    const int b_lo = ch * kChunkBlocks;
-    const int nb = min(kChunkBlocks, nblk - b_lo);
+    const bool special = named_barrier_or(kBarConsumers, kConsumerThreads, bad != 0);
+    const int ntok = min(kGroup, tb.cnt[c.e] - c.gr * kGroup);
+    const uint8_t* brow = nullptr;
+    const uint16_t* bglob = nullptr;
+    float bmul = 1.0f;
+    if (g < ntok) {
+      const int qpos = tb.off[c.e] + c.gr * kGroup + g;
+      const int r = qpos - p_lo;
+      if (r >= 0 && r < xs_rows) {
+        brow = xs_base + (size_t)r * xs_stride;
+      } else {
+        bglob = act_row<PHASE>(a, tb, qpos);
+        bmul = pow2f(-(r >= 0 && r < n_sh ? row_sh[r] : 0));
+      }
+    }
+    const bool glob = __any_sync(0xffffffffu, bglob != nullptr);
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[tt][q] = 0.f;
+    const int ch_end = (int)min((int64_t)NC, ch + (cue - u));
+    const int ch_start = ch;
     if (!special && !glob)
-      consume_stage<true, false>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
+      consume_item<true, false>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
+                                nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
     else if (!special)
-      consume_stage<true, true>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
+      consume_item<true, true>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
+                               nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
     else
-      consume_stage<false, true>(acc, stg, sc, b_lo, nb, cw, g, t, aoff0, aoff1, soff0, soff1, brow, bglob, bmul);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    if (++st == S) {
-      st = 0;
-      phase ^= 1u;
-    }
+      consume_item<false, true>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
+                                nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
+    u += ch_end - ch_start;
 
-    const bool item_end = (ch == NC - 1) || (u + 1 == cue);
-    if (!item_end) {
-      ++ch;
-      continue;
-    }
-
-    // ---- item end: reduce the 8 warps' fragments, then finish or publish
+    // ---- item end: reduce the warps' fragments, then finish or publish
     float* my = red + ((size_t)cw * 2 * 32 + lane) * 4;
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt)
@@ -608,15 +610,15 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
       for (int w = 0; w < kConsumerWarps; ++w) v += red[(((size_t)w * 2 + tt) * 32 + l) * 4 + q];
     }
-    const bool whole = (ch == NC - 1) && (item * NC >= cub);
+    const bool whole = (ch_end == NC) && (item * NC >= cub);
     if (whole) {
       finish_item<PHASE>(v, c, x, a, fin, ctid, p_lo, n_sh, row_sh, flags);
     } else {
       // partial item: publish, count, and let the last CTA to arrive finish it
       const int va = owner_of_unit(item * NC, U, nCta);
       const int vb = owner_of_unit(item * NC + NC - 1, U, nCta);
-      const int slot = (item == i_first) ? 0 : 1;
-      if (ctid < 256) a.parts[((size_t)blockIdx.x * 2 + slot) * 256 + ctid] = v;
+      const int pslot = (item == i_first) ? 0 : 1;
+      if (ctid < 256) a.parts[((size_t)blockIdx.x * 2 + pslot) * 256 + ctid] = v;
       __threadfence();
       named_barrier(kBarConsumers, kConsumerThreads);
       if (ctid == 0) flags[1] = atomicAdd(&a.item_ctr[va], 1);
@@ -636,7 +638,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     named_barrier(kBarConsumers, kConsumerThreads);
     if (lane == 0) mbar_arrive(&sempty[seq % kScaleSlots]);
     ++seq;
-    item_start = true;
     ch = 0;
     ++item;
     cursor_next_item(c, x);
