@@ -26,7 +26,7 @@
 // Work decomposition. An *item* is (touched expert d, row tile nt, token
 // group gr): 32 weight rows against up to 8 of the expert's tokens (phase 1:
 // gate rows 16nt..16nt+15 and the matching up rows; phase 2: w2 rows
-// 32nt..32nt+31). Its K range is cut into *chunks* of 24 scale blocks (one
+// 32nt..32nt+31). Its K range is cut into *chunks* of 48 scale blocks (one
 // pipeline stage each). The (item, chunk) units are dealt to CTAs in equal
 // contiguous ranges, so every SM streams the same number of bytes whatever
 // the routing; an item cut between CTAs is finished by whichever CTA arrives
@@ -45,9 +45,9 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kGroup = 8;            // tokens per mma n-tile
 constexpr int kItemRows = 32;        // weight rows per item (two m16 tiles)
-constexpr int kChunkBlocks = 24;     // scale blocks per stage (3 TMA columns of 128 B)
+constexpr int kChunkBlocks = 48;     // scale blocks per stage (6 TMA columns of 128 B)
 constexpr int kWarpBlocks = kChunkBlocks / kConsumerWarps;   // blocks per consumer warp per stage
-constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 12 KB
+constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 24 KB
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 128 bytes
 constexpr int kScaleSlots = 3;
 constexpr int kBarConsumers = 1;     // named barrier id of the consumer warps
@@ -228,12 +228,16 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
   } else {
     const int m = c.nt * kItemRows + tt * 16 + g + 8 * (q >> 1);
     if (col < ntok) a.P[(size_t)r * a.K + m] = a.wts[r] * (v * colmul);
-    __threadfence();
+    // the CTA barrier orders every thread's stores before thread 0's fence
+    // (cumulative), which releases them with the counter increment
     named_barrier(kBarConsumers, kConsumerThreads);
-    if (ctid == 0) flags[0] = atomicAdd(&a.tile_ctr[c.nt], 1);
+    if (ctid == 0) {
+      __threadfence();
+      flags[0] = atomicAdd(&a.tile_ctr[c.nt], 1);
+      __threadfence();
+    }
     named_barrier(kBarConsumers, kConsumerThreads);
     if (flags[0] != x.G - 1) return;
-    __threadfence();
     const int k = a.topk, m0 = c.nt * kItemRows;
     for (int idx = ctid; idx < a.T * kItemRows; idx += kConsumerThreads) {
       const int tok = idx / kItemRows, mm = m0 + idx % kItemRows;
@@ -619,12 +623,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       const int vb = owner_of_unit(item * NC + NC - 1, U, nCta);
       const int pslot = (item == i_first) ? 0 : 1;
       if (ctid < 256) a.parts[((size_t)blockIdx.x * 2 + pslot) * 256 + ctid] = v;
-      __threadfence();
       named_barrier(kBarConsumers, kConsumerThreads);
-      if (ctid == 0) flags[1] = atomicAdd(&a.item_ctr[va], 1);
+      if (ctid == 0) {
+        __threadfence();
+        flags[1] = atomicAdd(&a.item_ctr[va], 1);
+        __threadfence();
+      }
       named_barrier(kBarConsumers, kConsumerThreads);
       if (flags[1] == vb - va) {
-        __threadfence();
         const bool va_first = range_begin(va, U, nCta) == item * NC;
         float tot = 0.f;
         for (int w = va; w <= vb && ctid < 256; ++w) {
@@ -667,8 +673,8 @@ cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_s
   const int R = a.T * a.topk;
   p.rows_cap = R;
   p.xs_stride = (int)round_up((size_t)kred * 2, 128) + 64;
-  // deepest pipeline (up to 8 stages) that still leaves room for a few rows
-  int stages = 8;
+  // deepest pipeline (up to 5 stages) that still leaves room for a few rows
+  int stages = 5;
   size_t fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
   const size_t want_rows = (size_t)(R < 8 ? R : 8) * p.xs_stride;
   while (stages > 3 && fixed + want_rows > (size_t)max_smem) {

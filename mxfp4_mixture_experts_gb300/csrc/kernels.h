@@ -32,7 +32,7 @@ constexpr int kMaxCtas = 256;            // grid cap; sizes the stream-K bookkee
 struct DecodeParams {
   CUtensorMap tmap;       // packed weights of the phase as 2-D u8 [rows][row bytes]
   DecodeArgs a;
-  int stages;             // weight pipeline depth (12 KB stages)
+  int stages;             // weight pipeline depth (24 KB stages)
   int rows_cap;           // activation rows whose prescale is tracked (>= routes)
   int xs_rows_cap;        // activation rows staged in shared memory
   int xs_stride;          // bytes per staged row (f16), = 64 mod 128
