@@ -268,7 +268,7 @@ def time_phases(wl, steps: int, warmup: int):
         for s in range(warmup + steps):
             recs = []
             for ly in wl.step_layers(s):
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
                 moe.set_phase_events(ev)
                 wl.call(ly)
                 recs.append((ly, ev))
@@ -279,7 +279,8 @@ def time_phases(wl, steps: int, warmup: int):
             for ly, ev in recs:
                 t13 = ev[0].elapsed_time(ev[1])
                 t2 = ev[1].elapsed_time(ev[2])
-                per_T[ly["T"]].append((t13 + t2, ly))
+                tc = ev[2].elapsed_time(ev[3])
+                per_T[ly["T"]].append((t13 + t2 + tc, ly, (t13, t2, tc)))
                 sh = wl.shape
                 w13.append((ly["D"] * w13_bytes(sh.K, sh.I), t13))
     return per_T, w13
@@ -361,7 +362,8 @@ def run_ours(args, dist: Dist):
     for T, recs in per_T_raw.items():
         ms = statistics.median([r[0] for r in recs])
         b = statistics.mean([wl.alg_bytes(r[1]) for r in recs])
-        per_T[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
+        phases = [round(statistics.median([r[2][i] for r in recs]) * 1000, 2) for i in range(3)]
+        per_T[str(T)] = {"us": round(ms * 1000, 2), "phase_us": phases, "alg_bytes": int(b),
                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
                          "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
@@ -384,7 +386,7 @@ def run_ours(args, dist: Dist):
         "e2e": {"value": round(aggregate_us_per_call(e2e_ms, calls, dist.world), 3),
                 "unit": "us_per_call", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 2 * calls,
+        "gpu_launches": 3 * calls,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
     }

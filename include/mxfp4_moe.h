@@ -31,7 +31,9 @@
  *    int32[4]) by the enqueued work:
  *       status[0] = number of routes whose expert id is >= E (skipped)
  *       status[1] = number of distinct experts touched by the call
- *       status[2], status[3] = 0 (reserved)
+ *       status[2] = 1 when a bounded wait inside a kernel gave up (the output
+ *                   of that call is then not valid; never expected)
+ *       status[3] = 0 (reserved)
  *    Negative expert ids are padding and are skipped silently.
  *  - Every call is deterministic: repeating it on the same inputs gives
  *    bit-identical outputs (no floating-point atomics anywhere).
@@ -117,8 +119,9 @@ int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int
 
 /* Profiling hook: when events (host array of n cudaEvent_t handles, n >= 3)
  * is non-NULL, each later forward call on this process records events[0]
- * before its first kernel and events[i] after its i-th kernel, on its stream.
- * Pass NULL to turn it off. Not thread-safe; meant for benchmarks. */
+ * before its first kernel and events[i] after its i-th kernel (while i < n),
+ * on its stream; the decode path runs 3 kernels. Pass NULL to turn it off.
+ * Not thread-safe; meant for benchmarks. */
 void mxfp4_moe_set_phase_events(void* const* events, int n);
 
 /* Static description of an error code (never NULL). */

@@ -194,7 +194,6 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a.h = reinterpret_cast<uint16_t*>(ws + L.h);
     a.P = reinterpret_cast<float*>(ws + L.P);
     a.y = static_cast<uint16_t*>(out);
-    a.tile_ctr = reinterpret_cast<int*>(ws + L.tile_ctr);
     a.status = status;
     if (!get_encoder()) return MXFP4_MOE_ERR_CUDA;
     CUtensorMap map1, map2;
@@ -220,6 +219,9 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     e = launch_decode(a2, 2, ctas, d->max_smem, map2, s, g_phase_events == nullptr);
     if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     record_phase(2, s);
+    e = launch_combine(a.P, topk_ids, T, K, E, topk, a.y, d->num_sms, s, g_phase_events == nullptr);
+    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
+    record_phase(3, s);
     return MXFP4_MOE_OK;
   }
 

@@ -1,15 +1,16 @@
 // Decode kernels (1..32 tokens): the routed experts run straight from the
 // packed MXFP4 bytes ("MXFP4 MoE decode kernels", Design).
 //
-// Two launches per layer call:
+// Three launches per layer call (each may start while the previous one
+// drains: programmatic dependent launch):
 //   phase 1 (w13): per touched expert, gate and up rows are streamed once,
 //                  decoded in registers, multiplied with the expert's tokens
 //                  on the tensor cores and finished with SwiGLU -> bf16 h [R, I];
 //   phase 2 (w2):  per touched expert, the w2 rows are streamed the same way
-//                  against h, scaled by the routing weight into fp32 route
-//                  outputs P [R, K]; the last contribution to each 32-row
-//                  output tile sums the k slots of every token in slot order
-//                  and writes bf16 y [T, K].
+//                  against h and scaled by the routing weight into fp32 route
+//                  outputs P [R, K];
+//   combine:       y [T, K] = bf16 of the sum of each token's k route outputs,
+//                  in slot order.
 //
 // CTA = 1 producer warp + 12 consumer warps, one CTA per SM.
 //  * The producer streams weight tiles with 2-D TMA (cp.async.bulk.tensor,
@@ -226,30 +227,46 @@ __device__ void finish_item(float v, const Cursor& c, const Ctx& x, const Decode
       a.h[(size_t)r * a.I + n] = f32_to_bf16_rne(silu_f32(gate) * up);
     }
   } else {
+    // weighted route output; the slot-order sum over each token's routes is
+    // done by combine_kernel once every route is complete
     const int m = c.nt * kItemRows + tt * 16 + g + 8 * (q >> 1);
     if (col < ntok) a.P[(size_t)r * a.K + m] = a.wts[r] * (v * colmul);
-    // the CTA barrier orders every thread's stores before thread 0's fence
-    // (cumulative), which releases them with the counter increment
-    named_barrier(kBarConsumers, kConsumerThreads);
-    if (ctid == 0) {
-      __threadfence();
-      flags[0] = atomicAdd(&a.tile_ctr[c.nt], 1);
-      __threadfence();
+  }
+}
+
+// y[t][m] = bf16( sum over slots j = 0..k-1 with a valid expert of
+// P[t*k + j][m] ), in slot order (deterministic). 8 outputs per thread.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ P,
+                                                      const int32_t* __restrict__ ids, int T,
+                                                      int K, int E, int topk,
+                                                      uint16_t* __restrict__ y) {
+  grid_dependency_wait();   // P comes from the w2 phase
+  const int per_row = K / 8;
+  const int64_t n = (int64_t)T * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per_row), m8 = (int)(i - (int64_t)t * per_row) * 8;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < topk; ++j) {
+      const int r = t * topk + j;
+      const int e = ids[r];
+      if (e < 0 || e >= E) continue;
+      const uint4 lo = ldcg16(P + (size_t)r * K + m8);
+      const uint4 hi = ldcg16(P + (size_t)r * K + m8 + 4);
+      s[0] += __uint_as_float(lo.x);
+      s[1] += __uint_as_float(lo.y);
+      s[2] += __uint_as_float(lo.z);
+      s[3] += __uint_as_float(lo.w);
+      s[4] += __uint_as_float(hi.x);
+      s[5] += __uint_as_float(hi.y);
+      s[6] += __uint_as_float(hi.z);
+      s[7] += __uint_as_float(hi.w);
     }
-    named_barrier(kBarConsumers, kConsumerThreads);
-    if (flags[0] != x.G - 1) return;
-    const int k = a.topk, m0 = c.nt * kItemRows;
-    for (int idx = ctid; idx < a.T * kItemRows; idx += kConsumerThreads) {
-      const int tok = idx / kItemRows, mm = m0 + idx % kItemRows;
-      float s = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int rr = tok * k + j;
-        const int e = a.ids[rr];
-        if (e >= 0 && e < a.E) s += ldcg_f32(a.P + (size_t)rr * a.K + mm);
-      }
-      a.y[(size_t)tok * a.K + mm] = f32_to_bf16_rne(s);
-    }
-    if (ctid == 0) a.tile_ctr[c.nt] = 0;
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(s[2 * q + 1]), "f"(s[2 * q]));
+    *reinterpret_cast<uint4*>(y + (size_t)t * K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -418,16 +435,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   }
 
   const int64_t U = (int64_t)x.NT * x.G * NC;
-  if (U == 0) {
-    if (PHASE == 2) {   // no valid route at all: y is zero
-      grid_dependency_wait();
-      const int64_t n = (int64_t)a.T * a.K;
-      for (int64_t i = blockIdx.x * (int64_t)blockDim.x + tid; i < n;
-           i += (int64_t)gridDim.x * blockDim.x)
-        a.y[i] = 0;
-    }
-    return;
-  }
+  if (U == 0) return;   // no valid route at all (the combine writes y = 0)
   const int nCta = gridDim.x;
   const int64_t cub = range_begin(blockIdx.x, U, nCta);
   const int64_t cue = range_begin(blockIdx.x + 1, U, nCta);
@@ -649,6 +657,24 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     cursor_next_item(c, x);
   }
   if (!ok && lane == 0 && a.status != nullptr) atomicOr(&a.status[2], 1);
+}
+
+cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
+                           uint16_t* y, int num_sms, cudaStream_t stream, bool pdl) {
+  const int64_t n = (int64_t)T * (K / 8);
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > (int64_t)num_sms * 4) blocks = (int64_t)num_sms * 4;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, P, ids, T, K, E, topk, y);
 }
 
 size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int stages) {

@@ -21,7 +21,6 @@ struct DecodeArgs {
   uint16_t* y;            // phase 2 output, bf16 [T, K]
   float* parts;           // stream-K partials [CTAs][2][256]
   int* item_ctr;          // [CTAs], zero between calls
-  int* tile_ctr;          // [K / 16], zero between calls (phase 2)
   int32_t* status;        // [4] or null (phase 1 writes it)
 };
 
@@ -44,6 +43,9 @@ size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int st
 
 cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_smem,
                           const CUtensorMap& tmap, cudaStream_t stream, bool pdl);
+
+cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
+                           uint16_t* y, int num_sms, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);
