@@ -74,7 +74,7 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, 
   m.scale = o;
   o += kScaleSlots * m.scale_slot;
   m.bars = o;
-  o += round_up((size_t)(2 * stages + 2 * kScaleSlots) * 8, 16);
+  o += round_up((size_t)(2 * stages + 2 * kScaleSlots + 1) * 8, 16);
   m.red = o;
   o += (size_t)kConsumerWarps * 2 * 32 * 4 * sizeof(float);
   m.fin = o;
@@ -367,6 +367,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   uint64_t* empty = full + S;                                     // [S]
   uint64_t* sfull = empty + S;                                    // [kScaleSlots]
   uint64_t* sempty = sfull + kScaleSlots;                         // [kScaleSlots]
+  uint64_t* xfull = sempty + kScaleSlots;                         // staged activation rows
   float* red = reinterpret_cast<float*>(smem + M.red);            // [warps][2][32][4]
   float* fin = reinterpret_cast<float*>(smem + M.fin);            // [256]
   int* flags = reinterpret_cast<int*>(smem + M.flags);
@@ -396,6 +397,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sempty[i], kConsumerWarps);
     }
+    mbar_init(xfull, 1);
     fence_barrier_init();
     prefetch_tensormap(&P.tmap);
   }
@@ -442,9 +444,31 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   if (cub >= cue) return;
   const int64_t i_first = cub / NC, i_last = (cue - 1) / NC;
 
+  // activation rows this CTA can need: every route of the touched experts
+  // its unit range covers (a contiguous stretch of the route list)
+  const Cursor c_first = cursor_of_item(i_first, x);
+  const Cursor c_last = cursor_of_item(i_last, x);
+  const int p_lo = tb.off[c_first.e];
+  const int p_need = tb.off[c_last.e] + tb.cnt[c_last.e] - p_lo;
+  const int n_sh = min(p_need, P.rows_cap);
+  const int xs_rows = min(n_sh, P.xs_rows_cap);
+
   // ======================= producer warp =======================
   if (warp == 0) {
     if (lane == 0) {
+      // raw bf16 activation rows -> shared memory (converted by the consumers)
+      auto issue_rows = [&]() {
+        if (xs_rows == 0) return;
+        mbar_arrive_expect_tx(xfull, (uint32_t)xs_rows * kred * 2);
+        for (int r = 0; r < xs_rows; ++r)
+          bulk_load(xs_base + (size_t)r * xs_stride, act_row<PHASE>(a, tb, p_lo + r),
+                    (uint32_t)kred * 2, xfull);
+      };
+      bool rows_issued = false;
+      if (PHASE == 1) {
+        issue_rows();
+        rows_issued = true;
+      }
       Cursor c = cursor_of_item(i_first, x);
       int ch = (int)(cub - i_first * NC);
       int k = 0, seq = 0, st = 0;
@@ -458,7 +482,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           issue_scales<PHASE>(c, a, nblk, scale_base + slot * M.scale_slot, &sfull[slot]);
           ++seq;
         }
-        if (k >= S) ok = mbar_wait(&empty[st], phase ^ 1u);
+        if (k >= S) {
+          if (!rows_issued) {   // phase 2: h rows once phase 1 is complete
+            grid_dependency_wait();
+            issue_rows();
+            rows_issued = true;
+          }
+          ok = mbar_wait(&empty[st], phase ^ 1u);
+        }
         if (!ok) break;
         uint8_t* dst = stage_base + (size_t)st * kStageBytes;
         // columns of 8 blocks that start inside the row (a partial last
@@ -482,6 +513,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           cursor_next_item(c, x);
         }
       }
+      if (!rows_issued) {
+        grid_dependency_wait();
+        issue_rows();
+      }
       if (!ok && a.status != nullptr) atomicOr(&a.status[2], 1);
     }
     return;
@@ -492,28 +527,21 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   const int ctid = tid - 32;      // 0..255
   const int g = lane >> 2, t = lane & 3;
 
-  // activation rows this CTA can need: every route of the touched experts
-  // its unit range covers (a contiguous stretch of the route list)
-  const Cursor c_first = cursor_of_item(i_first, x);
-  const Cursor c_last = cursor_of_item(i_last, x);
-  const int p_lo = tb.off[c_first.e];
-  const int p_need = tb.off[c_last.e] + tb.cnt[c_last.e] - p_lo;
-  const int n_sh = min(p_need, P.rows_cap);
-  const int xs_rows = min(n_sh, P.xs_rows_cap);
 
   if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
-  // One warp per row: load the bf16 row once (kept raw in shared memory when
-  // the row is staged), take the largest exponent, then convert in place to
-  // f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact in f16 down to 2^-31 of
-  // the row maximum.
+  bool ok = true;
+  if (xs_rows > 0) ok = mbar_wait(xfull, 0);
+  // One warp per row: the largest exponent of the row, then (staged rows)
+  // conversion in place to f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact
+  // in f16 down to 2^-31 of the row maximum. Rows past the staged ones are
+  // only scanned (read from global memory when used).
   for (int r = cw; r < n_sh; r += kConsumerWarps) {
-    const uint4* src = reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r));
-    uint4* dst = reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride);
     const bool staged = r < xs_rows;
+    uint4* row = reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride);
+    const uint4* src = reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r));
     uint32_t emax = 0;
     for (int c16 = lane; c16 < kred / 8; c16 += 32) {
-      const uint4 v = ldcg16(src + c16);
-      if (staged) dst[c16] = v;
+      const uint4 v = staged ? row[c16] : ldcg16(src + c16);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -526,9 +554,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
     if (lane == 0) row_sh[r] = sh;
     if (staged) {
-      __syncwarp();
       const float mul = pow2f(-sh);
-      for (int c16 = lane; c16 < kred / 8; c16 += 32) dst[c16] = bf16x8_to_f16x8(dst[c16], mul);
+      for (int c16 = lane; c16 < kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
     }
   }
   named_barrier(kBarConsumers, kConsumerThreads);
@@ -537,7 +564,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   int64_t item = i_first;
   int st = 0, seq = 0;
   uint32_t phase = 0;
-  bool ok = true;
   float acc[2][4];
   LaneOffsets lo;
 #pragma unroll
