@@ -221,6 +221,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// A contiguous copy as pieces of at most 4 KB (larger single bulk copies were
+// seen never to complete their transaction count on this part).
+constexpr uint32_t kBulkPiece = 4096;
+__device__ __forceinline__ void bulk_load_split(void* dst, const void* src, uint32_t bytes,
+                                                uint64_t* bar) {
+  for (uint32_t o = 0; o < bytes; o += kBulkPiece)
+    bulk_load(static_cast<uint8_t*>(dst) + o, static_cast<const uint8_t*>(src) + o,
+              bytes - o < kBulkPiece ? bytes - o : kBulkPiece, bar);
+}
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

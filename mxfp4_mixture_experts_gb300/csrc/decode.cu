@@ -52,6 +52,8 @@ constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 24 KB
 constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 128 bytes
 constexpr int kScaleSlots = 3;
 constexpr int kBarConsumers = 1;     // named barrier id of the consumer warps
+constexpr int kRowBars = 16;         // barriers of the staged activation rows
+constexpr uint32_t kRowBarBytes = 32768;   // bytes tracked by one of them (at most)
 
 __host__ __device__ inline size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
@@ -74,7 +76,7 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, 
   m.scale = o;
   o += kScaleSlots * m.scale_slot;
   m.bars = o;
-  o += round_up((size_t)(2 * stages + 2 * kScaleSlots + 1) * 8, 16);
+  o += round_up((size_t)(2 * stages + 2 * kScaleSlots + kRowBars) * 8, 16);
   m.red = o;
   o += (size_t)kConsumerWarps * 2 * 32 * 4 * sizeof(float);
   m.fin = o;
@@ -162,10 +164,10 @@ __device__ __forceinline__ void issue_scales(const Cursor& c, const DecodeArgs& 
   const uint32_t run = 16u * nblk;
   mbar_arrive_expect_tx(bar, 2 * run);
   if (PHASE == 1) {
-    bulk_load(dst, a.wsc + (size_t)box_row<1>(c, a, 0) * nblk, run, bar);
-    bulk_load(dst + run, a.wsc + (size_t)box_row<1>(c, a, 1) * nblk, run, bar);
+    bulk_load_split(dst, a.wsc + (size_t)box_row<1>(c, a, 0) * nblk, run, bar);
+    bulk_load_split(dst + run, a.wsc + (size_t)box_row<1>(c, a, 1) * nblk, run, bar);
   } else {
-    bulk_load(dst, a.wsc + (size_t)box_row<2>(c, a, 0) * nblk, 2 * run, bar);
+    bulk_load_split(dst, a.wsc + (size_t)box_row<2>(c, a, 0) * nblk, 2 * run, bar);
   }
 }
 
@@ -367,7 +369,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   uint64_t* empty = full + S;                                     // [S]
   uint64_t* sfull = empty + S;                                    // [kScaleSlots]
   uint64_t* sempty = sfull + kScaleSlots;                         // [kScaleSlots]
-  uint64_t* xfull = sempty + kScaleSlots;                         // staged activation rows
+  uint64_t* xfull = sempty + kScaleSlots;                         // [kRowBars] staged rows
   float* red = reinterpret_cast<float*>(smem + M.red);            // [warps][2][32][4]
   float* fin = reinterpret_cast<float*>(smem + M.fin);            // [256]
   int* flags = reinterpret_cast<int*>(smem + M.flags);
@@ -397,7 +399,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sempty[i], kConsumerWarps);
     }
-    mbar_init(xfull, 1);
+    for (int i = 0; i < kRowBars; ++i) mbar_init(&xfull[i], 1);
     fence_barrier_init();
     prefetch_tensormap(&P.tmap);
   }
@@ -451,18 +453,23 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   const int p_lo = tb.off[c_first.e];
   const int p_need = tb.off[c_last.e] + tb.cnt[c_last.e] - p_lo;
   const int n_sh = min(p_need, P.rows_cap);
-  const int xs_rows = min(n_sh, P.xs_rows_cap);
+  // staged rows, tracked by kRowBars barriers of at most kRowBarBytes each
+  const int rows_per_bar = max(1, (int)(kRowBarBytes / ((uint32_t)kred * 2)));
+  const int xs_rows = min(min(n_sh, P.xs_rows_cap), rows_per_bar * kRowBars);
 
   // ======================= producer warp =======================
   if (warp == 0) {
     if (lane == 0) {
       // raw bf16 activation rows -> shared memory (converted by the consumers)
       auto issue_rows = [&]() {
-        if (xs_rows == 0) return;
-        mbar_arrive_expect_tx(xfull, (uint32_t)xs_rows * kred * 2);
-        for (int r = 0; r < xs_rows; ++r)
-          bulk_load(xs_base + (size_t)r * xs_stride, act_row<PHASE>(a, tb, p_lo + r),
-                    (uint32_t)kred * 2, xfull);
+        for (int r0 = 0; r0 < xs_rows; r0 += rows_per_bar) {
+          const int r1 = min(xs_rows, r0 + rows_per_bar);
+          uint64_t* bar = &xfull[r0 / rows_per_bar];
+          mbar_arrive_expect_tx(bar, (uint32_t)(r1 - r0) * kred * 2);
+          for (int r = r0; r < r1; ++r)
+            bulk_load_split(xs_base + (size_t)r * xs_stride, act_row<PHASE>(a, tb, p_lo + r),
+                            (uint32_t)kred * 2, bar);
+        }
       };
       bool rows_issued = false;
       if (PHASE == 1) {
@@ -530,7 +537,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
 
   if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
   bool ok = true;
-  if (xs_rows > 0) ok = mbar_wait(xfull, 0);
+  for (int i = 0; i * rows_per_bar < xs_rows; ++i) ok = ok && mbar_wait(&xfull[i], 0);
   // One warp per row: the largest exponent of the row, then (staged rows)
   // conversion in place to f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact
   // in f16 down to 2^-31 of the row maximum. Rows past the staged ones are

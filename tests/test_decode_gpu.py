@@ -26,9 +26,12 @@ def moe():
 
 def run(moe, case, path=1, workspace=None, status=None):
     g = case.to("cuda")
+    if status is None:
+        status = torch.zeros(4, dtype=torch.int32, device="cuda")
     y = moe.forward(g.hidden, g.topk_ids, g.topk_weights, g.w13, g.s13, g.w2, g.s2,
                     workspace=workspace, status=status, path=path)
     torch.cuda.synchronize()
+    assert int(status[2]) == 0, "a bounded wait inside a kernel gave up"
     return y
 
 
