@@ -31,9 +31,10 @@
  *    int32[4]) by the enqueued work:
  *       status[0] = number of routes whose expert id is >= E (skipped)
  *       status[1] = number of distinct experts touched by the call
- *       status[2] = 1 when a bounded wait inside a kernel gave up (the output
- *                   of that call is then not valid; never expected)
- *       status[3] = 0 (reserved)
+ *       status[2] = non-zero when a bounded wait inside a kernel gave up (the
+ *                   output of that call is then not valid; never expected);
+ *                   the bits name the wait, bits 8.. for the second kernel
+ *       status[3] = 1 + the first CTA that reported such a wait, else 0
  *    Negative expert ids are padding and are skipped silently.
  *  - Every call is deterministic: repeating it on the same inputs gives
  *    bit-identical outputs (no floating-point atomics anywhere).

@@ -165,7 +165,7 @@ namespace mxmoe {
 
 // Upper bound on polls of one mbarrier wait; a wait that runs out reports an
 // error through the status word instead of spinning forever.
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

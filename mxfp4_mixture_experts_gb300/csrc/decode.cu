@@ -471,11 +471,18 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             (uint32_t)kred * 2, bar);
         }
       };
+      // Phase 2 issues the h rows once phase 1 is complete, and always before
+      // its first blocking wait: the consumers need the rows before they can
+      // free any stage or scale slot.
       bool rows_issued = false;
-      if (PHASE == 1) {
+      auto ensure_rows = [&]() {
+        if (rows_issued) return;
+        if (PHASE == 2) grid_dependency_wait();
         issue_rows();
         rows_issued = true;
-      }
+      };
+      int fail_site = 0;
+      if (PHASE == 1) ensure_rows();
       Cursor c = cursor_of_item(i_first, x);
       int ch = (int)(cub - i_first * NC);
       int k = 0, seq = 0, st = 0;
@@ -484,20 +491,25 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
       for (int64_t u = cub; u < cue && ok; ++u) {
         if (u == cub || ch == 0) {
           const int slot = seq % kScaleSlots;
-          if (seq >= kScaleSlots) ok = mbar_wait(&sempty[slot], ((seq / kScaleSlots) - 1) & 1);
-          if (!ok) break;
+          if (seq >= kScaleSlots) {
+            ensure_rows();
+            ok = mbar_wait(&sempty[slot], ((seq / kScaleSlots) - 1) & 1);
+          }
+          if (!ok) {
+            fail_site |= 1;
+            break;
+          }
           issue_scales<PHASE>(c, a, nblk, scale_base + slot * M.scale_slot, &sfull[slot]);
           ++seq;
         }
         if (k >= S) {
-          if (!rows_issued) {   // phase 2: h rows once phase 1 is complete
-            grid_dependency_wait();
-            issue_rows();
-            rows_issued = true;
-          }
+          ensure_rows();
           ok = mbar_wait(&empty[st], phase ^ 1u);
         }
-        if (!ok) break;
+        if (!ok) {
+          fail_site |= 2;
+          break;
+        }
         uint8_t* dst = stage_base + (size_t)st * kStageBytes;
         // columns of 8 blocks that start inside the row (a partial last
         // column reads zeros past the row end)
@@ -520,11 +532,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
           cursor_next_item(c, x);
         }
       }
-      if (!rows_issued) {
-        grid_dependency_wait();
-        issue_rows();
+      ensure_rows();
+      if (fail_site != 0 && a.status != nullptr) {
+        atomicOr(&a.status[2], fail_site << (PHASE == 1 ? 0 : 8));
+        atomicCAS(&a.status[3], 0, blockIdx.x + 1);
       }
-      if (!ok && a.status != nullptr) atomicOr(&a.status[2], 1);
     }
     return;
   }
@@ -537,7 +549,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
 
   if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
   bool ok = true;
+  int fail_site = 0;
   for (int i = 0; i * rows_per_bar < xs_rows; ++i) ok = ok && mbar_wait(&xfull[i], 0);
+  if (!ok) fail_site |= 4;
   // One warp per row: the largest exponent of the row, then (staged rows)
   // conversion in place to f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact
   // in f16 down to 2^-31 of the row maximum. Rows past the staged ones are
@@ -600,7 +614,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   while (u < cue) {
     // ---- item start: its scales, the special-byte flag, this lane's B row
     const int slot = seq % kScaleSlots;
-    if (ok) ok = mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
+    if (ok) {
+      ok = mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
+      if (!ok) fail_site |= 8;
+    }
     const uint8_t* sc = scale_base + slot * M.scale_slot;
     int bad = 0;
     const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
@@ -689,7 +706,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     ++item;
     cursor_next_item(c, x);
   }
-  if (!ok && lane == 0 && a.status != nullptr) atomicOr(&a.status[2], 1);
+  if (!ok && lane == 0 && a.status != nullptr) {
+    atomicOr(&a.status[2], (fail_site | 16) << (PHASE == 1 ? 0 : 8));
+    atomicCAS(&a.status[3], 0, blockIdx.x + 1);
+  }
 }
 
 cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
