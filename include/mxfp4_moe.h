@@ -109,6 +109,35 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
                       void* workspace, size_t workspace_bytes,
                       int path, void* stream);
 
+/* The forward call for callers that cannot allocate device memory. The pages
+ * have no counterpart of this entry point: it is a convenience of this
+ * library. Some callers may not call cudaMalloc at all -- code that runs under
+ * a host framework that owns every device allocation (a plugin interface that
+ * hands out no scratch space), latency-critical serving loops that must never
+ * synchronise the device (cudaMalloc and cudaFree can), or pipelines that fix
+ * their memory footprint before they start. This variant takes the same
+ * arguments as mxfp4_moe_forward without the workspace, and uses instead a
+ * fixed device array of MXFP4_MOE_NOALLOC_BYTES bytes compiled into the
+ * library: every GPU that loads the library holds that array until the
+ * process exits. Nothing is allocated by this call (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *  - Sizes whose mxfp4_moe_workspace_size(T, K, I, E, topk) exceeds
+ *    MXFP4_MOE_NOALLOC_BYTES are rejected with MXFP4_MOE_ERR_WORKSPACE (the
+ *    decode path of the four workload shapes fits up to T = 32).
+ *  - The first call on a device performs the set-up for that device (looks up
+ *    the array's device address and clears its bookkeeping part on `stream`);
+ *    make that first call before any stream capture.
+ *  - All calls share the one array, and it keeps the last call's contents:
+ *    calls whose work may overlap on the GPU (different streams without
+ *    ordering) race on it; issue them on one stream or order them. */
+#define MXFP4_MOE_NOALLOC_BYTES (16u * 1024u * 1024u)
+int mxfp4_moe_forward_noalloc(const void* hidden, const int32_t* topk_ids,
+                              const float* topk_weights,
+                              const uint8_t* w13, const uint8_t* s13,
+                              const uint8_t* w2, const uint8_t* s2,
+                              int T, int K, int I, int E, int topk,
+                              void* out, int32_t* status, int path, void* stream);
+
 /* Dequantise packed rows to bf16 ("MXFP4 MoE decode kernels", Prefill:
  * mxk_deq unpacks an expert's MXFP4 weights straight to bf16).
  *   packed uint8 [rows, cols/2], scale uint8 [rows, cols/32] -> out bf16 [rows, cols]
