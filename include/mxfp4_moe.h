@@ -33,7 +33,9 @@
  *       status[1] = number of distinct experts touched by the call
  *       status[2] = non-zero when a bounded wait inside a kernel gave up (the
  *                   output of that call is then not valid; never expected);
- *                   the bits name the wait, bits 8.. for the second kernel
+ *                   the bits name the wait: bits 0..7 the decode path's first
+ *                   kernel, 8..15 its second, 16..23 the prefill path's first
+ *                   GEMM, 24..31 its second
  *       status[3] = 1 + the first CTA that reported such a wait, else 0
  *    Negative expert ids are padding and are skipped silently.
  *  - Every call is deterministic: repeating it on the same inputs gives

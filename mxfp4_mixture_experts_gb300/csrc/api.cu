@@ -93,7 +93,7 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
   size_t item_ctr1, item_ctr2, tile_ctr, pf_ctr;          // zero-kept
-  size_t parts1, parts2, h, P, rcount, roffset, rlist, xp, hp;   // scratch
+  size_t parts1, parts2, h, P, rcount, roffset, rlist, xp;   // scratch
   size_t total;
 };
 
@@ -123,7 +123,6 @@ Layout layout(int T, int K, int I, int E, int topk) {
   L.roffset = take((size_t)(E + 1) * sizeof(int));
   L.rlist = take(R * sizeof(int));
   L.xp = take(R * K * 2);
-  L.hp = take(R * I * 2);
   L.total = o;
   return L;
 }
@@ -136,6 +135,21 @@ void record_phase(int i, cudaStream_t s) {
 }
 
 }  // namespace
+
+namespace mxmoe {
+bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0,
+                     uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+                     CUtensorMapSwizzle swizzle) {
+  if (!get_encoder()) return false;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode_tiled(m, type, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace mxmoe
 
 extern "C" {
 
@@ -244,7 +258,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   p.offset = reinterpret_cast<int32_t*>(ws + L.roffset);
   p.list = reinterpret_cast<int32_t*>(ws + L.rlist);
   p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
-  p.hp = reinterpret_cast<uint16_t*>(ws + L.hp);
+  p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
   p.P = reinterpret_cast<float*>(ws + L.P);
   p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
   p.num_sms = d->num_sms;

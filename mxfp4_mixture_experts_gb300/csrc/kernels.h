@@ -47,6 +47,12 @@ cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_s
 cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
                            uint16_t* y, int num_sms, cudaStream_t stream, bool pdl);
 
+// 2-D tiled tensor map [dim1 rows][dim0 elements] with the given row pitch,
+// box {box0, box1}; reads past the tensor return zeros (api.cu).
+bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0,
+                     uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+                     CUtensorMapSwizzle swizzle);
+
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);
 
