@@ -8,8 +8,10 @@ uses its own layer's weights (8 distinct layers, 1.69 GB of packed weights
 each), so between two uses of one layer the other calls stream >= 2 GB and
 the 129 MB L2 holds nothing useful: inputs are larger than L2.
 
-``--workload prefill`` times the glm256 prefill chunk (T = 8192, 65,536
-token-expert pairs) instead.
+``--workload prefill`` times the prefill chunk on the 6144 x 2048 shape
+instead (T = 8192 tokens, 256 experts, top-8 sigmoid routing: 65,536
+token-expert pairs) and reports TFLOP/s of the two grouped GEMMs; the default
+line carries the same measurement, shorter, under ``prefill``.
 
 Printed: one JSON line (rank 0). ``value`` is microseconds per MoE call
 (whole job: all calls of all ranks / time), taken from CUDA-graph replays of
@@ -216,6 +218,194 @@ def decode_config(s, tokens, layers):
             "weights": "uniform random MXFP4 bytes, E8M0 scales 118..124 (synthetic)"}
 
 
+class PrefillWorkload:
+    """One prefill chunk: T = 8192 tokens on the 6144 x 2048, 256-expert,
+    top-8 shape. 4.8 GB of packed weights and 805 MB of permuted activations
+    per call: inputs larger than L2."""
+    name = "prefill256"
+    T = 8192
+
+    def __init__(self, dev):
+        from mxfp4_mixture_experts_gb300 import moe
+        self.moe = moe
+        self.shape = s = synth.SHAPES[self.name]
+        self.dev = dev
+        rng = np.random.Generator(np.random.PCG64(self.T))
+        hidden, logits, ids, w = synth.draw_activations(s, self.T, rng)
+        self.w13, self.s13, self.w2, self.s2 = synth.draw_weights_cuda(s, seed=0, layer=0,
+                                                                      device=dev)
+        self.hidden, self.ids, self.w = hidden.to(dev), ids.to(dev), w.to(dev)
+        self.host_hidden, self.host_ids, self.host_w = (hidden.pin_memory(), ids.pin_memory(),
+                                                        w.pin_memory())
+        self.out = torch.empty(self.T, s.K, dtype=torch.bfloat16, device=dev)
+        self.host_out = torch.empty(self.T, s.K, dtype=torch.bfloat16).pin_memory()
+        self.ws = moe.new_workspace(self.T, s.K, s.I, s.E, s.topk, dev)
+        ids_np = ids.numpy()
+        self.routes = int(((ids_np >= 0) & (ids_np < s.E)).sum())
+        self.D = touched_experts(self.ids, s.E)
+
+    def flops(self):
+        """(GEMM1, GEMM2) multiply-add flops: 2 per MAC over the valid routes."""
+        s = self.shape
+        return 2.0 * self.routes * s.K * 2 * s.I, 2.0 * self.routes * s.I * s.K
+
+    def call(self, stream=None):
+        self.moe.forward(self.hidden, self.ids, self.w, self.w13, self.s13, self.w2, self.s2,
+                         out=self.out, workspace=self.ws, path=2, stream=stream)
+
+    def call_e2e(self, stream):
+        self.hidden.copy_(self.host_hidden, non_blocking=True)
+        self.ids.copy_(self.host_ids, non_blocking=True)
+        self.w.copy_(self.host_w, non_blocking=True)
+        self.call(stream)
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        s = self.shape
+        return self.T * s.K * 2 + 2 * self.T * s.topk * 4, self.T * s.K * 2
+
+    def config(self):
+        s = self.shape
+        return {"workload": "prefill chunk: MoE layer K=6144, I=2048, 256 experts, top-8 "
+                            "sigmoid routing, T=8192 tokens (65,536 token-expert pairs)",
+                "K": s.K, "I": s.I, "E": s.E, "topk": s.topk, "tokens": self.T,
+                "l2": "inputs larger than L2: 4.8 GB packed weights, 805 MB permuted "
+                      "activations per call",
+                "weights": "uniform random MXFP4 bytes, E8M0 scales 118..124 (synthetic)"}
+
+
+def time_prefill(wl: PrefillWorkload, steps: int, warmup: int, dist: Dist):
+    """Graph-replayed calls (headline), then per-kernel events, then e2e."""
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        wl.call()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        wl.call()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    stream.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    torch.cuda.synchronize()
+    dist.barrier()
+    ck = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    # per kernel: events 0..4 around route+gather, GEMM1, GEMM2, combine
+    from mxfp4_mixture_experts_gb300 import moe
+    phases = []
+    with torch.cuda.stream(stream):
+        for i in range(warmup + steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            moe.set_phase_events(ev)
+            wl.call()
+            moe.set_phase_events(None)
+            stream.synchronize()
+            if i >= warmup:
+                phases.append([ev[j].elapsed_time(ev[j + 1]) for j in range(4)])
+    # end to end through the public call with host buffers
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            wl.call_e2e(stream)
+        stream.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            wl.call_e2e(stream)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    return ms, phases, e2e_ms, ck, t_wall
+
+
+def prefill_cpu_sample(wl: PrefillWorkload, budget_s: float = 15.0):
+    """The oracle on a bounded sample of the chunk's tokens (first 4 tokens,
+    then more until about budget_s), scaled to TFLOP/s."""
+    from oracle import mxfp4_moe_oracle as O
+    s = wl.shape
+    ids = wl.ids.cpu().numpy().astype(np.int64)
+    hb = wl.hidden.cpu().view(torch.int16).numpy().view(np.uint16)
+    w = wl.w.cpu().numpy()
+    done, flops, el = 0, 0.0, 0.0
+    n = 4
+    while el < budget_s and done + n <= wl.T:
+        tok = np.arange(done, done + n)
+        sub = ids[tok]
+        used = np.unique(sub[(sub >= 0) & (sub < s.E)])
+        remap = np.full(s.E, -1)
+        remap[used] = np.arange(len(used))
+        idx = torch.as_tensor(used, device=wl.w13.device)
+        host = [t.index_select(0, idx).cpu().numpy() for t in (wl.w13, wl.s13, wl.w2, wl.s2)]
+        t0 = time.perf_counter()
+        O.forward(hb[tok], remap[sub], w[tok], *host)
+        el += time.perf_counter() - t0
+        flops += 2.0 * int(((sub >= 0) & (sub < s.E)).sum()) * 3 * s.I * s.K
+        done += n
+        n *= 2
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"the first {done} of the chunk's 8192 tokens through the float64 numpy "
+                      f"oracle ({el:.1f} s of CPU work), flops of the sampled routes / time"}
+
+
+def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+    wl = PrefillWorkload(dev)
+    ms, phases, e2e_ms, clocks, t_wall = time_prefill(wl, steps, warmup, dist)
+    ms, e2e_ms = dist.max(ms), dist.max(e2e_ms)
+    f1, f2 = wl.flops()
+    tflops = (f1 + f2) * dist.world * steps / (ms * 1e-3) / 1e12
+    med = [statistics.median([p[j] for p in phases]) for j in range(4)]
+    peak = peaks["bf16_tflops"]
+    g1 = f1 / (med[1] * 1e-3) / 1e12
+    g2 = f2 / (med[2] * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": round(tflops, 1), "unit": "TFLOP/s",
+        "n_gpus": dist.world, "steps": steps, "warmup": warmup,
+        "ms_per_step": round(ms / steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": wl.config(),
+        "phase_ms": {"route_gather": round(med[0], 4), "gemm1": round(med[1], 4),
+                     "gemm2": round(med[2], 4), "combine": round(med[3], 4)},
+        "gemm_tflops": {"gemm1": round(g1, 1), "gemm2": round(g2, 1)},
+        "roofline": {"kernel": "gemm_kernel<1> (w13 grouped GEMM + SwiGLU)", "bound": "tensor",
+                     "achieved": round(g1, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(g1 / peak, 3), "peak_kind": peak_kind + " bf16 burst",
+                     "traffic": None, "alg_flops_per_launch": f1,
+                     "avg_launch_us": round(med[1] * 1000, 1)},
+        "e2e": {"value": round((f1 + f2) * dist.world * steps / (e2e_ms * 1e-3) / 1e12, 1),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": wl.e2e_bytes()[0],
+                "d2h_bytes_per_step": wl.e2e_bytes()[1]},
+        "gpu_launches": 5 * steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if cpu and dist.rank == 0:
+        out["cpu_baseline"] = prefill_cpu_sample(wl)
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     """Headline timing: each step is captured once as a CUDA graph (two graphs
@@ -347,8 +537,8 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     peaks, peak_kind = load_peaks()
-    if args.workload != "gptoss128":
-        raise SystemExit(f"workload {args.workload} is not wired into the benchmark yet")
+    if args.workload == "prefill":
+        return run_prefill(args, dist, args.steps, args.warmup, not args.no_cpu_baseline)
     wl = DecodeWorkload(dev)
     elapsed_ms, clocks, t_wall = time_graph_loop(wl, args.steps, args.warmup, dist)
     elapsed_ms = dist.max(elapsed_ms)
@@ -392,6 +582,13 @@ def run_ours(args, dist: Dist):
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_oracle_sample(wl)
+    if not args.no_prefill:
+        del wl
+        torch.cuda.empty_cache()
+        pf = run_prefill(args, dist, 10, 3, False)
+        out["prefill"] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "config",
+                                             "phase_ms", "gemm_tflops", "roofline", "e2e",
+                                             "gpu_launches", "clocks")}
     return out
 
 
@@ -447,7 +644,11 @@ def run_profile_case(args):
     from mxfp4_mixture_experts_gb300 import moe
     name, T = args.profile_case.split(":")
     T = int(T)
-    shape = synth.SHAPES[name]
+    if name in synth.SHAPES:
+        shape = synth.SHAPES[name]
+    else:   # "K,I,E,topk": a smaller layer of the same kind, for counter captures
+        K, I, E, k = (int(v) for v in name.split(","))
+        shape = synth.custom_shape(K, I, E, k, scoring="sigmoid_renorm")
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     hidden, _, ids, w = synth.draw_activations(shape, T, np.random.Generator(np.random.PCG64(T)))
@@ -470,8 +671,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gptoss128", choices=["gptoss128", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave the shorter prefill measurement out of the default line")
     ap.add_argument("--profile-case", default=None,
-                    help="NAME:T -- run warmup+steps calls of one layer, untimed (for ncu)")
+                    help="NAME:T or K,I,E,topk:T -- run warmup+steps calls of one layer, "
+                         "untimed (for ncu)")
     args = ap.parse_args()
     if args.profile_case:
         run_profile_case(args)
