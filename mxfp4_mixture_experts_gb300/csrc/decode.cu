@@ -339,6 +339,9 @@ __device__ __forceinline__ void consume_item(float (&acc)[2][4], uint8_t* stage_
     consume_stage<FAST, GLOB>(acc, stage_base + st * kStageBytes, sc, b_lo,
                               min(kChunkBlocks, nblk - b_lo), cw, t, lo, brow, zero16, bglob,
                               bmul);
+    // the stage is refilled by tensor copies (async proxy): order the generic
+    // reads of it before that write
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
     if (++st == S) {
@@ -699,6 +702,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         if (ctid == 0) a.item_ctr[va] = 0;
       }
     }
+    fence_proxy_async_smem();   // scale slot: refilled by a bulk copy (async proxy)
     named_barrier(kBarConsumers, kConsumerThreads);
     if (lane == 0) mbar_arrive(&sempty[seq % kScaleSlots]);
     ++seq;

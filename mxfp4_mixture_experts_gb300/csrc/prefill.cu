@@ -28,19 +28,22 @@
 
 namespace mxmoe {
 
-constexpr int kPfWarps = 12;
+constexpr int kPfWarps = 16;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kBM = 128;                  // tokens per m-tile
 constexpr int kBN = 128;                  // weight rows per tile
 constexpr int kBK = 64;                   // K values per stage (128 bytes of bf16)
 constexpr int kMT = 2;                    // m-tiles per tile
-constexpr int kSA = 3, kSP = 4, kSB = 3;  // ring depths: activations, packed, bf16 weights
+// ring depths: activations (from L2), packed weights (from DRAM: deepest), bf16 weights
+constexpr int kSA = 3, kSP = 12, kSB = 4;
 constexpr int kATile = kBM * kBK * 2;     // 16 KB
 constexpr int kAStage = kMT * kATile;     // 32 KB
 constexpr int kPStage = kBN * kBK / 2;    // 4 KB of packed bytes
 constexpr int kBStage = kBN * kBK * 2;    // 16 KB of bf16
 constexpr int kTmemCols = 512;            // 2 buffers x 2 m-tiles x 128 fp32 columns
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpEpi = 4, kWarpDeq = 8;
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmaW = 2, kWarpEpi = 4, kWarpDeq = 8;
+constexpr int kDeqWarps = 8;              // two threads per weight row, one 32-value block each
+constexpr int kScaleAhead = 8;            // k-stages of scale bytes held in registers
 constexpr int kTokensPerTile = kMT * kBM;
 
 struct GemmParams {
@@ -119,8 +122,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   const int E = p.E;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSA; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
-    for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], 4); }
-    for (int i = 0; i < kSB; ++i) { mbar_init(&b_full[i], 4); mbar_init(&b_empty[i], 1); }
+    for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kDeqWarps); }
+    for (int i = 0; i < kSB; ++i) { mbar_init(&b_full[i], kDeqWarps); mbar_init(&b_empty[i], 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
     mbar_init(drain, 1);
     fence_barrier_init();
@@ -154,13 +157,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   int fail = 0;
 
   if (warp == kWarpTma && lane == 0) {
-    // ------------------------------------------------------------ producer
-    int sa = 0, sp = 0, ka = 0, kp = 0;
-    uint32_t pa = 0, pp = 0, apar = 0, ppar = 0;   // parity of each stage's last fill
+    // ------------------------------------------------------------ activation producer
+    int sa = 0, ka = 0;
+    uint32_t pa = 0, apar = 0;   // parity of each stage's last fill
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
       const int m0 = p.offset[id.e] + id.mp * kTokensPerTile;
-      const int r0 = weight_row<PHASE>(id, p, 0), r1 = weight_row<PHASE>(id, p, 64);
       for (int kc = 0; kc < nK; ++kc) {
         if (ka >= kSA && !mbar_wait(&a_empty[sa], pa ^ 1u)) { fail = 1; break; }
         apar = (apar & ~(1u << sa)) | (pa << sa);
@@ -169,6 +171,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           tma_load_2d(sA + sa * kAStage + mt * kATile, &p.tmapA, kc * kBK, m0 + mt * kBM, &a_full[sa]);
         if (++sa == kSA) { sa = 0; pa ^= 1u; }
         ++ka;
+      }
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    for (int i = 0; i < kSA && i < ka; ++i) mbar_wait(&a_full[i], (apar >> i) & 1u);
+  } else if (warp == kWarpTmaW && lane == 0) {
+    // ------------------------------------------------------------ packed-weight producer
+    // runs up to kSP stages ahead of the dequant warps, across tile boundaries
+    int sp = 0, kp = 0;
+    uint32_t pp = 0, ppar = 0;
+    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
+      const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
+      const int r0 = weight_row<PHASE>(id, p, 0), r1 = weight_row<PHASE>(id, p, 64);
+      for (int kc = 0; kc < nK; ++kc) {
         if (kp >= kSP && !mbar_wait(&p_empty[sp], pp ^ 1u)) { fail = 2; break; }
         ppar = (ppar & ~(1u << sp)) | (pp << sp);
         mbar_arrive_expect_tx(&p_full[sp], kPStage);
@@ -178,8 +193,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         ++kp;
       }
     }
-    // no copy may still be landing in shared memory when the CTA exits
-    for (int i = 0; i < kSA && i < ka; ++i) mbar_wait(&a_full[i], (apar >> i) & 1u);
     for (int i = 0; i < kSP && i < kp; ++i) mbar_wait(&p_full[i], (ppar >> i) & 1u);
   } else if (warp == kWarpMma && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -213,9 +226,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     // every issued MMA has finished before tensor memory is released
     umma_commit(drain);
     mbar_wait(drain, 0);
-  } else if (warp >= kWarpDeq && warp < kWarpDeq + 4) {
+  } else if (warp >= kWarpDeq && warp < kWarpDeq + kDeqWarps) {
     // ------------------------------------------------------------ dequant
-    const int j = threadIdx.x - kWarpDeq * 32;   // B row 0..127
+    // thread (j, hb): B row j, values 32*hb .. 32*hb+31 of each 64-value stage
+    const int dq = threadIdx.x - kWarpDeq * 32;
+    const int j = dq >> 1, hb = dq & 1;
     int sp = 0, sb = 0, kb = 0;
     uint32_t pp = 0, pb = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
@@ -223,36 +238,50 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
       // the last w2 tile may hang past K rows: those B rows are never stored,
       // so they take any in-bounds scale row
       const bool row_ok = PHASE == 1 || id.nt * kBN + j < p.K;
-      const uint8_t* srow =
-          p.wsc + (size_t)weight_row<PHASE>(id, p, row_ok ? j : 0) * (p.kred / kScaleBlock);
-      for (int kc = 0; kc < nK; ++kc) {
-        if (!warp_wait(&p_full[sp], pp)) { fail = 16; break; }
-        const uint4* src = reinterpret_cast<const uint4*>(sP + sp * kPStage + j * (kBK / 2));
-        const uint4 q0 = src[0], q1 = src[1];
-        const uint32_t sc = *reinterpret_cast<const uint16_t*>(srow + kc * 2);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_empty[sp]);
-        if (++sp == kSP) { sp = 0; pp ^= 1u; }
-        if (kb >= kSB && !warp_wait(&b_empty[sb], pb ^ 1u)) { fail = 32; break; }
-        const ScaleMul s0 = scale_mul(sc & 0xFFu), s1 = scale_mul(sc >> 8);
-        const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        uint8_t* drow = sB + sb * kBStage + (j >> 3) * 1024 + (j & 7) * 128;
+      const uint8_t* srow = p.wsc +
+                            (size_t)weight_row<PHASE>(id, p, row_ok ? j : 0) * (p.kred / kScaleBlock) + hb;
+      // scale bytes of the next kScaleAhead stages, loaded one window early
+      uint32_t sc[kScaleAhead];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {   // chunk c = values 8c .. 8c+7
-          const ScaleMul& sm = c < 4 ? s0 : s1;
-          const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(w[c]), sm);   // (n0, n4)
-          const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(w[c]), sm);   // (n1, n5)
-          const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(w[c]), sm);   // (n2, n6)
-          const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(w[c]), sm);   // (n3, n7)
-          *reinterpret_cast<uint4*>(drow + ((c ^ (j & 7)) << 4)) =
-              make_uint4(prmt(p0, p1, 0x5410u), prmt(p2, p3, 0x5410u), prmt(p0, p1, 0x7632u),
-                         prmt(p2, p3, 0x7632u));
+      for (int i = 0; i < kScaleAhead; ++i) sc[i] = i < nK ? ldg_u8(srow + 2 * i) : 0u;
+      for (int k0 = 0; k0 < nK && !fail; k0 += kScaleAhead) {
+        uint32_t nx[kScaleAhead];
+#pragma unroll
+        for (int i = 0; i < kScaleAhead; ++i)
+          nx[i] = k0 + kScaleAhead + i < nK ? ldg_u8(srow + 2 * (k0 + kScaleAhead + i)) : 0u;
+#pragma unroll
+        for (int i = 0; i < kScaleAhead; ++i) {
+          if (k0 + i >= nK || fail) break;
+          if (!warp_wait(&p_full[sp], pp)) { fail = 16; break; }
+          const uint4 q = *reinterpret_cast<const uint4*>(sP + sp * kPStage + j * (kBK / 2) + hb * 16);
+          // the stage is refilled by the tensor-copy engine (async proxy): the
+          // generic reads above must be ordered before that write
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_empty[sp]);
+          if (++sp == kSP) { sp = 0; pp ^= 1u; }
+          if (kb >= kSB && !warp_wait(&b_empty[sb], pb ^ 1u)) { fail = 32; break; }
+          const ScaleMul sm = scale_mul(sc[i]);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+          uint8_t* drow = sB + sb * kBStage + (j >> 3) * 1024 + (j & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {   // chunk 4*hb + c = values 8(4hb+c) .. +7 of the stage
+            const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(w[c]), sm);   // (n0, n4)
+            const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(w[c]), sm);   // (n1, n5)
+            const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(w[c]), sm);   // (n2, n6)
+            const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(w[c]), sm);   // (n3, n7)
+            *reinterpret_cast<uint4*>(drow + (((4 * hb + c) ^ (j & 7)) << 4)) =
+                make_uint4(prmt(p0, p1, 0x5410u), prmt(p2, p3, 0x5410u), prmt(p0, p1, 0x7632u),
+                           prmt(p2, p3, 0x7632u));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&b_full[sb]);
+          if (++sb == kSB) { sb = 0; pb ^= 1u; }
+          ++kb;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b_full[sb]);
-        if (++sb == kSB) { sb = 0; pb ^= 1u; }
-        ++kb;
+#pragma unroll
+        for (int i = 0; i < kScaleAhead; ++i) sc[i] = nx[i];
       }
     }
   } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
