@@ -10,16 +10,19 @@
 //   GEMM2   per expert: [M_e x I] x [I x K]^T -> x routing weight -> P[route] fp32
 //   combine y[t] = bf16(sum of the token's route outputs, slot order)
 //
-// GEMM kernel: one persistent CTA per SM, tiles (expert, 128 weight rows, up to
+// GEMM kernel: one persistent CTA per SM, tiles (expert, 256 weight rows, up to
 // 2 x 128 tokens) dealt round-robin. Warp roles:
-//   warp 0      TMA producer: activation tiles (128 rows x 64 bf16, 128-byte
-//               swizzle) and packed weight bytes (2 x 64 rows x 32 bytes)
-//   warp 1      MMA issuer: tcgen05.mma M128 N128 K16 (bf16, fp32 in tensor
-//               memory), two accumulator buffers of 2 x 128 columns
+//   warp 0      TMA producer of activation tiles (128 rows x 64 bf16, 128-byte
+//               swizzle)
+//   warp 1      MMA issuer: tcgen05.mma M128 N256 K16 (bf16, fp32 accumulators
+//               in tensor memory: 2 m-tiles x 256 columns)
+//   warp 2      TMA producer of packed weight bytes (256 rows x 32 bytes a stage)
 //   warps 4..7  epilogue: tcgen05.ld of the accumulators (one TMEM lane per
 //               token row) -> SwiGLU / routing weight -> global
-//   warps 8..11 dequant: packed E2M1 + E8M0 -> exact bf16 in the canonical
-//               K-major 128-byte-swizzled layout the MMA reads
+//   warps 8..15 dequant: packed E2M1 + E8M0 -> exact bf16 in the canonical
+//               K-major 128-byte-swizzled layout the MMA reads, one row a thread
+// The two m-tiles' accumulators are released separately, so the next tile's
+// first MMAs start as soon as the epilogue has read the first m-tile.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -31,24 +34,26 @@ namespace mxmoe {
 constexpr int kPfWarps = 16;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kBM = 128;                  // tokens per m-tile
-constexpr int kBN = 128;                  // weight rows per tile
+constexpr int kBN = 256;                  // weight rows per tile (MMA N)
+constexpr int kHalf = kBN / 2;            // GEMM1: gate rows, then as many up rows
 constexpr int kBK = 64;                   // K values per stage (128 bytes of bf16)
 constexpr int kMT = 2;                    // m-tiles per tile
-// ring depths: activations (from L2), packed weights (from DRAM: deepest), bf16 weights
-constexpr int kSA = 3, kSP = 12, kSB = 4;
+constexpr int kSA = 3, kSB = 3, kSP = 3;  // ring depths: activations, bf16 weights, packed
 constexpr int kATile = kBM * kBK * 2;     // 16 KB
 constexpr int kAStage = kMT * kATile;     // 32 KB
-constexpr int kPStage = kBN * kBK / 2;    // 4 KB of packed bytes
-constexpr int kBStage = kBN * kBK * 2;    // 16 KB of bf16
-constexpr int kTmemCols = 512;            // 2 buffers x 2 m-tiles x 128 fp32 columns
+constexpr int kPStage = kBN * kBK / 2;    // 8 KB of packed bytes
+constexpr int kBStage = kBN * kBK * 2;    // 32 KB of bf16
+constexpr int kPBoxRows = 128;            // packed-weight copies are 128 rows x 32 bytes
+constexpr int kTmemCols = kMT * kBN;      // 512: both m-tiles' accumulators
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmaW = 2, kWarpEpi = 4, kWarpDeq = 8;
-constexpr int kDeqWarps = 8;              // two threads per weight row, one 32-value block each
+constexpr int kDeqWarps = 8;              // one weight row per thread
 constexpr int kScaleAhead = 8;            // k-stages of scale bytes held in registers
 constexpr int kTokensPerTile = kMT * kBM;
+static_assert(kDeqWarps * 32 == kBN, "one dequant thread per B row");
 
 struct GemmParams {
   CUtensorMap tmapA;   // activations bf16 [R][kred], box {64, 128}, 128-byte swizzle
-  CUtensorMap tmapB;   // packed weights u8 [rows][kred/2], box {32, 64}
+  CUtensorMap tmapB;   // packed weights u8 [rows][kred/2], box {32, 128}
   const uint8_t* wsc;  // scales u8 [rows][kred/32]
   const int32_t* count;
   const int32_t* offset;
@@ -83,12 +88,21 @@ __device__ __forceinline__ TileId decode_tile(int t, const int* tile_base, const
   return id;
 }
 
-// Weight row of row j (0..127) of the tile's B operand.
+// Output index (GEMM1: intermediate index, GEMM2: output column) of B row j,
+// and whether it exists (the last tile of a dimension may be partial).
+template <int PHASE>
+__device__ __forceinline__ int out_index(const TileId& id, int j) {
+  return PHASE == 1 ? id.nt * kHalf + (j & (kHalf - 1)) : id.nt * kBN + j;
+}
+template <int PHASE>
+__device__ __forceinline__ bool row_valid(const TileId& id, const GemmParams& p, int j) {
+  return out_index<PHASE>(id, j) < (PHASE == 1 ? p.I : p.K);
+}
+// Weight row of B row j: GEMM1 takes 128 gate rows then the matching 128 up rows.
 template <int PHASE>
 __device__ __forceinline__ int weight_row(const TileId& id, const GemmParams& p, int j) {
-  if (PHASE == 1)   // 64 gate rows then the matching 64 up rows
-    return id.e * (2 * p.I) + (j < 64 ? 0 : p.I) + id.nt * 64 + (j & 63);
-  return id.e * p.K + id.nt * kBN + j;
+  if (PHASE == 1) return id.e * (2 * p.I) + (j < kHalf ? 0 : p.I) + out_index<1>(id, j);
+  return id.e * p.K + out_index<2>(id, j);
 }
 
 // Bounded wait taken by a whole warp: every lane gets the same answer, so the
@@ -97,7 +111,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z * sigmoid(z) with the fast exponential and division (a few ulp
+// of fp32; the product is rounded to bf16 afterwards).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+__device__ __forceinline__ uint32_t ldg_u16(const uint8_t* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
 
 template <int PHASE>
 __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -112,9 +134,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   uint64_t* p_empty = p_full + kSP;
   uint64_t* b_full = p_empty + kSP;
   uint64_t* b_empty = b_full + kSB;
-  uint64_t* d_full = b_empty + kSB;
-  uint64_t* d_empty = d_full + 2;
-  uint64_t* drain = d_empty + 2;
+  uint64_t* d_full = b_empty + kSB;    // [kMT]
+  uint64_t* d_empty = d_full + kMT;    // [kMT]
+  uint64_t* drain = d_empty + kMT;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* tile_base = reinterpret_cast<int*>(tmem_slot + 4);   // [E+1]
 
@@ -124,14 +146,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     for (int i = 0; i < kSA; ++i) { mbar_init(&a_full[i], 1); mbar_init(&a_empty[i], 1); }
     for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kDeqWarps); }
     for (int i = 0; i < kSB; ++i) { mbar_init(&b_full[i], kDeqWarps); mbar_init(&b_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
+    for (int i = 0; i < kMT; ++i) { mbar_init(&d_full[i], 1); mbar_init(&d_empty[i], 4); }
     mbar_init(drain, 1);
     fence_barrier_init();
     prefetch_tensormap(&p.tmapA);
     prefetch_tensormap(&p.tmapB);
   }
   if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
-  if (warp == 2) {   // tile table: experts in order, (nt, mp) inside an expert
+  if (warp == 3) {   // tile table: experts in order, (nt, mp) inside an expert
     int carry = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
@@ -177,18 +199,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     for (int i = 0; i < kSA && i < ka; ++i) mbar_wait(&a_full[i], (apar >> i) & 1u);
   } else if (warp == kWarpTmaW && lane == 0) {
     // ------------------------------------------------------------ packed-weight producer
-    // runs up to kSP stages ahead of the dequant warps, across tile boundaries
+    // runs ahead of the dequant warps across tile boundaries
     int sp = 0, kp = 0;
     uint32_t pp = 0, ppar = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
-      const int r0 = weight_row<PHASE>(id, p, 0), r1 = weight_row<PHASE>(id, p, 64);
+      // rows of a partial last tile past the matrix read other experts' rows
+      // (or zeros past the tensor): never stored
+      const int r0 = weight_row<PHASE>(id, p, 0);
+      const int r1 = PHASE == 1 ? r0 + p.I : r0 + kPBoxRows;
       for (int kc = 0; kc < nK; ++kc) {
         if (kp >= kSP && !mbar_wait(&p_empty[sp], pp ^ 1u)) { fail = 2; break; }
         ppar = (ppar & ~(1u << sp)) | (pp << sp);
         mbar_arrive_expect_tx(&p_full[sp], kPStage);
         tma_load_2d(sP + sp * kPStage, &p.tmapB, kc * (kBK / 2), r0, &p_full[sp]);
-        tma_load_2d(sP + sp * kPStage + 64 * (kBK / 2), &p.tmapB, kc * (kBK / 2), r1, &p_full[sp]);
+        tma_load_2d(sP + sp * kPStage + kPBoxRows * (kBK / 2), &p.tmapB, kc * (kBK / 2), r1,
+                    &p_full[sp]);
         if (++sp == kSP) { sp = 0; pp ^= 1u; }
         ++kp;
       }
@@ -197,23 +223,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   } else if (warp == kWarpMma && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = umma_idesc_bf16(kBM, kBN);
-    int sa = 0, sb = 0, it = 0;
+    int sa = 0, sb = 0;
     uint32_t pa = 0, pb = 0;
-    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++it) {
+    int uses[kMT] = {0, 0};   // earlier tiles that accumulated into each m-tile
+    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
-      const int buf = it & 1;
-      if (it >= 2 && !mbar_wait(&d_empty[buf], ((it >> 1) - 1) & 1)) { fail = 4; break; }
-      tc_fence_after();
-      for (int kc = 0; kc < nK; ++kc) {
+      for (int kc = 0; kc < nK && !fail; ++kc) {
         if (!mbar_wait(&a_full[sa], pa) || !mbar_wait(&b_full[sb], pb)) { fail = 8; break; }
         tc_fence_after();
         const uint32_t a_addr = smem_u32(sA + sa * kAStage);
         const uint32_t b_addr = smem_u32(sB + sb * kBStage);
         for (int mt = 0; mt < id.nm; ++mt) {
+          if (kc == 0 && uses[mt] > 0) {   // the epilogue must have read the last tile's m-tile
+            if (!mbar_wait(&d_empty[mt], (uses[mt] - 1) & 1)) { fail = 4; break; }
+            tc_fence_after();
+          }
 #pragma unroll
           for (int k16 = 0; k16 < kBK / 16; ++k16)
-            umma_bf16(tmem + buf * (kMT * kBN) + mt * kBN,
-                      umma_desc_sw128(a_addr + mt * kATile + k16 * 32),
+            umma_bf16(tmem + mt * kBN, umma_desc_sw128(a_addr + mt * kATile + k16 * 32),
                       umma_desc_sw128(b_addr + k16 * 32), idesc, kc > 0 || k16 > 0);
         }
         umma_commit(&a_empty[sa]);
@@ -221,39 +248,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         if (++sa == kSA) { sa = 0; pa ^= 1u; }
         if (++sb == kSB) { sb = 0; pb ^= 1u; }
       }
-      umma_commit(&d_full[buf]);
+      if (fail) break;
+      for (int mt = 0; mt < id.nm; ++mt) {
+        umma_commit(&d_full[mt]);
+        ++uses[mt];
+      }
     }
     // every issued MMA has finished before tensor memory is released
     umma_commit(drain);
     mbar_wait(drain, 0);
   } else if (warp >= kWarpDeq && warp < kWarpDeq + kDeqWarps) {
     // ------------------------------------------------------------ dequant
-    // thread (j, hb): B row j, values 32*hb .. 32*hb+31 of each 64-value stage
-    const int dq = threadIdx.x - kWarpDeq * 32;
-    const int j = dq >> 1, hb = dq & 1;
+    // thread j: B row j, all 64 values of each stage
+    const int j = threadIdx.x - kWarpDeq * 32;
     int sp = 0, sb = 0, kb = 0;
     uint32_t pp = 0, pb = 0;
+    uint8_t* const drow0 = sB + (j >> 3) * 1024 + (j & 7) * 128;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
-      // the last w2 tile may hang past K rows: those B rows are never stored,
-      // so they take any in-bounds scale row
-      const bool row_ok = PHASE == 1 || id.nt * kBN + j < p.K;
-      const uint8_t* srow = p.wsc +
-                            (size_t)weight_row<PHASE>(id, p, row_ok ? j : 0) * (p.kred / kScaleBlock) + hb;
-      // scale bytes of the next kScaleAhead stages, loaded one window early
+      // rows of a partial last tile are never stored: they take any
+      // in-bounds scale row
+      const int row = weight_row<PHASE>(id, p, row_valid<PHASE>(id, p, j) ? j : 0);
+      const uint8_t* srow = p.wsc + (size_t)row * (p.kred / kScaleBlock);
+      // the two scale bytes of each of the next kScaleAhead stages, loaded one window early
       uint32_t sc[kScaleAhead];
 #pragma unroll
-      for (int i = 0; i < kScaleAhead; ++i) sc[i] = i < nK ? ldg_u8(srow + 2 * i) : 0u;
+      for (int i = 0; i < kScaleAhead; ++i) sc[i] = i < nK ? ldg_u16(srow + 2 * i) : 0u;
       for (int k0 = 0; k0 < nK && !fail; k0 += kScaleAhead) {
         uint32_t nx[kScaleAhead];
 #pragma unroll
         for (int i = 0; i < kScaleAhead; ++i)
-          nx[i] = k0 + kScaleAhead + i < nK ? ldg_u8(srow + 2 * (k0 + kScaleAhead + i)) : 0u;
+          nx[i] = k0 + kScaleAhead + i < nK ? ldg_u16(srow + 2 * (k0 + kScaleAhead + i)) : 0u;
 #pragma unroll
         for (int i = 0; i < kScaleAhead; ++i) {
           if (k0 + i >= nK || fail) break;
           if (!warp_wait(&p_full[sp], pp)) { fail = 16; break; }
-          const uint4 q = *reinterpret_cast<const uint4*>(sP + sp * kPStage + j * (kBK / 2) + hb * 16);
+          const uint4* src = reinterpret_cast<const uint4*>(sP + sp * kPStage + j * (kBK / 2));
+          const uint4 q0 = src[0], q1 = src[1];
           // the stage is refilled by the tensor-copy engine (async proxy): the
           // generic reads above must be ordered before that write
           fence_proxy_async_smem();
@@ -261,16 +292,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(&p_empty[sp]);
           if (++sp == kSP) { sp = 0; pp ^= 1u; }
           if (kb >= kSB && !warp_wait(&b_empty[sb], pb ^ 1u)) { fail = 32; break; }
-          const ScaleMul sm = scale_mul(sc[i]);
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-          uint8_t* drow = sB + sb * kBStage + (j >> 3) * 1024 + (j & 7) * 128;
+          const ScaleMul s0 = scale_mul(sc[i] & 0xFFu), s1 = scale_mul(sc[i] >> 8);
+          const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          uint8_t* drow = drow0 + sb * kBStage;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {   // chunk 4*hb + c = values 8(4hb+c) .. +7 of the stage
+          for (int c = 0; c < 8; ++c) {   // chunk c = values 8c .. 8c+7 of the stage
+            const ScaleMul& sm = c < 4 ? s0 : s1;
             const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(w[c]), sm);   // (n0, n4)
             const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(w[c]), sm);   // (n1, n5)
             const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(w[c]), sm);   // (n2, n6)
             const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(w[c]), sm);   // (n3, n7)
-            *reinterpret_cast<uint4*>(drow + (((4 * hb + c) ^ (j & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(drow + ((c ^ (j & 7)) << 4)) =
                 make_uint4(prmt(p0, p1, 0x5410u), prmt(p2, p3, 0x5410u), prmt(p0, p1, 0x7632u),
                            prmt(p2, p3, 0x7632u));
           }
@@ -287,33 +319,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quarter of this warp
-    int it = 0;
-    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++it) {
+    int uses[kMT] = {0, 0};
+    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E, p.NT);
-      const int buf = it & 1;
-      if (!warp_wait(&d_full[buf], (it >> 1) & 1)) { fail = 64; break; }
-      tc_fence_after();
       const int c = p.count[id.e];
       for (int mt = 0; mt < id.nm; ++mt) {
+        if (!warp_wait(&d_full[mt], uses[mt] & 1)) { fail = 64; break; }
+        tc_fence_after();
         const int local = id.mp * kTokensPerTile + mt * kBM + q * 32 + lane;
         const bool valid = local < c;
         const int pos = p.offset[id.e] + local;
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * (kMT * kBN) + mt * kBN;
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + mt * kBN;
         if (PHASE == 1) {
+          const int n32 = min(kHalf, p.I - id.nt * kHalf) >> 5;
 #pragma unroll 1
-          for (int c32 = 0; c32 < 2; ++c32) {
+          for (int c32 = 0; c32 < n32; ++c32) {
             float gv[32], uv[32];
             tmem_ld32(taddr + c32 * 32, gv);
-            tmem_ld32(taddr + 64 + c32 * 32, uv);
+            tmem_ld32(taddr + kHalf + c32 * 32, uv);
             uint32_t hb[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float h0 = silu(gv[2 * i]) * uv[2 * i];
-              const float h1 = silu(gv[2 * i + 1]) * uv[2 * i + 1];
+              const float h0 = silu_fast(gv[2 * i]) * uv[2 * i];
+              const float h1 = silu_fast(gv[2 * i + 1]) * uv[2 * i + 1];
               asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hb[i]) : "f"(h1), "f"(h0));
             }
             if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(p.hp + (size_t)pos * p.I + id.nt * 64 + c32 * 32);
+              uint4* dst = reinterpret_cast<uint4*>(p.hp + (size_t)pos * p.I + id.nt * kHalf + c32 * 32);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(hb[4 * i], hb[4 * i + 1], hb[4 * i + 2], hb[4 * i + 3]);
@@ -336,10 +368,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&d_empty[mt]);
+        ++uses[mt];
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_empty[buf]);
     }
   }
   __syncwarp();
@@ -374,7 +407,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 
 static size_t gemm_smem_bytes(int E) {
   return 1024 + (size_t)kSA * kAStage + (size_t)kSB * kBStage + (size_t)kSP * kPStage +
-         (size_t)(2 * kSA + 2 * kSP + 2 * kSB + 5) * 8 + 16 + (size_t)(E + 1) * 4;
+         (size_t)(2 * kSA + 2 * kSP + 2 * kSB + 2 * kMT + 1) * 8 + 16 + (size_t)(E + 1) * 4;
 }
 
 size_t prefill_counter_bytes(int, int, int, int, int) { return 256; }
@@ -412,7 +445,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   if (!encode_tiled_2d(&g1.tmapA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.xp, (uint64_t)a.K, (uint64_t)R,
                        (uint64_t)a.K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tiled_2d(&g1.tmapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w13, (uint64_t)a.K / 2,
-                       (uint64_t)a.E * 2 * a.I, (uint64_t)a.K / 2, 32, 64,
+                       (uint64_t)a.E * 2 * a.I, (uint64_t)a.K / 2, 32, kPBoxRows,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   g1.wsc = a.s13;
@@ -426,7 +459,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   g1.K = a.K;
   g1.I = a.I;
   g1.kred = a.K;
-  g1.NT = a.I / 64;
+  g1.NT = (a.I + kHalf - 1) / kHalf;   // I % 64 == 0: the last tile may hold 64 rows
   g1.status = a.status;
   if ((e = launch_gemm<1>(g1, a.num_sms, stream)) != cudaSuccess) return e;
   rec(2);
@@ -435,11 +468,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   if (!encode_tiled_2d(&g2.tmapA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.hp, (uint64_t)a.I, (uint64_t)R,
                        (uint64_t)a.I * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tiled_2d(&g2.tmapB, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w2, (uint64_t)a.I / 2,
-                       (uint64_t)a.E * a.K, (uint64_t)a.I / 2, 32, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+                       (uint64_t)a.E * a.K, (uint64_t)a.I / 2, 32, kPBoxRows,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   g2.wsc = a.s2;
   g2.kred = a.I;
-  g2.NT = (a.K + kBN - 1) / kBN;   // K % 64 == 0: the last tile may hold 64 rows
+  g2.NT = (a.K + kBN - 1) / kBN;   // K % 64 == 0: the last tile may be partial
   if ((e = launch_gemm<2>(g2, a.num_sms, stream)) != cudaSuccess) return e;
   rec(3);
   if ((e = launch_combine(a.P, a.ids, a.T, a.K, a.E, a.topk, a.y, a.num_sms, stream, false)) !=
