@@ -34,24 +34,27 @@
 
 namespace mxmoe {
 
-constexpr int kPfWarps = 16;
+constexpr int kPfWarps = 20;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 64;                   // K values per stage (128 bytes of bf16)
-constexpr int kMaxTok = 384;              // tokens per tile (accumulator columns)
-constexpr int kXBox = 128;                // token rows per TMA copy
-constexpr int kSX = 3, kSP = 8, kSW = 4;  // rings: tokens (smem), packed (smem), bf16 weights (TMEM)
-constexpr int kXStage = kMaxTok * kBK * 2;   // 48 KB
-constexpr int kXBoxBytes = kXBox * kBK * 2;  // 16 KB
+constexpr int kMaxTok = 320;              // tokens per tile (accumulator columns)
+constexpr int kXBox = 64;                 // token rows per TMA copy (<= 5 a stage)
+constexpr int kSX = 4, kSP = 12, kSW = 4; // rings: tokens (smem), packed (smem), bf16 weights (TMEM)
+constexpr int kXStage = kMaxTok * kBK * 2;   // 40 KB
+constexpr int kXBoxBytes = kXBox * kBK * 2;  // 8 KB
 constexpr int kPStage = kBM * kBK / 2;       // 4 KB of packed bytes
 constexpr int kPBoxRows = 64;
 constexpr int kTmemCols = 512;
-constexpr int kWCol0 = kMaxTok;           // operand-A ring: columns 384..511
+constexpr int kWCol0 = kMaxTok;           // operand-A ring: columns 320..447
 constexpr int kWCols = kBK / 2;           // 32 columns (bf16 pairs) a stage
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmaW = 2, kWarpEpi = 4, kWarpDeq = 8;
+constexpr int kWarpEpi2 = 16;            // second epilogue group: the upper half of the tokens
+constexpr int kEpiWarps = 8;
 constexpr int kDeqWarps = 8;
 constexpr int kScaleAhead = 8;            // k-stages of scale bytes held in registers
 static_assert(kWCol0 + kSW * kWCols <= kTmemCols, "tensor memory budget");
+static_assert(kMaxTok % kXBox == 0 && kMaxTok % 16 == 0, "token boxes fill a stage exactly");
 
 struct GemmParams {
   CUtensorMap tmapX;   // tokens bf16 [R][kred], box {64, 128}, 128-byte swizzle
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kDeqWarps); }
     for (int i = 0; i < kSW; ++i) { mbar_init(&w_full[i], kDeqWarps); mbar_init(&w_empty[i], 1); }
     mbar_init(d_full, 1);
-    mbar_init(d_empty, 4);
+    mbar_init(d_empty, kEpiWarps);
     mbar_init(drain, 1);
     fence_barrier_init();
     prefetch_tensormap(&p.tmapX);
@@ -326,9 +329,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         for (int i = 0; i < kScaleAhead; ++i) sc[i] = nx[i];
       }
     }
-  } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
+  } else if ((warp >= kWarpEpi && warp < kWarpEpi + 4) || warp >= kWarpEpi2) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;   // TMEM lane quarter of this warp
+    const int half = warp >= kWarpEpi2;   // which half of the tile's tokens (32-column blocks)
     int tiles = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++tiles) {
       const TileId id = decode_tile(t, tile_base, p.count, E);
@@ -343,8 +347,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           const int g = 2 * q + s;
           const int i = id.nt * 64 + 8 * g + (lane >> 2);
           const uint32_t taddr = tmem + ((uint32_t)(16 * g) << 16);
+          const int n32 = (id.n + 31) >> 5, lo32 = (n32 + 1) >> 1;
 #pragma unroll 1
-          for (int b = 0; b * 8 < id.n; b += 4) {
+          for (int b = (half ? lo32 : 0) * 4; b < (half ? n32 : lo32) * 4; b += 4) {
             uint32_t v[4][4];
             tmem_ld_16x256b_x4(taddr + b * 8, v);
 #pragma unroll
@@ -362,8 +367,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         const int k = id.nt * kBM + q * 32 + lane;
         const bool kvalid = k < p.K;
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        const int n32 = (id.n + 31) >> 5, lo32 = (n32 + 1) >> 1;
 #pragma unroll 1
-        for (int c0 = 0; c0 < id.n; c0 += 32) {
+        for (int c0 = (half ? lo32 : 0) * 32; c0 < (half ? n32 : lo32) * 32; c0 += 32) {
           float v[32];
           tmem_ld32(taddr + c0, v);
           // lane j fetches token c0 + j's route and routing weight
