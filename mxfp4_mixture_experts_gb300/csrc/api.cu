@@ -93,7 +93,7 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
   size_t item_ctr1, item_ctr2, tile_ctr, pf_ctr;          // zero-kept
-  size_t parts1, parts2, h, P, rcount, roffset, rlist, xp;   // scratch
+  size_t parts1, parts2, h, P, rcount, roffset, rlist, rinv, xp;   // scratch
   size_t total;
 };
 
@@ -122,6 +122,7 @@ Layout layout(int T, int K, int I, int E, int topk) {
   L.rcount = take((size_t)E * sizeof(int));
   L.roffset = take((size_t)(E + 1) * sizeof(int));
   L.rlist = take(R * sizeof(int));
+  L.rinv = take(R * sizeof(int));
   L.xp = take(R * K * 2);
   L.total = o;
   return L;
@@ -260,6 +261,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
   p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
   p.P = reinterpret_cast<float*>(ws + L.P);
+  p.inv = reinterpret_cast<int32_t*>(ws + L.rinv);
   p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
   p.num_sms = d->num_sms;
   return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));

@@ -7,8 +7,9 @@
 //   route   stable counting sort of the routes by expert (route.cu)
 //   gather  xp[pos] = hidden[token of route list[pos]]: rows in expert order
 //   GEMM1   per expert: [M_e x K] x [K x 2I]^T -> SwiGLU -> hp [M_e x I] bf16
-//   GEMM2   per expert: [M_e x I] x [I x K]^T -> x routing weight -> P[route] fp32
-//   combine y[t] = bf16(sum of the token's route outputs, slot order)
+//   GEMM2   per expert: [M_e x I] x [I x K]^T -> P[pos] fp32 (expert order)
+//   combine y[t] = bf16(sum over the token's slots of w * P[pos of the route]),
+//           slot order
 //
 // GEMM kernel: weight-stationary, one persistent CTA per SM. A tile is
 // (expert, 128 weight rows, a chunk of up to 384 of the expert's tokens); the
@@ -65,7 +66,7 @@ struct GemmParams {
   const int32_t* list;
   const float* wts;
   uint16_t* hp;        // GEMM1 output bf16 [R][I]
-  float* P;            // GEMM2 output fp32 [R][K] (route order)
+  float* P;            // GEMM2 output fp32 [R][K] (expert order, unweighted)
   int E, K, I, kred, NT;
   int32_t* status;
 };
@@ -372,15 +373,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         for (int c0 = (half ? lo32 : 0) * 32; c0 < (half ? n32 : lo32) * 32; c0 += 32) {
           float v[32];
           tmem_ld32(taddr + c0, v);
-          // lane j fetches token c0 + j's route and routing weight
-          const int nj = c0 + lane;
-          const int rj = nj < id.n ? p.list[pos0 + nj] : 0;
-          const float wj = nj < id.n ? p.wts[rj] : 0.f;
+          // one 128-byte row segment per token: 32 consecutive output columns
+          float* dst = p.P + (size_t)(pos0 + c0) * p.K + k;
+          const int nv = min(32, id.n - c0);
+          if (kvalid) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = __shfl_sync(0xffffffffu, rj, j);
-            const float w = __shfl_sync(0xffffffffu, wj, j);
-            if (c0 + j < id.n && kvalid) p.P[(size_t)r * p.K + k] = w * v[j];
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) dst[(size_t)j * p.K] = v[j];
           }
         }
       }
@@ -403,11 +402,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
 }
 
 // xp[pos] = hidden[list[pos] / topk] for the valid (expert-sorted) routes.
+// Also inv[route] = pos, the row of the route's output in P.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ hidden,
                                                      const int32_t* __restrict__ list,
                                                      const int32_t* __restrict__ n_valid, int K,
-                                                     int topk, uint16_t* __restrict__ xp) {
+                                                     int topk, uint16_t* __restrict__ xp,
+                                                     int32_t* __restrict__ inv) {
   const int n = *n_valid;
+  for (int pos = blockIdx.x * blockDim.x + threadIdx.x; pos < n; pos += gridDim.x * blockDim.x)
+    inv[list[pos]] = pos;
   const int per_row = K / 8;
   const int64_t total = (int64_t)n * per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -416,6 +419,45 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     const int tok = list[pos] / topk;
     reinterpret_cast<uint4*>(xp + (size_t)pos * K)[c] =
         reinterpret_cast<const uint4*>(hidden + (size_t)tok * K)[c];
+  }
+}
+
+// y[t][m] = bf16( sum over slots j = 0..k-1 with a valid expert of
+// w[t][j] * P[inv[t*k + j]][m] ), in slot order (deterministic). 8 outputs a thread.
+__global__ void __launch_bounds__(256) combine_pos_kernel(const float* __restrict__ P,
+                                                          const int32_t* __restrict__ ids,
+                                                          const float* __restrict__ wts,
+                                                          const int32_t* __restrict__ inv, int T,
+                                                          int K, int E, int topk,
+                                                          uint16_t* __restrict__ y) {
+  const int per_row = K / 8;
+  const int64_t n = (int64_t)T * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per_row), m8 = (int)(i - (int64_t)t * per_row) * 8;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < topk; ++j) {
+      const int r = t * topk + j;
+      const int e = ids[r];
+      if (e < 0 || e >= E) continue;
+      const float w = wts[r];
+      const float* row = P + (size_t)inv[r] * K + m8;
+      const uint4 lo = ldcg16(row);
+      const uint4 hi = ldcg16(row + 4);
+      s[0] += w * __uint_as_float(lo.x);
+      s[1] += w * __uint_as_float(lo.y);
+      s[2] += w * __uint_as_float(lo.z);
+      s[3] += w * __uint_as_float(lo.w);
+      s[4] += w * __uint_as_float(hi.x);
+      s[5] += w * __uint_as_float(hi.y);
+      s[6] += w * __uint_as_float(hi.z);
+      s[7] += w * __uint_as_float(hi.w);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(s[2 * q + 1]), "f"(s[2 * q]));
+    *reinterpret_cast<uint4*>(y + (size_t)t * K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -451,7 +493,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   cudaError_t e = launch_route(a.ids, R, a.E, a.count, a.offset, a.list, a.status, stream);
   if (e != cudaSuccess) return e;
   int gblocks = a.num_sms * 8;
-  gather_kernel<<<gblocks, 256, 0, stream>>>(a.hidden, a.list, a.offset + a.E, a.K, a.topk, a.xp);
+  gather_kernel<<<gblocks, 256, 0, stream>>>(a.hidden, a.list, a.offset + a.E, a.K, a.topk, a.xp,
+                                             a.inv);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   rec(1);
 
@@ -490,9 +533,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   g2.NT = (a.K + kBM - 1) / kBM;   // K % 64 == 0: the last tile may hold 64 rows
   if ((e = launch_gemm<2>(g2, a.num_sms, stream)) != cudaSuccess) return e;
   rec(3);
-  if ((e = launch_combine(a.P, a.ids, a.T, a.K, a.E, a.topk, a.y, a.num_sms, stream, false)) !=
-      cudaSuccess)
-    return e;
+  {
+    const int64_t n = (int64_t)a.T * (a.K / 8);
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > (int64_t)a.num_sms * 8) blocks = (int64_t)a.num_sms * 8;
+    combine_pos_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a.P, a.ids, a.wts, a.inv, a.T, a.K,
+                                                             a.E, a.topk, a.y);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   rec(4);
   return cudaSuccess;
 }

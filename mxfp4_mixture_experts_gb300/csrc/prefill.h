@@ -22,7 +22,8 @@ struct PrefillArgs {
   int32_t* list;            // [R]
   uint16_t* xp;             // bf16 [R, K], rows in expert order
   uint16_t* hp;             // bf16 [R, I], rows in expert order
-  float* P;                 // fp32 [R, K], rows in route order
+  float* P;                 // fp32 [R, K], rows in expert order, unweighted
+  int32_t* inv;             // [R] route -> row of P
   int* counters;            // zero-kept scheduler counters
   int num_sms;
 };
