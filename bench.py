@@ -15,9 +15,10 @@ line carries the same measurement, shorter, under ``prefill``.
 
 Printed: one JSON line (rank 0). ``value`` is microseconds per MoE call
 (whole job: all calls of all ranks / time), taken from CUDA-graph replays of
-the step with events on the replay stream. ``roofline`` is the dominant kernel
-(decode phase 1, gate/up projection) timed with CUDA events around each of its
-launches over a second timed pass. ``e2e`` repeats the metric through the C-ABI
+the step with events on the replay stream. ``roofline`` is the decode kernel
+(one cooperative launch per call: w13 + SwiGLU, w2, combine) timed with CUDA
+events around each launch over a second timed pass, against the touched
+experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
 with host buffers (pinned host -> device copies of each call's activations and
 routing, device -> host copy of its output, inside the timed region).
 ``--impl reference`` times the CPU oracle on the same workload instead.
@@ -449,16 +450,17 @@ def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
 
 
 def time_phases(wl, steps: int, warmup: int):
-    """Per-kernel durations: events recorded by the library around each kernel."""
+    """Per-call kernel durations: events recorded by the library around the
+    decode kernel (one cooperative launch per call)."""
     from mxfp4_mixture_experts_gb300 import moe
     stream = torch.cuda.Stream()
     per_T = {T: [] for T in wl.tokens}
-    w13 = []          # (alg bytes, ms) per phase-1 launch
+    launches = []          # (algorithmic bytes, ms) per launch
     with torch.cuda.stream(stream):
         for s in range(warmup + steps):
             recs = []
             for ly in wl.step_layers(s):
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
                 moe.set_phase_events(ev)
                 wl.call(ly)
                 recs.append((ly, ev))
@@ -467,13 +469,10 @@ def time_phases(wl, steps: int, warmup: int):
             if s < warmup:
                 continue
             for ly, ev in recs:
-                t13 = ev[0].elapsed_time(ev[1])
-                t2 = ev[1].elapsed_time(ev[2])
-                tc = ev[2].elapsed_time(ev[3])
-                per_T[ly["T"]].append((t13 + t2 + tc, ly, (t13, t2, tc)))
-                sh = wl.shape
-                w13.append((ly["D"] * w13_bytes(sh.K, sh.I), t13))
-    return per_T, w13
+                ms = ev[0].elapsed_time(ev[1])
+                per_T[ly["T"]].append((ms, ly))
+                launches.append((wl.alg_bytes(ly), ms))
+    return per_T, launches
 
 
 def time_e2e(wl, steps: int, warmup: int):
@@ -544,7 +543,7 @@ def run_ours(args, dist: Dist):
     elapsed_ms = dist.max(elapsed_ms)
     calls = args.steps * wl.calls_per_step
     value = aggregate_us_per_call(elapsed_ms, calls, dist.world)
-    per_T_raw, w13 = time_phases(wl, args.steps, min(args.warmup, 3))
+    per_T_raw, launches = time_phases(wl, args.steps, min(args.warmup, 3))
     e2e_ms, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
     e2e_ms = dist.max(e2e_ms)
     per_T = {}
@@ -552,13 +551,12 @@ def run_ours(args, dist: Dist):
     for T, recs in per_T_raw.items():
         ms = statistics.median([r[0] for r in recs])
         b = statistics.mean([wl.alg_bytes(r[1]) for r in recs])
-        phases = [round(statistics.median([r[2][i] for r in recs]) * 1000, 2) for i in range(3)]
-        per_T[str(T)] = {"us": round(ms * 1000, 2), "phase_us": phases, "alg_bytes": int(b),
+        per_T[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
                          "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
-    tot_b = sum(b for b, _ in w13)
-    tot_ms = sum(t for _, t in w13)
+    tot_b = sum(b for b, _ in launches)
+    tot_ms = sum(t for _, t in launches)
     achieved = tot_b / (tot_ms * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "us_per_call",
@@ -567,16 +565,17 @@ def run_ours(args, dist: Dist):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": wl.config(),
         "per_T": per_T,
-        "roofline": {"kernel": "decode_kernel<1> (w13 gate/up + SwiGLU)", "bound": "hbm",
+        "roofline": {"kernel": "decode_kernel (w13 + SwiGLU, w2, combine: one launch per call)",
+                     "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
                      "traffic": None,
-                     "alg_bytes_per_launch": int(tot_b / max(len(w13), 1)),
-                     "avg_launch_us": round(tot_ms / max(len(w13), 1) * 1000, 2)},
+                     "alg_bytes_per_launch": int(tot_b / max(len(launches), 1)),
+                     "avg_launch_us": round(tot_ms / max(len(launches), 1) * 1000, 2)},
         "e2e": {"value": round(aggregate_us_per_call(e2e_ms, calls, dist.world), 3),
                 "unit": "us_per_call", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * calls,
+        "gpu_launches": calls,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
     }

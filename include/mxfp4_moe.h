@@ -33,9 +33,10 @@
  *       status[1] = number of distinct experts touched by the call
  *       status[2] = non-zero when a bounded wait inside a kernel gave up (the
  *                   output of that call is then not valid; never expected);
- *                   the bits name the wait: bits 0..7 the decode path's first
- *                   kernel, 8..15 its second, 16..23 the prefill path's first
- *                   GEMM, 24..31 its second
+ *                   the bits name the wait: bits 0..7 the decode kernel's
+ *                   producer, 8..15 its consumers, 16..23 the prefill path's
+ *                   first GEMM, 24..31 its second. After such a call the
+ *                   workspace must be zeroed again before it is reused
  *       status[3] = 1 + the first CTA that reported such a wait, else 0
  *    Negative expert ids are padding and are skipped silently.
  *  - Every call is deterministic: repeating it on the same inputs gives
@@ -64,7 +65,10 @@ typedef enum {
 /* Shape limits (checked on the host, MXFP4_MOE_ERR_SHAPE otherwise):
  *   K % 32 == 0, I % 32 == 0, 32 <= K, I <= 16384
  *   1 <= E <= 1024, 1 <= topk <= 32, topk <= E, 0 <= T
- *   decode path: T <= 32 and T * topk <= 1024 (the shared-memory tables must fit)
+ *   decode path: T <= 32, T * topk <= 1024, K % 64 == 0, I % 64 == 0 (scale
+ *                rows are copied 8 rows at a time) and the kernel's shared-memory
+ *                plan must fit: about 12 * max(K, I) + 20 * E + 2 * max(K, I)
+ *                + 66 KB <= 227 KB (K, I <= 8192 always fit for E <= 256)
  *   prefill path: K % 64 == 0, I % 64 == 0 (tensor-core tiles), T * topk < 2^31 / K
  * Alignment (MXFP4_MOE_ERR_ALIGN otherwise): w13, s13, w2, s2, hidden and out
  * 16-byte aligned; workspace 256-byte aligned. */
@@ -149,10 +153,12 @@ int mxfp4_moe_forward_noalloc(const void* hidden, const int32_t* topk_ids,
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
                       void* out, void* stream);
 
-/* Profiling hook: when events (host array of n cudaEvent_t handles, n >= 3)
+/* Profiling hook: when events (host array of n cudaEvent_t handles, n >= 2)
  * is non-NULL, each later forward call on this process records events[0]
  * before its first kernel and events[i] after its i-th kernel (while i < n),
- * on its stream; the decode path runs 3 kernels. Pass NULL to turn it off.
+ * on its stream; the decode path runs 1 kernel (one cooperative launch), the
+ * prefill path 5 (the first two events bracket route + gather). Pass NULL to
+ * turn it off.
  * Not thread-safe; meant for benchmarks. */
 void mxfp4_moe_set_phase_events(void* const* events, int n);
 

@@ -48,20 +48,6 @@ bool get_encoder() {
   return true;
 }
 
-// Packed weights viewed as a 2-D byte tensor [rows][row_bytes]; tiles of 16
-// rows x 128 bytes land in shared memory with the 128-byte swizzle; reads past
-// the end of a row return zeros.
-bool weight_tensor_map(CUtensorMap* m, const uint8_t* base, uint64_t row_bytes, uint64_t rows) {
-  const cuuint64_t dims[2] = {row_bytes, rows};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {128, 16};
-  const cuuint32_t es[2] = {1, 1};
-  return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Checks the current device once (sm_103) and caches its SM count.
 int current_device(DeviceInfo** out) {
   int dev = 0;
@@ -92,8 +78,8 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // Workspace layout. The bookkeeping that must be zero between calls comes
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
-  size_t item_ctr1, item_ctr2, tile_ctr, pf_ctr;          // zero-kept
-  size_t parts1, parts2, h, P, rcount, roffset, rlist, rinv, xp;   // scratch
+  size_t gbar, pf_ctr;                                     // zero-kept
+  size_t h, P, rcount, roffset, rlist, rinv, xp;           // scratch
   size_t total;
 };
 
@@ -108,15 +94,10 @@ bool shape_ok(int T, int K, int I, int E, int topk) {
 Layout layout(int T, int K, int I, int E, int topk) {
   Layout L;
   const size_t R = (size_t)T * topk;
-  const size_t ctas = (size_t)kMaxCtas;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
-  L.item_ctr1 = take(ctas * sizeof(int));
-  L.item_ctr2 = take(ctas * sizeof(int));
-  L.tile_ctr = take((size_t)(K / 16) * sizeof(int));
+  L.gbar = take(2 * sizeof(int));
   L.pf_ctr = take(prefill_counter_bytes(T, K, I, E, topk));
-  L.parts1 = take(ctas * 2 * 256 * sizeof(float));
-  L.parts2 = take(ctas * 2 * 256 * sizeof(float));
   L.h = take(R * I * 2);
   L.P = take(R * K * sizeof(float));
   L.rcount = take((size_t)E * sizeof(int));
@@ -189,18 +170,24 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   const Layout L = layout(T, K, I, E, topk);
   if (workspace_bytes < L.total) return MXFP4_MOE_ERR_WORKSPACE;
   const bool decode = path == 1 || (path == 0 && T <= kDecodeMaxT);
-  if (decode && (T > kDecodeMaxT || T * topk > kDecodeMaxRoutes)) return MXFP4_MOE_ERR_SHAPE;
+  if (decode && (T > kDecodeMaxT || T * topk > kDecodeMaxRoutes || K % 64 || I % 64))
+    return MXFP4_MOE_ERR_SHAPE;
   if (!decode && (K % 64 || I % 64)) return MXFP4_MOE_ERR_SHAPE;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
+  if (decode && !decode_fits(K, I, E, T * topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  const int ctas = d->num_sms < kMaxCtas ? d->num_sms : kMaxCtas;
 
   if (decode) {
     DecodeArgs a = {};
+    a.x = static_cast<const uint16_t*>(hidden);
     a.ids = topk_ids;
     a.wts = topk_weights;
+    a.w13 = w13;
+    a.s13 = s13;
+    a.w2 = w2;
+    a.s2 = s2;
     a.T = T;
     a.K = K;
     a.I = I;
@@ -209,34 +196,20 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a.h = reinterpret_cast<uint16_t*>(ws + L.h);
     a.P = reinterpret_cast<float*>(ws + L.P);
     a.y = static_cast<uint16_t*>(out);
+    a.gbar = reinterpret_cast<int*>(ws + L.gbar);
     a.status = status;
-    if (!get_encoder()) return MXFP4_MOE_ERR_CUDA;
+    // packed weights as 2-D byte tensors [rows][row bytes], 128-byte swizzled
+    // tiles of 128 bytes x 8 rows (w13: gate and up runs) / x 16 rows (w2)
     CUtensorMap map1, map2;
-    if (!weight_tensor_map(&map1, w13, (uint64_t)K / 2, (uint64_t)E * 2 * I) ||
-        !weight_tensor_map(&map2, w2, (uint64_t)I / 2, (uint64_t)E * K))
+    if (!encode_tiled_2d(&map1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, (uint64_t)K / 2,
+                         (uint64_t)E * 2 * I, (uint64_t)K / 2, 128, 8, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_2d(&map2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, (uint64_t)I / 2, (uint64_t)E * K,
+                         (uint64_t)I / 2, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
       return MXFP4_MOE_ERR_CUDA;
     record_phase(0, s);
-    DecodeArgs a1 = a;
-    a1.x = static_cast<const uint16_t*>(hidden);
-    a1.wq = w13;
-    a1.wsc = s13;
-    a1.parts = reinterpret_cast<float*>(ws + L.parts1);
-    a1.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr1);
-    cudaError_t e = launch_decode(a1, 1, ctas, d->max_smem, map1, s, g_phase_events == nullptr);
+    const cudaError_t e = launch_decode(a, map1, map2, d->num_sms, d->max_smem, s);
     if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     record_phase(1, s);
-    DecodeArgs a2 = a;
-    a2.x = a.h;
-    a2.wq = w2;
-    a2.wsc = s2;
-    a2.parts = reinterpret_cast<float*>(ws + L.parts2);
-    a2.item_ctr = reinterpret_cast<int*>(ws + L.item_ctr2);
-    e = launch_decode(a2, 2, ctas, d->max_smem, map2, s, g_phase_events == nullptr);
-    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
-    record_phase(2, s);
-    e = launch_combine(a.P, topk_ids, T, K, E, topk, a.y, d->num_sms, s, g_phase_events == nullptr);
-    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
-    record_phase(3, s);
     return MXFP4_MOE_OK;
   }
 

@@ -1,38 +1,41 @@
-// Decode kernels (1..32 tokens): the routed experts run straight from the
-// packed MXFP4 bytes ("MXFP4 MoE decode kernels", Design).
+// Decode (1..32 tokens): the routed experts run straight from the packed
+// MXFP4 bytes ("MXFP4 MoE decode kernels", Design), in ONE cooperative
+// launch per layer call:
 //
-// Three launches per layer call (each may start while the previous one
-// drains: programmatic dependent launch):
-//   phase 1 (w13): per touched expert, gate and up rows are streamed once,
-//                  decoded in registers, multiplied with the expert's tokens
-//                  on the tensor cores and finished with SwiGLU -> bf16 h [R, I];
-//   phase 2 (w2):  per touched expert, the w2 rows are streamed the same way
-//                  against h and scaled by the routing weight into fp32 route
-//                  outputs P [R, K];
-//   combine:       y [T, K] = bf16 of the sum of each token's k route outputs,
-//                  in slot order.
+//   phase 1 (w13): per touched expert, every gate/up row is streamed once,
+//                  decoded on the fly, multiplied with all of the expert's
+//                  tokens on the tensor cores and finished with SwiGLU into
+//                  bf16 h [R, I];
+//   grid barrier   (h complete; each warp's first w2 stages were issued
+//                  before it);
+//   phase 2 (w2):  the same over the w2 rows against h, scaled by the routing
+//                  weight into fp32 route outputs P [R, K];
+//   grid barrier;
+//   combine:       y [T, K] = bf16 of the slot-order sum of each token's route
+//                  outputs.
 //
-// CTA = 1 producer warp + 12 consumer warps, one CTA per SM.
-//  * The producer streams weight tiles with 2-D TMA (cp.async.bulk.tensor,
-//    128-byte swizzle) into a ring of shared-memory stages, and each item's
-//    E8M0 scale rows with 1-D bulk copies; mbarriers track both.
+// CTA = 1 control warp + 8 consumer warps, one CTA per SM.
+//  * Work item = 16 weight rows of one touched expert over the whole
+//    reduction (phase 1: gate rows i0..i0+7 and the matching up rows; phase 2:
+//    16 w2 rows). A phase's items are split into equal contiguous ranges, one
+//    per CTA, and a CTA's items are dealt round-robin to its consumer warps:
+//    a warp owns whole items, so no partial sums cross warps or CTAs, and the
+//    SwiGLU of a gate/up pair happens in the thread that holds both.
+//  * Each consumer warp streams its own items: lane 0 keeps 3 stages of 16
+//    rows x 256 bytes in flight in the warp's 4-stage ring (2-D TMA, 128-byte
+//    swizzle), running on into its phase-2 items before h exists, and
+//    bulk-copies each item's E8M0 rows into one of the warp's two scale slots.
+//    Spreading the issue over 8 warps keeps enough bytes in flight per SM.
 //  * Consumers decode E2M1 with the hardware e2m1x2 -> f16x2 conversion
-//    (exact), run one m16n8k16 f16 MMA pair per 32-value scale block into a
-//    fresh fp32 fragment and fold it into the accumulator with one FFMA by
+//    (exact), run one m16n8k16 f16 MMA pair per 32-value block into a fresh
+//    fp32 fragment and fold it into the accumulator with one FFMA by
 //    2^(s-127) (exact for every scale byte, 0 and 255 included).
-//  * Activations (hidden rows for phase 1, h rows for phase 2) are staged once
-//    per CTA in shared memory as f16 after an exact power-of-two prescale per
-//    row (max |x| lands in [2^14, 2^15)); the epilogue multiplies it back.
-//
-// Work decomposition. An *item* is (touched expert d, row tile nt, token
-// group gr): 32 weight rows against up to 8 of the expert's tokens (phase 1:
-// gate rows 16nt..16nt+15 and the matching up rows; phase 2: w2 rows
-// 32nt..32nt+31). Its K range is cut into *chunks* of 48 scale blocks (one
-// pipeline stage each). The (item, chunk) units are dealt to CTAs in equal
-// contiguous ranges, so every SM streams the same number of bytes whatever
-// the routing; an item cut between CTAs is finished by whichever CTA arrives
-// last (an integer counter per item), adding the fp32 partials in fixed CTA
-// order, so the result is deterministic.
+//  * Activations (hidden rows for phase 1, h rows for phase 2) are staged in
+//    shared memory by the control warp and converted to f16 after an exact
+//    power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
+//    epilogue multiplies it back. Rows that do not fit are read from global
+//    memory and converted on the fly. The control warp waits for the grid
+//    between the phases.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -41,52 +44,53 @@
 
 namespace mxmoe {
 
-constexpr int kConsumerWarps = 12;   // 13 warps: at most 4 per SM sub-partition, 128 registers each
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kGroup = 8;            // tokens per mma n-tile
-constexpr int kItemRows = 32;        // weight rows per item (two m16 tiles)
-constexpr int kChunkBlocks = 48;     // scale blocks per stage (6 TMA columns of 128 B)
-constexpr int kWarpBlocks = kChunkBlocks / kConsumerWarps;   // blocks per consumer warp per stage
-constexpr int kStageBytes = kItemRows * kChunkBlocks * 16;   // 24 KB
-constexpr int kBoxBytes = 16 * 128;  // one TMA box: 16 rows x 128 bytes
-constexpr int kScaleSlots = 3;
-constexpr int kBarConsumers = 1;     // named barrier id of the consumer warps
-constexpr int kRowBars = 16;         // barriers of the staged activation rows
-constexpr uint32_t kRowBarBytes = 32768;   // bytes tracked by one of them (at most)
+constexpr int kCW = 8;                       // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;     // 288
+constexpr int kD = 4;                        // stages in each consumer warp's ring
+constexpr int kConsumerThreads = kCW * 32;
+constexpr int kRows = 16;                    // weight rows per item (one m16 tile)
+constexpr int kChunk = 256;                  // packed bytes per row per stage
+constexpr int kChunkBlocks = kChunk / 16;    // 16 scale blocks per stage
+constexpr int kStageBytes = kRows * kChunk;  // 4 KB
+constexpr int kColBytes = kRows * 128;       // one 128-byte column of a stage
+constexpr int kScaleSlots = 2 * kCW;         // two per consumer warp
+constexpr int kRingBytes = kCW * kD * kStageBytes;
+constexpr int kGroup = 8;                    // tokens per mma n-tile
+constexpr int kBatch = 32;                   // routes of one expert an item multiplies at most
+constexpr int kMaxGroups = kBatch / kGroup;
+constexpr int kBarConsumers = 1;             // named barrier of the consumer warps
+constexpr int kRowBars = 16;                 // barriers of the staged activation rows
+constexpr uint32_t kRowBarBytes = 32768;     // bytes tracked by one of them (at most)
+
 
 __host__ __device__ inline size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
 
 // Shared-memory plan (byte offsets from a 1024-byte aligned base).
 struct DecodeSmem {
-  size_t stage, scale, scale_slot, bars, red, fin, flags, ints, row_sh, xs, total;
+  size_t ring, scales, bars, flags, ints, eb, row_sh, xs, total;
+  int slot_bytes;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, int I, int E,
-                                                       int topk, int stages, int rows_cap,
-                                                       int xs_rows, int xs_stride) {
+__host__ __device__ inline DecodeSmem decode_smem_plan(int K, int I, int E, int R, int xs_rows,
+                                                       int xs_stride) {
   DecodeSmem m;
-  const int kred = phase == 1 ? K : I;
-  const int nblk = kred / kScaleBlock;
-  const int R = T * topk;
+  const int nblk = (K > I ? K : I) / kScaleBlock;
   size_t o = 0;
-  m.stage = o;
-  o += (size_t)stages * kStageBytes;
-  m.scale_slot = round_up((size_t)kItemRows * nblk, 128);
-  m.scale = o;
-  o += kScaleSlots * m.scale_slot;
+  m.ring = o;
+  o += kRingBytes;
+  m.slot_bytes = (int)round_up((size_t)kRows * nblk, 128);
+  m.scales = o;
+  o += (size_t)kScaleSlots * m.slot_bytes;
   m.bars = o;
-  o += round_up((size_t)(2 * stages + 2 * kScaleSlots + kRowBars) * 8, 16);
-  m.red = o;
-  o += (size_t)kConsumerWarps * 2 * 32 * 4 * sizeof(float);
-  m.fin = o;
-  o += 256 * sizeof(float);
+  o += round_up((size_t)(kCW * kD + kScaleSlots + kRowBars + 1) * 8, 16);
   m.flags = o;
-  o += 32;   // int flags[4] + a 16-byte zero chunk
+  o += 64;   // int flags[8] + a 16-byte zero chunk + spare
   m.ints = o;
   o += (size_t)(5 * E + R + 6) * sizeof(int);
+  m.eb = o;
+  o += (size_t)(E + kDecodeMaxRoutes / kBatch + 2) * sizeof(int);
   m.row_sh = o;
-  o += (size_t)rows_cap * sizeof(int);
+  o += (size_t)R * sizeof(int);
   o = round_up(o, 128);
   m.xs = o;
   o += (size_t)xs_rows * xs_stride;
@@ -94,91 +98,14 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int phase, int T, int K, 
   return m;
 }
 
-struct Cursor {
-  int nt, gr, d, ng, e;
-};
-
-struct Ctx {
-  RouteTables tb;
-  const int* gbase;
-  int nD, NT, G;
-};
-
-__device__ __forceinline__ void cursor_expert(Cursor& c, const Ctx& x) {
-  if (c.d < x.nD) {
-    c.e = x.tb.touched[c.d];
-    c.ng = (x.tb.cnt[c.e] + kGroup - 1) / kGroup;
-  }
+// Balanced split of U units over n CTAs (the first U % n CTAs get one more).
+__device__ __forceinline__ int range_begin(int v, int U, int n) {
+  const int q = U / n, rem = U % n;
+  return v * q + (v < rem ? v : rem);
 }
 
-// Item index -> (d, nt, gr); items of expert d start at NT * gbase[d].
-__device__ __forceinline__ Cursor cursor_of_item(int64_t item, const Ctx& x) {
-  Cursor c;
-  int lo = 0, hi = x.nD;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((int64_t)x.NT * x.gbase[mid] <= item) lo = mid; else hi = mid;
-  }
-  c.d = lo;
-  cursor_expert(c, x);
-  const int local = (int)(item - (int64_t)x.NT * x.gbase[lo]);
-  c.nt = local / c.ng;
-  c.gr = local - c.nt * c.ng;
-  return c;
-}
-
-__device__ __forceinline__ void cursor_next_item(Cursor& c, const Ctx& x) {
-  if (++c.gr == c.ng) {
-    c.gr = 0;
-    if (++c.nt == x.NT) {
-      c.nt = 0;
-      ++c.d;
-      cursor_expert(c, x);
-    }
-  }
-}
-
-// Balanced split of U units over n CTAs (first U % n CTAs get one more).
-__device__ __forceinline__ int64_t range_begin(int v, int64_t U, int n) {
-  const int64_t q = U / n, rem = U % n;
-  return (int64_t)v * q + (v < rem ? v : rem);
-}
-__device__ __forceinline__ int owner_of_unit(int64_t u, int64_t U, int n) {
-  const int64_t q = U / n, rem = U % n;
-  if (u < rem * (q + 1)) return (int)(u / (q + 1));
-  return (int)(rem + (u - rem * (q + 1)) / q);
-}
-
-// First weight row of TMA box h (0, 1) of an item.
-template <int PHASE>
-__device__ __forceinline__ int box_row(const Cursor& c, const DecodeArgs& a, int h) {
-  if (PHASE == 1) return c.e * (2 * a.I) + h * a.I + c.nt * 16;
-  return c.e * a.K + c.nt * kItemRows + h * 16;
-}
-
-// Scale rows of an item into [32][nblk]: phase 1 two runs of 16 rows (gate,
-// up), phase 2 one run of 32 rows.
-template <int PHASE>
-__device__ __forceinline__ void issue_scales(const Cursor& c, const DecodeArgs& a, int nblk,
-                                             uint8_t* dst, uint64_t* bar) {
-  const uint32_t run = 16u * nblk;
-  mbar_arrive_expect_tx(bar, 2 * run);
-  if (PHASE == 1) {
-    bulk_load_split(dst, a.wsc + (size_t)box_row<1>(c, a, 0) * nblk, run, bar);
-    bulk_load_split(dst + run, a.wsc + (size_t)box_row<1>(c, a, 1) * nblk, run, bar);
-  } else {
-    bulk_load_split(dst, a.wsc + (size_t)box_row<2>(c, a, 0) * nblk, 2 * run, bar);
-  }
-}
-
-// Activation row (bf16) of route-list position q.
-template <int PHASE>
-__device__ __forceinline__ const uint16_t* act_row(const DecodeArgs& a, const RouteTables& tb,
-                                                   int q) {
-  const int r = tb.lst[q];
-  if (PHASE == 1) return a.x + (size_t)(r / a.topk) * a.K;
-  return a.x + (size_t)r * a.I;
-}
+// Items a warp owns among n items dealt round-robin to kCW warps.
+__device__ __forceinline__ int warp_items(int w, int n) { return n / kCW + (w < n % kCW ? 1 : 0); }
 
 __device__ __forceinline__ float pow2f(int e) {   // 2^e, -126 <= e <= 127
   return __uint_as_float((uint32_t)(e + 127) << 23);
@@ -199,183 +126,341 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float mul) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
-// Epilogue of one item from the 256 reduced values (thread o = consumer
-// thread ctid holds output (tile tt, lane l, element q): MMA row
-// tt*16 + l/4 + 8*(q/2), token column 2*(l%4) + q%2). All 256 consumer
-// threads call it.
-template <int PHASE>
-__device__ void finish_item(float v, const Cursor& c, const Ctx& x, const DecodeArgs& a,
-                            float* fin, int ctid, int p_lo, int n_sh, const int* row_sh,
-                            int* flags) {
-  const bool own = ctid < 256;     // threads 256.. only join the barriers
-  const int tt = (ctid >> 7) & 1, l = (ctid >> 2) & 31, q = ctid & 3;
-  const int g = l >> 2, t = l & 3;
-  const int col = 2 * t + (q & 1);
-  const int ntok = own ? min(kGroup, x.tb.cnt[c.e] - c.gr * kGroup) : 0;
-  const int qpos = x.tb.off[c.e] + c.gr * kGroup + col;   // route-list position of the column
-  float colmul = 1.0f;
-  int r = -1;
-  if (col < ntok) {
-    r = x.tb.lst[qpos];
-    const int idx = qpos - p_lo;
-    colmul = pow2f(idx >= 0 && idx < n_sh ? row_sh[idx] : 0);
-  }
-  if (PHASE == 1) {
-    if (own) fin[ctid] = v;
-    named_barrier(kBarConsumers, kConsumerThreads);
-    if (q < 2 && col < ntok) {
-      const float gate = fin[ctid] * colmul, up = fin[ctid + 2] * colmul;
-      const int n = c.nt * 16 + tt * 8 + g;
-      a.h[(size_t)r * a.I + n] = f32_to_bf16_rne(silu_f32(gate) * up);
-    }
-  } else {
-    // weighted route output; the slot-order sum over each token's routes is
-    // done by combine_kernel once every route is complete
-    const int m = c.nt * kItemRows + tt * 16 + g + 8 * (q >> 1);
-    if (col < ntok) a.P[(size_t)r * a.K + m] = a.wts[r] * (v * colmul);
-  }
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Order this thread's generic global writes before later async-proxy (bulk
+// copy) reads of them by any CTA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// y[t][m] = bf16( sum over slots j = 0..k-1 with a valid expert of
-// P[t*k + j][m] ), in slot order (deterministic). 8 outputs per thread.
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ P,
-                                                      const int32_t* __restrict__ ids, int T,
-                                                      int K, int E, int topk,
-                                                      uint16_t* __restrict__ y) {
-  grid_dependency_wait();   // P comes from the w2 phase
-  const int per_row = K / 8;
-  const int64_t n = (int64_t)T * per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / per_row), m8 = (int)(i - (int64_t)t * per_row) * 8;
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < topk; ++j) {
-      const int r = t * topk + j;
-      const int e = ids[r];
-      if (e < 0 || e >= E) continue;
-      const uint4 lo = ldcg16(P + (size_t)r * K + m8);
-      const uint4 hi = ldcg16(P + (size_t)r * K + m8 + 4);
-      s[0] += __uint_as_float(lo.x);
-      s[1] += __uint_as_float(lo.y);
-      s[2] += __uint_as_float(lo.z);
-      s[3] += __uint_as_float(lo.w);
-      s[4] += __uint_as_float(hi.x);
-      s[5] += __uint_as_float(hi.y);
-      s[6] += __uint_as_float(hi.z);
-      s[7] += __uint_as_float(hi.w);
-    }
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(s[2 * q + 1]), "f"(s[2 * q]));
-    *reinterpret_cast<uint4*>(y + (size_t)t * K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
+// Bounded wait until the grid counter reaches target; false when it gave up.
+__device__ __forceinline__ bool grid_wait(const int* ctr, uint32_t target) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    __nanosleep(64);
   }
+  return false;
 }
 
-// Lane-constant shared-memory offsets of the consumer warp's kWarpBlocks
-// blocks (bi = cw * kWarpBlocks + j) inside a stage / an item.
-struct LaneOffsets {
-  int a[kWarpBlocks][2][2];   // A word: [j][tile][row g | row g + 8], from the stage base
-  int s[kWarpBlocks][2][2];   // scale byte: [j][tile][row], from the item's scale rows + b_lo
-  int b[kWarpBlocks];         // B chunk: from the token row + 64 * b_lo
+// An item's routes: expert e, route-list positions q0 .. q0 + cnt - 1 (a batch
+// of at most kBatch of the expert's routes; more than one batch per expert
+// only when a token names the same expert in several slots).
+struct ItemRoutes {
+  int e, q0, cnt;
+};
+__device__ __forceinline__ ItemRoutes item_routes(const RouteTables& tb, const int* eb, int j) {
+  ItemRoutes r;
+  r.e = eb[j] >> 8;
+  const int t0 = (eb[j] & 255) * kBatch;
+  r.q0 = tb.off[r.e] + t0;
+  r.cnt = min(kBatch, tb.cnt[r.e] - t0);
+  return r;
+}
+
+// Per-phase view of the CTA's item range.
+struct PhaseView {
+  int kred, nblk, nc, NB;   // reduction length, scale blocks, stages per item, items per batch
+  int ib, n;                // first item and count of this CTA
+  int p_lo, n_need;         // route-list positions whose activation rows the items use
 };
 
-// One stage (chunk) of the current item for one consumer warp, both m16 tiles.
-// FAST: the item has no E8M0 byte 0 or 255, so 2^(s-127) is a single shift.
-// GLOB: some lane's token row is read (and converted) from global memory.
+__device__ __forceinline__ PhaseView phase_view(int phase, const DecodeArgs& a,
+                                                const RouteTables& tb, const int* eb, int nEB) {
+  PhaseView v;
+  v.kred = phase == 1 ? a.K : a.I;
+  v.nblk = v.kred / kScaleBlock;
+  v.nc = (v.kred / 2 + kChunk - 1) / kChunk;
+  v.NB = phase == 1 ? a.I / 8 : a.K / kRows;
+  const int U = nEB * v.NB;
+  v.ib = range_begin(blockIdx.x, U, gridDim.x);
+  v.n = range_begin(blockIdx.x + 1, U, gridDim.x) - v.ib;
+  v.p_lo = 0;
+  v.n_need = 0;
+  if (v.n > 0) {
+    const ItemRoutes r0 = item_routes(tb, eb, v.ib / v.NB);
+    const ItemRoutes r1 = item_routes(tb, eb, (v.ib + v.n - 1) / v.NB);
+    v.p_lo = r0.q0;
+    v.n_need = r1.q0 + r1.cnt - v.p_lo;
+  }
+  return v;
+}
+
+// Activation row (bf16) of route-list position q.
+__device__ __forceinline__ const uint16_t* act_row(int phase, const DecodeArgs& a,
+                                                   const RouteTables& tb, int q) {
+  const int r = tb.lst[q];
+  if (phase == 1) return a.x + (size_t)(r / a.topk) * a.K;
+  return a.h + (size_t)r * a.I;
+}
+
+// Weight row of item row 0 (half 0) or item row 8 (half 1) of item (e, rb).
+__device__ __forceinline__ int item_row(int phase, const DecodeArgs& a, int e, int rb, int half) {
+  if (phase == 1) return e * (2 * a.I) + half * a.I + rb * 8;
+  return e * a.K + rb * kRows + half * 8;
+}
+
+// Staged activation rows of a phase and the barriers that track them.
+struct RowPlan {
+  int xs_rows, rows_per_bar, nbars;
+};
+__device__ __forceinline__ RowPlan row_plan(const PhaseView& v, int xs_rows_cap) {
+  RowPlan r;
+  r.rows_per_bar = max(1, (int)(kRowBarBytes / ((uint32_t)v.kred * 2)));
+  r.xs_rows = min(min(v.n_need, xs_rows_cap), r.rows_per_bar * kRowBars);
+  r.nbars = (r.xs_rows + r.rows_per_bar - 1) / r.rows_per_bar;
+  return r;
+}
+
+// B operand of one token group for this lane (token column g): a staged f16
+// row (advanced 64 bytes per block; 0 for padding columns, which read a zero
+// chunk), or a bf16 row in global memory converted on the fly.
+struct BRows {
+  const uint8_t* row[kMaxGroups];
+  int step[kMaxGroups];
+  const uint16_t* src[kMaxGroups];
+  float mul[kMaxGroups];
+};
+
+// One 32-value block of one item for one warp: both m16 rows' 4-byte words,
+// their scales, and one MMA pair per token group.
 template <bool FAST, bool GLOB>
-__device__ __forceinline__ void consume_stage(float (&acc)[2][4], const uint8_t* stg,
-                                              const uint8_t* sc, int b_lo, int nb, int cw,
-                                              int t, const LaneOffsets& lo, const uint8_t* brow,
-                                              const uint8_t* zero16, const uint16_t* bglob,
-                                              float bmul) {
+__device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uint8_t* stg, int b,
+                                          int g, int t, const uint8_t* sc_g, const uint8_t* sc_g8,
+                                          int bglob, int ng, const BRows& br) {
+  const int off = (b >> 3) * kColBytes + g * 128 + ((((b & 7) ^ g) << 4) + (t << 2));
+  const uint32_t w0 = *reinterpret_cast<const uint32_t*>(stg + off);
+  const uint32_t w1 = *reinterpret_cast<const uint32_t*>(stg + off + 8 * 128);
+  const uint32_t s0 = sc_g[bglob], s1 = sc_g8[bglob];
+  uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+  e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
+  e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
+  const float f0 = FAST ? e8m0_to_f32_normal(s0) : e8m0_to_f32(s0);
+  const float f1 = FAST ? e8m0_to_f32_normal(s1) : e8m0_to_f32(s1);
 #pragma unroll
-  for (int j = 0; j < kWarpBlocks; ++j) {
-    if (nb < kChunkBlocks && cw * kWarpBlocks + j >= nb) break;
-    // B: token column g, physical k = 32b + 8t .. 32b + 8t + 7 (f16); padding
-    // columns read a zero chunk
+  for (int gr = 0; gr < kMaxGroups; ++gr) {
+    if (gr >= ng) break;
+    // B: token column g of the group, physical k = 32 bglob + 8t .. +7 (f16)
     uint4 bv;
-    if (GLOB && bglob != nullptr) {
-      const int b = b_lo + cw * kWarpBlocks + j;
-      bv = bf16x8_to_f16x8(ldcg16(bglob + b * 32 + t * 8), bmul);
-    } else {
-      const uint8_t* bp = brow != nullptr ? brow + b_lo * 64 + lo.b[j] : zero16;
-      bv = *reinterpret_cast<const uint4*>(bp);
-    }
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt) {
-      const uint32_t w0 = *reinterpret_cast<const uint32_t*>(stg + lo.a[j][tt][0]);
-      const uint32_t w1 = *reinterpret_cast<const uint32_t*>(stg + lo.a[j][tt][1]);
-      const uint32_t sb0 = sc[b_lo + lo.s[j][tt][0]], sb1 = sc[b_lo + lo.s[j][tt][1]];
-      uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
-      e2m1x8_to_f16x2(w0, a0, a1, a2, a3);
-      e2m1x8_to_f16x2(w1, c0, c1, c2, c3);
-      float d[4];
-      // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
-      mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
-      mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
-      const float f0 = FAST ? e8m0_to_f32_normal(sb0) : e8m0_to_f32(sb0);
-      const float f1 = FAST ? e8m0_to_f32_normal(sb1) : e8m0_to_f32(sb1);
-      acc[tt][0] = fmaf(d[0], f0, acc[tt][0]);
-      acc[tt][1] = fmaf(d[1], f0, acc[tt][1]);
-      acc[tt][2] = fmaf(d[2], f1, acc[tt][2]);
-      acc[tt][3] = fmaf(d[3], f1, acc[tt][3]);
-    }
+    if (GLOB && br.src[gr] != nullptr)
+      bv = bf16x8_to_f16x8(ldcg16(br.src[gr] + bglob * 32 + t * 8), br.mul[gr]);
+    else
+      bv = *reinterpret_cast<const uint4*>(br.row[gr] + bglob * br.step[gr]);
+    float d[4];
+    // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
+    mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
+    mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
+    acc[gr][0] = fmaf(d[0], f0, acc[gr][0]);
+    acc[gr][1] = fmaf(d[1], f0, acc[gr][1]);
+    acc[gr][2] = fmaf(d[2], f1, acc[gr][2]);
+    acc[gr][3] = fmaf(d[3], f1, acc[gr][3]);
   }
 }
 
-// All chunks [ch, ch_end) of one item: wait for each stage, consume, release.
+// NBAT consecutive 32-value blocks b0 .. b0+NBAT-1 of a stage (b0 a
+// compile-time multiple of 8) for an item with a single token group,
+// software-pipelined: every shared-memory load of the batch is issued before
+// the first conversion, and the blocks' MMA chains are independent, so their
+// latencies overlap. xo[u] is this lane's byte offset of block (8k + u) inside
+// a 128-byte column (row g, 128-byte swizzle); brow / scg / scg8 point at
+// block b0's activation chunk and scale bytes.
+template <bool FAST, int NBAT, int B0>
+__device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, const int (&xo)[8],
+                                           const uint8_t* scg, const uint8_t* scg8,
+                                           const uint8_t* brow) {
+  uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
+  uint4 bv[NBAT];
+#pragma unroll
+  for (int u = 0; u < NBAT; ++u) {
+    const uint8_t* p = stg + ((B0 + u) >> 3) * kColBytes + xo[(B0 + u) & 7];
+    w0[u] = *reinterpret_cast<const uint32_t*>(p);
+    w1[u] = *reinterpret_cast<const uint32_t*>(p + 8 * 128);
+    s0[u] = scg[u];
+    s1[u] = scg8[u];
+    bv[u] = *reinterpret_cast<const uint4*>(brow + u * 64);
+  }
+#pragma unroll
+  for (int u = 0; u < NBAT; ++u) {
+    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+    e2m1x8_to_f16x2(w0[u], a0, a1, a2, a3);
+    e2m1x8_to_f16x2(w1[u], c0, c1, c2, c3);
+    const float f0 = FAST ? e8m0_to_f32_normal(s0[u]) : e8m0_to_f32(s0[u]);
+    const float f1 = FAST ? e8m0_to_f32_normal(s1[u]) : e8m0_to_f32(s1[u]);
+    float d[4];
+    mma_f16_16816_z(d, a0, c0, a1, c1, bv[u].x, bv[u].y);
+    mma_f16_16816(d, a2, c2, a3, c3, bv[u].z, bv[u].w);
+    acc[0] = fmaf(d[0], f0, acc[0]);
+    acc[1] = fmaf(d[1], f0, acc[1]);
+    acc[2] = fmaf(d[2], f1, acc[2]);
+    acc[3] = fmaf(d[3], f1, acc[3]);
+  }
+}
+
+// The item sequence of one consumer warp across both phases (items k =
+// 0, 1, .. of phase 1, then of phase 2): weight rows of item row 0 / row 8.
+struct ItemCursor {
+  int phase, k;   // phase 3 = past the last item
+  int j, rb;      // expert-batch index and row block of the item (it = j NB + rb)
+};
+// Positions the cursor on the warp's first item of its phase (one division).
+__device__ __forceinline__ void cursor_locate(ItemCursor& c, const PhaseView& v1,
+                                              const PhaseView& v2, int cw) {
+  if (c.phase > 2) return;
+  const PhaseView& v = c.phase == 1 ? v1 : v2;
+  const int it = v.ib + c.k * kCW + cw;
+  c.j = it / v.NB;
+  c.rb = it - c.j * v.NB;
+}
+__device__ __forceinline__ void cursor_skip_empty(ItemCursor& c, int n1, int n2,
+                                                  const PhaseView& v1, const PhaseView& v2, int cw) {
+  bool moved = false;
+  while (c.phase <= 2 && c.k >= (c.phase == 1 ? n1 : n2)) {
+    ++c.phase;
+    c.k = 0;
+    moved = true;
+  }
+  if (moved) cursor_locate(c, v1, v2, cw);
+}
+// Next item of the warp: kCW items further in the CTA's range.
+__device__ __forceinline__ void cursor_next(ItemCursor& c, int n1, int n2, const PhaseView& v1,
+                                            const PhaseView& v2, int cw) {
+  const PhaseView& v = c.phase == 1 ? v1 : v2;
+  ++c.k;
+  c.rb += kCW;
+  while (c.rb >= v.NB) {
+    c.rb -= v.NB;
+    ++c.j;
+  }
+  cursor_skip_empty(c, n1, n2, v1, v2, cw);
+}
+__device__ __forceinline__ void cursor_rows(const ItemCursor& c, const DecodeArgs& a,
+                                            const int* eb, int& r0, int& r1) {
+  const int e = eb[c.j] >> 8;
+  r0 = item_row(c.phase, a, e, c.rb, 0);
+  r1 = item_row(c.phase, a, e, c.rb, 1);
+}
+
+// Lane 0 of a consumer warp: issues the warp's weight stages in order into
+// its kD-stage ring (stage n goes to slot n % kD, tracked by full[n % kD]).
+struct StageIssuer {
+  ItemCursor cur;
+  int c, count, row0, row1;
+};
+__device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams& P,
+                                            const PhaseView& v1, const PhaseView& v2, int n1,
+                                            int n2, const int* eb, int cw, uint8_t* ring_w,
+                                            uint64_t* full_w) {
+  if (is.cur.phase > 2) return;
+  const PhaseView& v = is.cur.phase == 1 ? v1 : v2;
+  if (is.c == 0) cursor_rows(is.cur, P.a, eb, is.row0, is.row1);
+  const int slot = is.count & (kD - 1);
+  uint8_t* dst = ring_w + slot * kStageBytes;
+  uint64_t* bar = &full_w[slot];
+  const int x0 = is.c * kChunk;
+  const int ncols = min(2, (v.kred / 2 - x0 + 127) / 128);
+  mbar_arrive_expect_tx(bar, (uint32_t)ncols * kColBytes);
+  for (int col = 0; col < ncols; ++col) {
+    if (is.cur.phase == 1) {   // 8 gate rows, then the 8 matching up rows
+      tma_load_2d(dst + col * kColBytes, &P.tmap1, x0 + col * 128, is.row0, bar);
+      tma_load_2d(dst + col * kColBytes + 8 * 128, &P.tmap1, x0 + col * 128, is.row1, bar);
+    } else {                   // 16 consecutive rows
+      tma_load_2d(dst + col * kColBytes, &P.tmap2, x0 + col * 128, is.row0, bar);
+    }
+  }
+  ++is.count;
+  if (++is.c == v.nc) {
+    is.c = 0;
+    cursor_next(is.cur, n1, n2, v1, v2, cw);
+  }
+}
+
+// Lane 0 of a consumer warp: the scale rows of the item at the cursor into
+// the warp's scale slot x (tracked by sfull_w[x]).
+__device__ __forceinline__ void issue_scales(const ItemCursor& cur, const DecodeArgs& a,
+                                             const PhaseView& v1, const PhaseView& v2,
+                                             const int* eb, int cw, uint8_t* dst, uint64_t* bar) {
+  const PhaseView& v = cur.phase == 1 ? v1 : v2;
+  const uint8_t* wsc = cur.phase == 1 ? a.s13 : a.s2;
+  int r0, r1;
+  cursor_rows(cur, a, eb, r0, r1);
+  const uint32_t run = 8u * v.nblk;   // scale bytes of 8 rows
+  mbar_arrive_expect_tx(bar, 2 * run);
+  bulk_load_split(dst, wsc + (size_t)r0 * v.nblk, run, bar);
+  bulk_load_split(dst + run, wsc + (size_t)r1 * v.nblk, run, bar);
+}
+
+// All stages of one item for one warp; false when a wait gave up. s is the
+// warp's running stage number (both phases).
 template <bool FAST, bool GLOB>
-__device__ __forceinline__ void consume_item(float (&acc)[2][4], uint8_t* stage_base,
-                                             uint64_t* full, uint64_t* empty, int S, int& st,
-                                             uint32_t& phase, bool& ok, const uint8_t* sc,
-                                             int ch, int ch_end, int nblk, int cw, int t,
-                                             int lane, const LaneOffsets& lo,
-                                             const uint8_t* brow, const uint8_t* zero16,
-                                             const uint16_t* bglob, float bmul) {
-  for (; ch < ch_end; ++ch) {
-    if (ok) ok = mbar_wait(&full[st], phase);
-    const int b_lo = ch * kChunkBlocks;
-    consume_stage<FAST, GLOB>(acc, stage_base + st * kStageBytes, sc, b_lo,
-                              min(kChunkBlocks, nblk - b_lo), cw, t, lo, brow, zero16, bglob,
-                              bmul);
-    // the stage is refilled by tensor copies (async proxy): order the generic
+__device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const int (&xo)[8],
+                                            const uint8_t* ring_w,
+                                            uint64_t* full_w, int& s, const PhaseView& v,
+                                            int lane, const uint8_t* sc, int ng, const BRows& br,
+                                            StageIssuer& is, const DecodeParams& P,
+                                            const PhaseView& v1, const PhaseView& v2, int n1,
+                                            int n2, const int* eb, int cw) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t* sc_g = sc + g * v.nblk;
+  const uint8_t* sc_g8 = sc + (g + 8) * v.nblk;
+  for (int c = 0; c < v.nc; ++c, ++s) {
+    // keep kD - 1 stages ahead: the slot refilled now held stage s - 1, which
+    // every lane has finished reading (fenced below)
+    if (lane == 0) issue_stage(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
+    const int slot = s & (kD - 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (uint32_t)(s / kD) & 1u))) return false;
+    const uint8_t* stg = ring_w + slot * kStageBytes;
+    const int nb = min(kChunkBlocks, v.nblk - c * kChunkBlocks);
+    const int bg = c * kChunkBlocks;   // first block of the stage in the row
+    if (!GLOB && ng == 1 && nb == kChunkBlocks) {
+      blocks_mma<FAST, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, br.row[0] + bg * 64);
+      blocks_mma<FAST, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8,
+                             br.row[0] + (bg + 8) * 64);
+    } else if (!GLOB && ng == 1) {   // partial last stage: batches of 8, 4, then single blocks
+      int b = 0;
+      if (nb >= 8) {
+        blocks_mma<FAST, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, br.row[0] + bg * 64);
+        b = 8;
+      }
+      for (; b < nb; ++b)
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+    } else if (nb == kChunkBlocks) {
+#pragma unroll 4
+      for (int b = 0; b < kChunkBlocks; ++b)
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, c * kChunkBlocks + b, ng, br);
+    } else {
+      for (int b = 0; b < nb; ++b)
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, c * kChunkBlocks + b, ng, br);
+    }
+    // the slot is refilled by tensor copies (async proxy): order the generic
     // reads of it before that write
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-    if (++st == S) {
-      st = 0;
-      phase ^= 1u;
-    }
   }
+  return true;
 }
 
-template <int PHASE>
-__global__ void __launch_bounds__(kThreads, 1)
-decode_kernel(const __grid_constant__ DecodeParams P) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (128-byte swizzled TMA tiles); offsetting the array
   // keeps the compiler's knowledge that these are shared-memory addresses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const DecodeArgs& a = P.a;
   const int E = a.E, R = a.T * a.topk;
-  const int kred = PHASE == 1 ? a.K : a.I;
-  const int nblk = kred / kScaleBlock;
-  const int NC = (nblk + kChunkBlocks - 1) / kChunkBlocks;
-  const int S = P.stages;
-  const DecodeSmem M = decode_smem_plan(PHASE, a.T, a.K, a.I, E, a.topk, S, P.rows_cap,
-                                        P.xs_rows_cap, P.xs_stride);
-  uint8_t* stage_base = smem + M.stage;
-  uint8_t* scale_base = smem + M.scale;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + M.bars);   // [S]
-  uint64_t* empty = full + S;                                     // [S]
-  uint64_t* sfull = empty + S;                                    // [kScaleSlots]
-  uint64_t* sempty = sfull + kScaleSlots;                         // [kScaleSlots]
-  uint64_t* xfull = sempty + kScaleSlots;                         // [kRowBars] staged rows
-  float* red = reinterpret_cast<float*>(smem + M.red);            // [warps][2][32][4]
-  float* fin = reinterpret_cast<float*>(smem + M.fin);            // [256]
+  const DecodeSmem M = decode_smem_plan(a.K, a.I, E, R, P.xs_rows_cap, P.xs_stride);
+  uint8_t* ring = smem + M.ring;
+  uint8_t* scales = smem + M.scales;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + M.bars);  // [kCW][kD]
+  uint64_t* sfull = wfull + kCW * kD;                             // [kCW][2]
+  uint64_t* xfull = sfull + kScaleSlots;                          // [kRowBars]
+  uint64_t* pdone = xfull + kRowBars;                             // control warp finished
   int* flags = reinterpret_cast<int*>(smem + M.flags);
+  const uint8_t* zero16 = reinterpret_cast<const uint8_t*>(flags + 8);
   RouteTables tb;
   tb.cnt = reinterpret_cast<int*>(smem + M.ints);
   tb.off = tb.cnt + E;
@@ -383,412 +468,392 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
   tb.touched = tb.run + E;
   tb.lst = tb.touched + E;
   tb.misc = tb.lst + R;
-  int* gbase = tb.misc + 4;                                        // [E+1]
-  int* row_sh = reinterpret_cast<int*>(smem + M.row_sh);          // [rows_cap]
-  uint8_t* xs_base = smem + M.xs;
+  int* row_sh = reinterpret_cast<int*>(smem + M.row_sh);          // [R]
+  int* eb = reinterpret_cast<int*>(smem + M.eb);                  // [nEB] (expert << 8) | batch
+  uint8_t* xs = smem + M.xs;
   const int xs_stride = P.xs_stride;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  const int nCta = gridDim.x;
 
-  if (PHASE == 1) grid_dependency_wait();   // inputs may come from the previous kernel
-  if (tid < 8) flags[tid] = 0;
+  if (tid < 16) flags[tid] = 0;
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
-    }
-    for (int i = 0; i < kScaleSlots; ++i) {
-      mbar_init(&sfull[i], 1);
-      mbar_init(&sempty[i], kConsumerWarps);
-    }
+    for (int i = 0; i < kCW * kD; ++i) mbar_init(&wfull[i], 1);
+    for (int i = 0; i < kScaleSlots; ++i) mbar_init(&sfull[i], 1);
     for (int i = 0; i < kRowBars; ++i) mbar_init(&xfull[i], 1);
+    mbar_init(pdone, 1);
     fence_barrier_init();
-    prefetch_tensormap(&P.tmap);
+    prefetch_tensormap(&P.tmap1);
+    prefetch_tensormap(&P.tmap2);
   }
   cta_route_small(a.ids, R, E, tb);   // ends with __syncthreads
   const int nD = tb.misc[0];
-  if (tid < 32) {
+  if (warp == 0) {   // expert-batch table: each touched expert's routes in batches of kBatch
     int carry = 0;
     for (int base = 0; base < nD; base += 32) {
       const int d = base + lane;
-      const int ng = d < nD ? (tb.cnt[tb.touched[d]] + kGroup - 1) / kGroup : 0;
-      int xsum = ng;
+      const int e = d < nD ? tb.touched[d] : 0;
+      const int nb = d < nD ? (tb.cnt[e] + kBatch - 1) / kBatch : 0;
+      int x = nb;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, xsum, o);
-        if (lane >= o) xsum += y;
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
-      if (d < nD) gbase[d] = carry + xsum - ng;
-      carry += __shfl_sync(0xffffffffu, xsum, 31);
+      for (int b = 0; b < nb; ++b) eb[carry + x - nb + b] = (e << 8) | b;
+      carry += __shfl_sync(0xffffffffu, x, 31);
     }
-    if (lane == 0) gbase[nD] = carry;
+    if (lane == 0) flags[2] = carry;
   }
   __syncthreads();
-  launch_dependents();
-
-  Ctx x;
-  x.tb = tb;
-  x.gbase = gbase;
-  x.nD = nD;
-  x.G = gbase[nD];
-  x.NT = PHASE == 1 ? a.I / 16 : a.K / kItemRows;
-
-  if (PHASE == 1 && blockIdx.x == 0 && tid == 0 && a.status != nullptr) {
+  const int nEB = flags[2];
+  if (blockIdx.x == 0 && tid == 0 && a.status != nullptr) {
     a.status[0] = tb.misc[1];
     a.status[1] = nD;
     a.status[2] = 0;
     a.status[3] = 0;
   }
+  const PhaseView v1 = phase_view(1, a, tb, eb, nEB);
+  const PhaseView v2 = phase_view(2, a, tb, eb, nEB);
+  const RowPlan rp1 = row_plan(v1, P.xs_rows_cap);
+  const RowPlan rp2 = row_plan(v2, P.xs_rows_cap);
+  int* gbar = a.gbar;   // [0] phase arrivals (two per CTA and call), [1] CTAs done
 
-  const int64_t U = (int64_t)x.NT * x.G * NC;
-  if (U == 0) return;   // no valid route at all (the combine writes y = 0)
-  const int nCta = gridDim.x;
-  const int64_t cub = range_begin(blockIdx.x, U, nCta);
-  const int64_t cue = range_begin(blockIdx.x + 1, U, nCta);
-  if (cub >= cue) return;
-  const int64_t i_first = cub / NC, i_last = (cue - 1) / NC;
-
-  // activation rows this CTA can need: every route of the touched experts
-  // its unit range covers (a contiguous stretch of the route list)
-  const Cursor c_first = cursor_of_item(i_first, x);
-  const Cursor c_last = cursor_of_item(i_last, x);
-  const int p_lo = tb.off[c_first.e];
-  const int p_need = tb.off[c_last.e] + tb.cnt[c_last.e] - p_lo;
-  const int n_sh = min(p_need, P.rows_cap);
-  // staged rows, tracked by kRowBars barriers of at most kRowBarBytes each
-  const int rows_per_bar = max(1, (int)(kRowBarBytes / ((uint32_t)kred * 2)));
-  const int xs_rows = min(min(n_sh, P.xs_rows_cap), rows_per_bar * kRowBars);
-
-  // ======================= producer warp =======================
+  // ======================= control warp =======================
   if (warp == 0) {
     if (lane == 0) {
-      // raw bf16 activation rows -> shared memory (converted by the consumers)
-      auto issue_rows = [&]() {
-        for (int r0 = 0; r0 < xs_rows; r0 += rows_per_bar) {
-          const int r1 = min(xs_rows, r0 + rows_per_bar);
-          uint64_t* bar = &xfull[r0 / rows_per_bar];
-          mbar_arrive_expect_tx(bar, (uint32_t)(r1 - r0) * kred * 2);
-          for (int r = r0; r < r1; ++r)
-            bulk_load_split(xs_base + (size_t)r * xs_stride, act_row<PHASE>(a, tb, p_lo + r),
-                            (uint32_t)kred * 2, bar);
-        }
-      };
-      // Phase 2 issues the h rows once phase 1 is complete, and always before
-      // its first blocking wait: the consumers need the rows before they can
-      // free any stage or scale slot.
-      bool rows_issued = false;
-      auto ensure_rows = [&]() {
-        if (rows_issued) return;
-        if (PHASE == 2) grid_dependency_wait();
-        issue_rows();
-        rows_issued = true;
-      };
-      int fail_site = 0;
-      if (PHASE == 1) ensure_rows();
-      Cursor c = cursor_of_item(i_first, x);
-      int ch = (int)(cub - i_first * NC);
-      int k = 0, seq = 0, st = 0;
-      uint32_t phase = 0;      // parity of the current pass over the stages
-      bool ok = true;
-      for (int64_t u = cub; u < cue && ok; ++u) {
-        if (u == cub || ch == 0) {
-          const int slot = seq % kScaleSlots;
-          if (seq >= kScaleSlots) {
-            ensure_rows();
-            ok = mbar_wait(&sempty[slot], ((seq / kScaleSlots) - 1) & 1);
-          }
-          if (!ok) {
-            fail_site |= 1;
+      int fail = 0;
+      for (int phase = 1; phase <= 2; ++phase) {
+        const PhaseView& v = phase == 1 ? v1 : v2;
+        const RowPlan& rp = phase == 1 ? rp1 : rp2;
+        if (phase == 2) {
+          if (!grid_wait(gbar, (uint32_t)nCta)) {
+            fail = 64;
             break;
           }
-          issue_scales<PHASE>(c, a, nblk, scale_base + slot * M.scale_slot, &sfull[slot]);
-          ++seq;
+          fence_proxy_async_global();
         }
-        if (k >= S) {
-          ensure_rows();
-          ok = mbar_wait(&empty[st], phase ^ 1u);
-        }
-        if (!ok) {
-          fail_site |= 2;
-          break;
-        }
-        uint8_t* dst = stage_base + (size_t)st * kStageBytes;
-        // columns of 8 blocks that start inside the row (a partial last
-        // column reads zeros past the row end)
-        const int ncols = min(kChunkBlocks / 8, (nblk - ch * kChunkBlocks + 7) / 8);
-        mbar_arrive_expect_tx(&full[st], ncols * 2 * kBoxBytes);
-        const int x0 = ch * kChunkBlocks * 16;
-        for (int col = 0; col < ncols; ++col) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(dst + (col * 2 + h) * kBoxBytes, &P.tmap, x0 + col * 128,
-                        box_row<PHASE>(c, a, h), &full[st]);
-        }
-        ++k;
-        if (++st == S) {
-          st = 0;
-          phase ^= 1u;
-        }
-        if (++ch == NC) {
-          ch = 0;
-          cursor_next_item(c, x);
+        // activation rows -> shared memory (converted by the consumers)
+        for (int r0 = 0; r0 < rp.xs_rows; r0 += rp.rows_per_bar) {
+          const int r1 = min(rp.xs_rows, r0 + rp.rows_per_bar);
+          uint64_t* bar = &xfull[r0 / rp.rows_per_bar];
+          mbar_arrive_expect_tx(bar, (uint32_t)(r1 - r0) * v.kred * 2);
+          for (int r = r0; r < r1; ++r)
+            bulk_load_split(xs + (size_t)r * xs_stride, act_row(phase, a, tb, v.p_lo + r),
+                            (uint32_t)v.kred * 2, bar);
         }
       }
-      ensure_rows();
-      if (fail_site != 0 && a.status != nullptr) {
-        atomicOr(&a.status[2], fail_site << (PHASE == 1 ? 0 : 8));
+      if (fail != 0 && a.status != nullptr) {
+        atomicOr(&a.status[2], fail);
         atomicCAS(&a.status[3], 0, blockIdx.x + 1);
       }
+      mbar_arrive(pdone);   // past its grid wait: the counters may be reset
     }
     return;
   }
 
   // ======================= consumer warps =======================
-  const int cw = warp - 1;        // consumer warp 0..7
-  const int ctid = tid - 32;      // 0..255
+  const int cw = warp - 1;
+  const int ctid = tid - 32;
   const int g = lane >> 2, t = lane & 3;
-
-
-  if (PHASE == 2) grid_dependency_wait();   // h is complete from here on
+  int xo[8];   // byte offset of this lane's word of block u (0..7) in a 128-byte column
+#pragma unroll
+  for (int u = 0; u < 8; ++u) xo[u] = g * 128 + (((u ^ g) << 4) + (t << 2));
+  uint8_t* ring_w = ring + (size_t)cw * kD * kStageBytes;
+  uint64_t* full_w = wfull + cw * kD;
+  uint64_t* sfull_w = sfull + cw * 2;
+  uint8_t* scale_w = scales + (size_t)cw * 2 * M.slot_bytes;
+  const int n1 = warp_items(cw, v1.n), n2 = warp_items(cw, v2.n);
   bool ok = true;
-  int fail_site = 0;
-  for (int i = 0; i * rows_per_bar < xs_rows; ++i) ok = ok && mbar_wait(&xfull[i], 0);
-  if (!ok) fail_site |= 4;
-  // One warp per row: the largest exponent of the row, then (staged rows)
-  // conversion in place to f16 with max |x| * 2^-sh in [2^14, 2^15) -- exact
-  // in f16 down to 2^-31 of the row maximum. Rows past the staged ones are
-  // only scanned (read from global memory when used).
-  for (int r = cw; r < n_sh; r += kConsumerWarps) {
-    const bool staged = r < xs_rows;
-    uint4* row = reinterpret_cast<uint4*>(xs_base + (size_t)r * xs_stride);
-    const uint4* src = reinterpret_cast<const uint4*>(act_row<PHASE>(a, tb, p_lo + r));
-    uint32_t emax = 0;
-    for (int c16 = lane; c16 < kred / 8; c16 += 32) {
-      const uint4 v = staged ? row[c16] : ldcg16(src + c16);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        emax = max(emax, (w[i] >> 7) & 0xFFu);
-        emax = max(emax, (w[i] >> 23) & 0xFFu);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-    const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
-    if (lane == 0) row_sh[r] = sh;
-    if (staged) {
-      const float mul = pow2f(-sh);
-      for (int c16 = lane; c16 < kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
+  int fail = 0;
+  int s = 0;                 // running stage number of this warp
+  int kitems = 0;            // items this warp has started
+  uint32_t rows_used = 0;    // staged-row barriers used in phase 1
+  // stage and scale pipelines: the first kD - 1 stages and the first item's scales
+  StageIssuer is;
+  is.cur.phase = 1;
+  is.cur.k = 0;
+  is.c = 0;
+  is.count = 0;
+  is.row0 = is.row1 = 0;
+  is.cur.j = is.cur.rb = 0;
+  cursor_locate(is.cur, v1, v2, cw);
+  cursor_skip_empty(is.cur, n1, n2, v1, v2, cw);
+  ItemCursor sc_next = is.cur;   // next item whose scale rows are to be issued
+  int sc_count = 0;              // scale copies issued (lane 0)
+  if (lane == 0) {
+    for (int i = 0; i < kD - 1; ++i) issue_stage(is, P, v1, v2, n1, n2, eb, cw, ring_w, full_w);
+    if (sc_next.phase <= 2) {
+      issue_scales(sc_next, a, v1, v2, eb, cw, scale_w, &sfull_w[0]);
+      ++sc_count;
     }
   }
-  named_barrier(kBarConsumers, kConsumerThreads);
+  cursor_next(sc_next, n1, n2, v1, v2, cw);
 
-  Cursor c = c_first;
-  int64_t item = i_first;
-  int st = 0, seq = 0;
-  uint32_t phase = 0;
-  float acc[2][4];
-  LaneOffsets lo;
-#pragma unroll
-  for (int j = 0; j < kWarpBlocks; ++j) {
-    const int bi = cw * kWarpBlocks + j;
-    const int colsw = (bi >> 3) * (2 * kBoxBytes) + ((((bi & 7) ^ g) << 4) + (t << 2));
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt) {
-      if (PHASE == 1) {   // box 0 = gate rows, box 1 = up rows; tile tt = rows tt*8 ..
-        lo.a[j][tt][0] = colsw + (tt * 8 + g) * 128;
-        lo.a[j][tt][1] = colsw + kBoxBytes + (tt * 8 + g) * 128;
-        lo.s[j][tt][0] = (tt * 8 + g) * nblk + bi;
-        lo.s[j][tt][1] = (16 + tt * 8 + g) * nblk + bi;
-      } else {            // box tt = rows 16tt .. 16tt+15
-        lo.a[j][tt][0] = colsw + tt * kBoxBytes + g * 128;
-        lo.a[j][tt][1] = colsw + tt * kBoxBytes + (g + 8) * 128;
-        lo.s[j][tt][0] = (tt * 16 + g) * nblk + bi;
-        lo.s[j][tt][1] = (tt * 16 + g + 8) * nblk + bi;
-      }
-    }
-    lo.b[j] = bi * 64 + t * 16;
-  }
-  const uint8_t* zero16 = reinterpret_cast<const uint8_t*>(flags + 4);   // B chunk of padding columns
-
-  int ch = (int)(cub - i_first * NC);
-  int64_t u = cub;
-  while (u < cue) {
-    // ---- item start: its scales, the special-byte flag, this lane's B row
-    const int slot = seq % kScaleSlots;
-    if (ok) {
-      ok = mbar_wait(&sfull[slot], (seq / kScaleSlots) & 1);
-      if (!ok) fail_site |= 8;
-    }
-    const uint8_t* sc = scale_base + slot * M.scale_slot;
-    int bad = 0;
-    const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
-    for (int i = ctid; i < (kItemRows * nblk) / 4; i += kConsumerThreads) {
-      const uint32_t w = sw[i];
-      const uint32_t z = (w - 0x01010101u) & ~w & 0x80808080u;     // some byte == 0
-      const uint32_t f = (~w - 0x01010101u) & w & 0x80808080u;     // some byte == 0xFF
-      bad |= (z | f) != 0u;
-    }
-    const bool special = named_barrier_or(kBarConsumers, kConsumerThreads, bad != 0);
-    const int ntok = min(kGroup, tb.cnt[c.e] - c.gr * kGroup);
-    const uint8_t* brow = nullptr;
-    const uint16_t* bglob = nullptr;
-    float bmul = 1.0f;
-    if (g < ntok) {
-      const int qpos = tb.off[c.e] + c.gr * kGroup + g;
-      const int r = qpos - p_lo;
-      if (r >= 0 && r < xs_rows) {
-        brow = xs_base + (size_t)r * xs_stride;
-      } else {
-        bglob = act_row<PHASE>(a, tb, qpos);
-        bmul = pow2f(-(r >= 0 && r < n_sh ? row_sh[r] : 0));
-      }
-    }
-    const bool glob = __any_sync(0xffffffffu, bglob != nullptr);
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) acc[tt][q] = 0.f;
-    const int ch_end = (int)min((int64_t)NC, ch + (cue - u));
-    const int ch_start = ch;
-    if (!special && !glob)
-      consume_item<true, false>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
-                                nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
-    else if (!special)
-      consume_item<true, true>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
-                               nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
-    else
-      consume_item<false, true>(acc, stage_base, full, empty, S, st, phase, ok, sc, ch, ch_end,
-                                nblk, cw, t, lane, lo, brow, zero16, bglob, bmul);
-    u += ch_end - ch_start;
-
-    // ---- item end: reduce the warps' fragments, then finish or publish
-    float* my = red + ((size_t)cw * 2 * 32 + lane) * 4;
-#pragma unroll
-    for (int tt = 0; tt < 2; ++tt)
-      *reinterpret_cast<float4*>(my + tt * 32 * 4) =
-          make_float4(acc[tt][0], acc[tt][1], acc[tt][2], acc[tt][3]);
-    named_barrier(kBarConsumers, kConsumerThreads);
-    float v = 0.f;
-    if (ctid < 256) {
-      const int tt = ctid >> 7, l = (ctid >> 2) & 31, q = ctid & 3;
-      for (int w = 0; w < kConsumerWarps; ++w) v += red[(((size_t)w * 2 + tt) * 32 + l) * 4 + q];
-    }
-    const bool whole = (ch_end == NC) && (item * NC >= cub);
-    if (whole) {
-      finish_item<PHASE>(v, c, x, a, fin, ctid, p_lo, n_sh, row_sh, flags);
-    } else {
-      // partial item: publish, count, and let the last CTA to arrive finish it
-      const int va = owner_of_unit(item * NC, U, nCta);
-      const int vb = owner_of_unit(item * NC + NC - 1, U, nCta);
-      const int pslot = (item == i_first) ? 0 : 1;
-      if (ctid < 256) a.parts[((size_t)blockIdx.x * 2 + pslot) * 256 + ctid] = v;
+  for (int phase = 1; phase <= 2; ++phase) {
+    const PhaseView& v = phase == 1 ? v1 : v2;
+    const RowPlan& rp = phase == 1 ? rp1 : rp2;
+    if (phase == 2) {   // h of every CTA is complete (also for rows read from global)
+      if (ctid == 0) flags[1] = grid_wait(gbar, (uint32_t)nCta) ? 1 : 0;
       named_barrier(kBarConsumers, kConsumerThreads);
-      if (ctid == 0) {
-        __threadfence();
-        flags[1] = atomicAdd(&a.item_ctr[va], 1);
-        __threadfence();
+      if (flags[1] == 0 && ok) {
+        ok = false;
+        fail |= 2;
       }
-      named_barrier(kBarConsumers, kConsumerThreads);
-      if (flags[1] == vb - va) {
-        const bool va_first = range_begin(va, U, nCta) == item * NC;
-        float tot = 0.f;
-        for (int w = va; w <= vb && ctid < 256; ++w) {
-          const int sl = (w == va && !va_first) ? 1 : 0;
-          tot += ldcg_f32(a.parts + ((size_t)w * 2 + sl) * 256 + ctid);
+    }
+    // -- activation rows: wait, prescale (one warp per row), convert to f16
+    for (int i = 0; i < rp.nbars && ok; ++i) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&xfull[i], phase == 2 ? (rows_used >> i & 1u) : 0u));
+      if (!ok) fail |= 4;
+    }
+    if (phase == 1) rows_used = (1u << rp.nbars) - 1u;
+    for (int r = cw; r < v.n_need && ok; r += kCW) {
+      const bool staged = r < rp.xs_rows;
+      uint4* row = reinterpret_cast<uint4*>(xs + (size_t)r * xs_stride);
+      const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
+      uint32_t emax = 0;
+      for (int c16 = lane; c16 < v.kred / 8; c16 += 32) {
+        const uint4 q = staged ? row[c16] : ldcg16(src + c16);
+        const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          emax = max(emax, (wq[i] >> 7) & 0xFFu);
+          emax = max(emax, (wq[i] >> 23) & 0xFFu);
         }
-        finish_item<PHASE>(tot, c, x, a, fin, ctid, p_lo, n_sh, row_sh, flags);
-        if (ctid == 0) a.item_ctr[va] = 0;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+      const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
+      if (lane == 0) row_sh[r] = sh;
+      if (staged) {
+        const float mul = pow2f(-sh);
+        for (int c16 = lane; c16 < v.kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
       }
     }
-    fence_proxy_async_smem();   // scale slot: refilled by a bulk copy (async proxy)
     named_barrier(kBarConsumers, kConsumerThreads);
-    if (lane == 0) mbar_arrive(&sempty[seq % kScaleSlots]);
-    ++seq;
-    ch = 0;
-    ++item;
-    cursor_next_item(c, x);
+
+    // -- this warp's items of the phase: item k of the warp is CTA item ib + k kCW + cw
+    const int my_n = phase == 1 ? n1 : n2;
+    for (int k = 0; k < my_n && ok; ++k) {
+      const int it = v.ib + k * kCW + cw;
+      const ItemRoutes ir = item_routes(tb, eb, it / v.NB);
+      const int rb = it % v.NB;
+      const int sx = kitems & 1;
+      // the next item's scale rows go to the other slot, which the previous
+      // item (finished and fenced) no longer reads
+      if (lane == 0 && sc_next.phase <= 2) {
+        issue_scales(sc_next, a, v1, v2, eb, cw, scale_w + (sx ^ 1) * M.slot_bytes, &sfull_w[sx ^ 1]);
+        ++sc_count;
+      }
+      cursor_next(sc_next, n1, n2, v1, v2, cw);
+      ok = __all_sync(0xffffffffu, mbar_wait(&sfull_w[sx], (uint32_t)(kitems >> 1) & 1u));
+      if (!ok) {
+        fail |= 8;
+        break;
+      }
+      const uint8_t* sc = scale_w + sx * M.slot_bytes;
+      // E8M0 bytes 0 / 255 in this item: take the exact general conversion
+      bool bad = false;
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
+      for (int i = lane; i < (kRows * v.nblk) / 4; i += 32) {
+        const uint32_t x = sw[i];
+        const uint32_t z = (x - 0x01010101u) & ~x & 0x80808080u;     // some byte == 0
+        const uint32_t f = (~x - 0x01010101u) & x & 0x80808080u;     // some byte == 0xFF
+        bad |= (z | f) != 0u;
+      }
+      const bool special = __any_sync(0xffffffffu, bad);
+      // B rows of the item's token groups for this lane's token column g
+      const int cnt = ir.cnt;
+      const int ng = (cnt + kGroup - 1) / kGroup;
+      BRows br;
+      bool glob = false;
+      // padding columns (tokens past the item's) read the item's first row when
+      // it is staged (their columns are never stored), else a zero chunk
+      const int q_first = ir.q0 - v.p_lo;
+      const bool first_staged = q_first < rp.xs_rows;
+#pragma unroll
+      for (int gr = 0; gr < kMaxGroups; ++gr) {
+        br.row[gr] = first_staged ? xs + (size_t)q_first * xs_stride + t * 16 : zero16;
+        br.step[gr] = first_staged ? 64 : 0;
+        br.src[gr] = nullptr;
+        br.mul[gr] = 1.f;
+        if (gr < ng && gr * kGroup + g < cnt) {
+          const int q = ir.q0 + gr * kGroup + g - v.p_lo;
+          if (q < rp.xs_rows) {
+            br.row[gr] = xs + (size_t)q * xs_stride + t * 16;
+            br.step[gr] = 64;
+          } else {
+            br.src[gr] = act_row(phase, a, tb, v.p_lo + q);
+            br.mul[gr] = pow2f(-row_sh[q]);
+            glob = true;
+          }
+        }
+      }
+      glob = __any_sync(0xffffffffu, glob);
+      float acc[kMaxGroups][4];
+#pragma unroll
+      for (int gr = 0; gr < kMaxGroups; ++gr)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
+      if (!special && !glob)
+        ok = item_stages<true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+                                      n1, n2, eb, cw);
+      else if (!special)
+        ok = item_stages<true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+                                     n1, n2, eb, cw);
+      else
+        ok = item_stages<false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+                                      n1, n2, eb, cw);
+      if (!ok) {
+        fail |= 16;
+        break;
+      }
+      // -- epilogue: rows g, g+8 and token columns 2t, 2t+1 of each group
+#pragma unroll
+      for (int gr = 0; gr < kMaxGroups; ++gr) {
+        if (gr >= ng) break;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int n = gr * kGroup + 2 * t + j;
+          if (n >= cnt) continue;
+          const int qpos = ir.q0 + n;
+          const int r = tb.lst[qpos];
+          const float colmul = pow2f(row_sh[qpos - v.p_lo]);
+          if (phase == 1) {
+            const float gate = acc[gr][j] * colmul, up = acc[gr][2 + j] * colmul;
+            a.h[(size_t)r * a.I + rb * 8 + g] = f32_to_bf16_rne(silu_f32(gate) * up);
+          } else {
+            const float wr = a.wts[r];
+            a.P[(size_t)r * a.K + rb * kRows + g] = wr * (acc[gr][j] * colmul);
+            a.P[(size_t)r * a.K + rb * kRows + g + 8] = wr * (acc[gr][2 + j] * colmul);
+          }
+        }
+      }
+      // the scale slot is refilled by a bulk copy (async proxy)
+      fence_proxy_async_smem();
+      __syncwarp();
+      ++kitems;
+    }
+    // -- grid arrival: this CTA's outputs of the phase are written
+    if (phase == 1) fence_proxy_async_global();   // h is read next by bulk copies
+    __threadfence();
+    named_barrier(kBarConsumers, kConsumerThreads);
+    if (ctid == 0) atomicAdd(gbar, 1);
+  }
+
+  // -- combine: y [T, K] (this CTA's slice), once every route output exists
+  if (ctid == 0) flags[0] = grid_wait(gbar, 2u * nCta) ? 1 : 0;
+  named_barrier(kBarConsumers, kConsumerThreads);
+  if (flags[0] == 0) {
+    ok = false;
+    fail |= 32;
+  } else {
+    const int per_row = a.K / 8;
+    const int total = a.T * per_row;
+    const int c0 = range_begin(blockIdx.x, total, nCta);
+    const int c1 = range_begin(blockIdx.x + 1, total, nCta);
+    for (int i = c0 + ctid; i < c1; i += kConsumerThreads) {
+      const int tt = i / per_row, m8 = (i - tt * per_row) * 8;
+      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < a.topk; ++j) {
+        const int r = tt * a.topk + j;
+        const int e = a.ids[r];
+        if (e < 0 || e >= E) continue;
+        const uint4 lo = ldcg16(a.P + (size_t)r * a.K + m8);
+        const uint4 hi = ldcg16(a.P + (size_t)r * a.K + m8 + 4);
+        sum[0] += __uint_as_float(lo.x);
+        sum[1] += __uint_as_float(lo.y);
+        sum[2] += __uint_as_float(lo.z);
+        sum[3] += __uint_as_float(lo.w);
+        sum[4] += __uint_as_float(hi.x);
+        sum[5] += __uint_as_float(hi.y);
+        sum[6] += __uint_as_float(hi.z);
+        sum[7] += __uint_as_float(hi.w);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(sum[2 * q + 1]), "f"(sum[2 * q]));
+      *reinterpret_cast<uint4*>(a.y + (size_t)tt * a.K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  // the last CTA out leaves the grid counters at zero for the next call (once
+  // this CTA's control warp no longer reads them)
+  named_barrier(kBarConsumers, kConsumerThreads);
+  if (ctid == 0) {
+    if (!mbar_wait(pdone, 0)) {
+      ok = false;
+      fail |= 64;
+    }
+    __threadfence();
+    if (atomicAdd(&gbar[1], 1) == nCta - 1) {
+      atomicExch(&gbar[0], 0);
+      atomicExch(&gbar[1], 0);
+    }
+  }
+  // stages issued ahead but never consumed (only after a failed wait) must
+  // land before the CTA exits
+  if (lane == 0) {
+    for (int n = s; n < is.count; ++n) mbar_wait(&full_w[n & (kD - 1)], (uint32_t)(n / kD) & 1u);
+    for (int n = kitems; n < sc_count; ++n) mbar_wait(&sfull_w[n & 1], (uint32_t)(n >> 1) & 1u);
   }
   if (!ok && lane == 0 && a.status != nullptr) {
-    atomicOr(&a.status[2], (fail_site | 16) << (PHASE == 1 ? 0 : 8));
+    atomicOr(&a.status[2], (fail | 128) << 8);
     atomicCAS(&a.status[3], 0, blockIdx.x + 1);
   }
 }
 
-cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
-                           uint16_t* y, int num_sms, cudaStream_t stream, bool pdl) {
-  const int64_t n = (int64_t)T * (K / 8);
-  int64_t blocks = (n + 255) / 256;
-  if (blocks > (int64_t)num_sms * 4) blocks = (int64_t)num_sms * 4;
-  if (blocks < 1) blocks = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, P, ids, T, K, E, topk, y);
+size_t decode_smem_bytes(int K, int I, int E, int R, int xs_rows, int xs_stride) {
+  return decode_smem_plan(K, I, E, R, xs_rows, xs_stride).total + 1024;
 }
 
-size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int stages) {
-  return decode_smem_plan(phase, T, K, I, E, topk, stages, T * topk, 0, 0).total + 1024;
+int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
+
+bool decode_fits(int K, int I, int E, int R, int max_smem) {
+  // one staged row at least (rows past the staged ones are read from global memory)
+  return decode_smem_bytes(K, I, E, R, 1, decode_row_stride(K, I)) <= (size_t)max_smem;
 }
 
-template <typename Kern>
-static cudaError_t ensure_smem(Kern kernel, size_t bytes, size_t& granted) {
-  if (bytes <= 48 * 1024 || bytes <= granted) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) granted = bytes;
-  return e;
-}
-
-cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_smem,
-                          const CUtensorMap& tmap, cudaStream_t stream, bool pdl) {
-  static size_t granted1 = 0, granted2 = 0;
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
+                          int num_sms, int max_smem, cudaStream_t stream) {
+  static size_t granted = 0;
   DecodeParams p;
-  p.tmap = tmap;
+  p.tmap1 = tmap1;
+  p.tmap2 = tmap2;
   p.a = a;
-  const int kred = phase == 1 ? a.K : a.I;
   const int R = a.T * a.topk;
-  p.rows_cap = R;
-  p.xs_stride = (int)round_up((size_t)kred * 2, 128) + 64;
-  // deepest pipeline (up to 5 stages) that still leaves room for a few rows
-  int stages = 5;
-  size_t fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
-  const size_t want_rows = (size_t)(R < 8 ? R : 8) * p.xs_stride;
-  while (stages > 3 && fixed + want_rows > (size_t)max_smem) {
-    --stages;
-    fixed = decode_fixed_smem(phase, a.T, a.K, a.I, a.E, a.topk, stages);
-  }
-  if (fixed > (size_t)max_smem) return cudaErrorInvalidValue;
-  p.stages = stages;
+  p.xs_stride = decode_row_stride(a.K, a.I);
+  const size_t fixed = decode_smem_bytes(a.K, a.I, a.E, R, 0, p.xs_stride);
+  if (fixed + p.xs_stride > (size_t)max_smem) return cudaErrorInvalidValue;
   size_t rows = ((size_t)max_smem - fixed) / p.xs_stride;
   if (rows > (size_t)R) rows = R;
   p.xs_rows_cap = (int)rows;
-  const size_t smem = fixed + rows * p.xs_stride;
-
+  p.stages = kD;
+  const size_t smem = decode_smem_bytes(a.K, a.I, a.E, R, (int)rows, p.xs_stride);
+  if (smem > granted) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    granted = smem;
+  }
+  // every CTA must be resident at once (grid barriers): one per SM, cooperative launch
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (phase == 1) {
-    cudaError_t e = ensure_smem(decode_kernel<1>, smem, granted1);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<1>, p);
-  }
-  cudaError_t e = ensure_smem(decode_kernel<2>, smem, granted2);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<2>, p);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, p);
 }
 
 }  // namespace mxmoe

@@ -8,44 +8,37 @@
 
 namespace mxmoe {
 
-// One decode phase (1: w13 + SwiGLU, 2: w2 + weighted combine).
+// One decode call (1..32 tokens): w13 + SwiGLU, w2 + routing weight, combine.
 struct DecodeArgs {
-  const uint16_t* x;      // phase 1: hidden bf16 [T, K]; phase 2: h bf16 [R, I]
+  const uint16_t* x;      // hidden bf16 [T, K]
   const int32_t* ids;     // [T * topk]
   const float* wts;       // [T * topk]
-  const uint8_t* wq;      // packed weights of the phase
-  const uint8_t* wsc;     // scales of the phase
+  const uint8_t *w13, *s13, *w2, *s2;
   int T, K, I, E, topk;
-  uint16_t* h;            // phase 1 output, bf16 [R, I]
-  float* P;               // phase 2 weighted route outputs, fp32 [R, K]
-  uint16_t* y;            // phase 2 output, bf16 [T, K]
-  float* parts;           // stream-K partials [CTAs][2][256]
-  int* item_ctr;          // [CTAs], zero between calls
-  int32_t* status;        // [4] or null (phase 1 writes it)
+  uint16_t* h;            // bf16 [R, I] (SwiGLU output)
+  float* P;               // weighted route outputs, fp32 [R, K]
+  uint16_t* y;            // bf16 [T, K]
+  int* gbar;              // [2] grid-barrier counters, zero between calls
+  int32_t* status;        // [4] or null
 };
 
-constexpr int kMaxCtas = 256;            // grid cap; sizes the stream-K bookkeeping
-
-// Kernel parameter block of one decode phase: the weight tensor map (TMA
-// descriptor, 64-byte aligned) and the launch-time shared-memory plan.
+// Kernel parameter block: the two weight tensor maps (TMA descriptors,
+// 64-byte aligned) and the launch-time shared-memory plan.
 struct DecodeParams {
-  CUtensorMap tmap;       // packed weights of the phase as 2-D u8 [rows][row bytes]
+  CUtensorMap tmap1;      // w13 packed as 2-D u8 [E*2I rows][K/2], box {128, 8}
+  CUtensorMap tmap2;      // w2 packed as 2-D u8 [E*K rows][I/2], box {128, 16}
   DecodeArgs a;
-  int stages;             // weight pipeline depth (24 KB stages)
-  int rows_cap;           // activation rows whose prescale is tracked (>= routes)
+  int stages;             // weight ring depth (4 KB stages)
   int xs_rows_cap;        // activation rows staged in shared memory
   int xs_stride;          // bytes per staged row (f16), = 64 mod 128
 };
 
-// Shared-memory plan of a decode phase for a given stage count; returns the
-// bytes needed before the staged activation rows (and their offset).
-size_t decode_fixed_smem(int phase, int T, int K, int I, int E, int topk, int stages);
+// Whether the decode kernel's shared-memory plan fits for these sizes.
+bool decode_fits(int K, int I, int E, int R, int max_smem);
 
-cudaError_t launch_decode(const DecodeArgs& a, int phase, int num_sms, int max_smem,
-                          const CUtensorMap& tmap, cudaStream_t stream, bool pdl);
-
-cudaError_t launch_combine(const float* P, const int32_t* ids, int T, int K, int E, int topk,
-                           uint16_t* y, int num_sms, cudaStream_t stream, bool pdl);
+// One cooperative launch (one CTA per SM, all resident) per decode call.
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
+                          int num_sms, int max_smem, cudaStream_t stream);
 
 // 2-D tiled tensor map [dim1 rows][dim0 elements] with the given row pitch,
 // box {box0, box1}; reads past the tensor return zeros (api.cu).

@@ -46,11 +46,26 @@ def oracle_rows(case: synth.Case, tokens=None, intermediate="bf16"):
     return O.forward(hb, sub_ids, wts, w13, s13, w2, s2, intermediate=intermediate)
 
 
-def compare(y_gpu: torch.Tensor, case: synth.Case, tokens=None):
-    """(rel_l2 vs bf16-intermediate oracle, rel_l2 vs fp32-intermediate, max abs err)."""
+def compare(y_gpu: torch.Tensor, case: synth.Case, tokens=None, with_gap: bool = False):
+    """(rel_l2 vs bf16-intermediate oracle, rel_l2 vs fp32-intermediate, max abs err)
+    and, with_gap, the two oracle modes' own rel_l2 distance."""
     got = bf16_to_f64(y_gpu)
     if tokens is not None:
         got = got[np.asarray(tokens)]
     ref_a = oracle_rows(case, tokens, "bf16")
     ref_b = oracle_rows(case, tokens, "fp32")
-    return rel_l2(got, ref_a), rel_l2(got, ref_b), float(np.abs(got - ref_a).max())
+    out = (rel_l2(got, ref_a), rel_l2(got, ref_b), float(np.abs(got - ref_a).max()))
+    return out + (rel_l2(ref_a, ref_b),) if with_gap else out
+
+
+def gate(y_gpu: torch.Tensor, case: synth.Case, tokens=None):
+    """The parity gate. Against the pages' reference (fp32 accumulation with a
+    bf16 intermediate h): rel_l2 <= TOL_REL_L2. Against the fp32-intermediate
+    reading: rel_l2 <= max(TOL_REL_L2, gap + rel_l2 vs the first), gap being the
+    distance of the two oracle modes themselves -- the bf16 rounding of h that
+    the layer specifies separates them, by more than the tolerance on short
+    reductions with few tokens (triangle inequality). Returns the figures."""
+    ra, rb, mx, gap = compare(y_gpu, case, tokens, with_gap=True)
+    assert ra <= TOL_REL_L2, (ra, rb, mx, gap)
+    assert rb <= max(TOL_REL_L2, gap + ra), (ra, rb, mx, gap)
+    return ra, rb, mx

@@ -98,6 +98,8 @@ def test_forward_rejects_bad_arguments_without_a_gpu(L):
     assert fwd(L, T=-1) == m.ERR_SHAPE
     assert fwd(L, T=33, path=1) == m.ERR_SHAPE    # decode limited to 32 tokens
     assert fwd(L, K=96, I=96, T=40, path=2) == m.ERR_SHAPE   # prefill needs multiples of 64
+    assert fwd(L, K=96, I=64, T=4, path=1) == m.ERR_SHAPE    # decode needs multiples of 64 too
+    assert fwd(L, K=64, I=96, T=4, path=1) == m.ERR_SHAPE
     assert fwd(L, hidden=VP(0x10008)) == m.ERR_ALIGN
     assert fwd(L, w13=VP(0x40004)) == m.ERR_ALIGN
     assert fwd(L, s2=VP(0x70001)) == m.ERR_ALIGN
