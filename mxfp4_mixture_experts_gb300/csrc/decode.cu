@@ -44,17 +44,14 @@
 
 namespace mxmoe {
 
-constexpr int kCW = 8;                       // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;     // 288
-constexpr int kD = 4;                        // stages in each consumer warp's ring
-constexpr int kConsumerThreads = kCW * 32;
+// stages in each warp's ring: 4 with 8 warps, 3 with 12 (shared memory)
+__host__ __device__ constexpr int ring_depth(int cw) { return cw >= 12 ? 3 : 4; }
 constexpr int kRows = 16;                    // weight rows per item (one m16 tile)
 constexpr int kChunk = 256;                  // packed bytes per row per stage
 constexpr int kChunkBlocks = kChunk / 16;    // 16 scale blocks per stage
 constexpr int kStageBytes = kRows * kChunk;  // 4 KB
 constexpr int kColBytes = kRows * 128;       // one 128-byte column of a stage
-constexpr int kScaleSlots = 2 * kCW;         // two per consumer warp
-constexpr int kRingBytes = kCW * kD * kStageBytes;
+
 constexpr int kGroup = 8;                    // tokens per mma n-tile
 constexpr int kBatch = 32;                   // routes of one expert an item multiplies at most
 constexpr int kMaxGroups = kBatch / kGroup;
@@ -71,18 +68,19 @@ struct DecodeSmem {
   int slot_bytes;
 };
 
-__host__ __device__ inline DecodeSmem decode_smem_plan(int K, int I, int E, int R, int xs_rows,
-                                                       int xs_stride) {
+// cw warps, each with a ring_depth(cw)-stage ring and two scale slots.
+__host__ __device__ inline DecodeSmem decode_smem_plan(int cw, int K, int I, int E, int R,
+                                                       int xs_rows, int xs_stride) {
   DecodeSmem m;
   const int nblk = (K > I ? K : I) / kScaleBlock;
   size_t o = 0;
   m.ring = o;
-  o += kRingBytes;
+  o += (size_t)cw * ring_depth(cw) * kStageBytes;
   m.slot_bytes = (int)round_up((size_t)kRows * nblk, 128);
   m.scales = o;
-  o += (size_t)kScaleSlots * m.slot_bytes;
+  o += (size_t)2 * cw * m.slot_bytes;
   m.bars = o;
-  o += round_up((size_t)(kCW * kD + kScaleSlots + kRowBars + 1) * 8, 16);
+  o += round_up((size_t)(cw * ring_depth(cw) + 2 * cw + kRowBars) * 8, 16);
   m.flags = o;
   o += 64;   // int flags[8] + a 16-byte zero chunk + spare
   m.ints = o;
@@ -104,8 +102,9 @@ __device__ __forceinline__ int range_begin(int v, int U, int n) {
   return v * q + (v < rem ? v : rem);
 }
 
-// Items a warp owns among n items dealt round-robin to kCW warps.
-__device__ __forceinline__ int warp_items(int w, int n) { return n / kCW + (w < n % kCW ? 1 : 0); }
+// Items a warp owns among n items dealt round-robin to CW warps.
+template <int CW>
+__device__ __forceinline__ int warp_items(int w, int n) { return n / CW + (w < n % CW ? 1 : 0); }
 
 __device__ __forceinline__ float pow2f(int e) {   // 2^e, -126 <= e <= 127
   return __uint_as_float((uint32_t)(e + 127) << 23);
@@ -309,14 +308,16 @@ struct ItemCursor {
   int j, rb;      // expert-batch index and row block of the item (it = j NB + rb)
 };
 // Positions the cursor on the warp's first item of its phase (one division).
+template <int CW>
 __device__ __forceinline__ void cursor_locate(ItemCursor& c, const PhaseView& v1,
                                               const PhaseView& v2, int cw) {
   if (c.phase > 2) return;
   const PhaseView& v = c.phase == 1 ? v1 : v2;
-  const int it = v.ib + c.k * kCW + cw;
+  const int it = v.ib + c.k * CW + cw;
   c.j = it / v.NB;
   c.rb = it - c.j * v.NB;
 }
+template <int CW>
 __device__ __forceinline__ void cursor_skip_empty(ItemCursor& c, int n1, int n2,
                                                   const PhaseView& v1, const PhaseView& v2, int cw) {
   bool moved = false;
@@ -325,19 +326,20 @@ __device__ __forceinline__ void cursor_skip_empty(ItemCursor& c, int n1, int n2,
     c.k = 0;
     moved = true;
   }
-  if (moved) cursor_locate(c, v1, v2, cw);
+  if (moved) cursor_locate<CW>(c, v1, v2, cw);
 }
-// Next item of the warp: kCW items further in the CTA's range.
+// Next item of the warp: CW items further in the CTA's range.
+template <int CW>
 __device__ __forceinline__ void cursor_next(ItemCursor& c, int n1, int n2, const PhaseView& v1,
                                             const PhaseView& v2, int cw) {
   const PhaseView& v = c.phase == 1 ? v1 : v2;
   ++c.k;
-  c.rb += kCW;
+  c.rb += CW;
   while (c.rb >= v.NB) {
     c.rb -= v.NB;
     ++c.j;
   }
-  cursor_skip_empty(c, n1, n2, v1, v2, cw);
+  cursor_skip_empty<CW>(c, n1, n2, v1, v2, cw);
 }
 __device__ __forceinline__ void cursor_rows(const ItemCursor& c, const DecodeArgs& a,
                                             const int* eb, int& r0, int& r1) {
@@ -347,11 +349,12 @@ __device__ __forceinline__ void cursor_rows(const ItemCursor& c, const DecodeArg
 }
 
 // Lane 0 of a consumer warp: issues the warp's weight stages in order into
-// its kD-stage ring (stage n goes to slot n % kD, tracked by full[n % kD]).
+// its KD-stage ring (stage n goes to slot n % KD, tracked by full[n % KD]).
 struct StageIssuer {
   ItemCursor cur;
   int c, count, row0, row1;
 };
+template <int CW>
 __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams& P,
                                             const PhaseView& v1, const PhaseView& v2, int n1,
                                             int n2, const int* eb, int cw, uint8_t* ring_w,
@@ -359,7 +362,8 @@ __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams&
   if (is.cur.phase > 2) return;
   const PhaseView& v = is.cur.phase == 1 ? v1 : v2;
   if (is.c == 0) cursor_rows(is.cur, P.a, eb, is.row0, is.row1);
-  const int slot = is.count & (kD - 1);
+  constexpr int KD = ring_depth(CW);
+  const int slot = is.count % KD;
   uint8_t* dst = ring_w + slot * kStageBytes;
   uint64_t* bar = &full_w[slot];
   const int x0 = is.c * kChunk;
@@ -376,7 +380,7 @@ __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams&
   ++is.count;
   if (++is.c == v.nc) {
     is.c = 0;
-    cursor_next(is.cur, n1, n2, v1, v2, cw);
+    cursor_next<CW>(is.cur, n1, n2, v1, v2, cw);
   }
 }
 
@@ -397,7 +401,7 @@ __device__ __forceinline__ void issue_scales(const ItemCursor& cur, const Decode
 
 // All stages of one item for one warp; false when a wait gave up. s is the
 // warp's running stage number (both phases).
-template <bool FAST, bool GLOB>
+template <int CW, bool FAST, bool GLOB>
 __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const int (&xo)[8],
                                             const uint8_t* ring_w,
                                             uint64_t* full_w, int& s, const PhaseView& v,
@@ -405,15 +409,16 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
                                             StageIssuer& is, const DecodeParams& P,
                                             const PhaseView& v1, const PhaseView& v2, int n1,
                                             int n2, const int* eb, int cw) {
+  constexpr int KD = ring_depth(CW);
   const int g = lane >> 2, t = lane & 3;
   const uint8_t* sc_g = sc + g * v.nblk;
   const uint8_t* sc_g8 = sc + (g + 8) * v.nblk;
   for (int c = 0; c < v.nc; ++c, ++s) {
-    // keep kD - 1 stages ahead: the slot refilled now held stage s - 1, which
+    // keep KD - 1 stages ahead: the slot refilled now held stage s - 1, which
     // every lane has finished reading (fenced below)
-    if (lane == 0) issue_stage(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
-    const int slot = s & (kD - 1);
-    if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (uint32_t)(s / kD) & 1u))) return false;
+    if (lane == 0) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
+    const int slot = s % KD;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (uint32_t)(s / KD) & 1u))) return false;
     const uint8_t* stg = ring_w + slot * kStageBytes;
     const int nb = min(kChunkBlocks, v.nblk - c * kChunkBlocks);
     const int bg = c * kChunkBlocks;   // first block of the stage in the row
@@ -445,20 +450,38 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
+// Stages the activation rows of a phase into shared memory (one thread).
+__device__ __forceinline__ void issue_rows(int phase, const PhaseView& v, const RowPlan& rp,
+                                           const DecodeArgs& a, const RouteTables& tb, uint8_t* xs,
+                                           int xs_stride, uint64_t* xfull) {
+  for (int r0 = 0; r0 < rp.xs_rows; r0 += rp.rows_per_bar) {
+    const int r1 = min(rp.xs_rows, r0 + rp.rows_per_bar);
+    uint64_t* bar = &xfull[r0 / rp.rows_per_bar];
+    mbar_arrive_expect_tx(bar, (uint32_t)(r1 - r0) * v.kred * 2);
+    for (int r = r0; r < r1; ++r)
+      bulk_load_split(xs + (size_t)r * xs_stride, act_row(phase, a, tb, v.p_lo + r),
+                      (uint32_t)v.kred * 2, bar);
+  }
+}
+
+// CW warps, all of them consumers; warp 0's lane 0 also stages the activation
+// rows and waits for the grid between the phases.
+template <int CW>
+__global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
+  constexpr int kThreadsCW = CW * 32;
+  constexpr int KD = ring_depth(CW);
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base (128-byte swizzled TMA tiles); offsetting the array
   // keeps the compiler's knowledge that these are shared-memory addresses
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const DecodeArgs& a = P.a;
   const int E = a.E, R = a.T * a.topk;
-  const DecodeSmem M = decode_smem_plan(a.K, a.I, E, R, P.xs_rows_cap, P.xs_stride);
+  const DecodeSmem M = decode_smem_plan(CW, a.K, a.I, E, R, P.xs_rows_cap, P.xs_stride);
   uint8_t* ring = smem + M.ring;
   uint8_t* scales = smem + M.scales;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + M.bars);  // [kCW][kD]
-  uint64_t* sfull = wfull + kCW * kD;                             // [kCW][2]
-  uint64_t* xfull = sfull + kScaleSlots;                          // [kRowBars]
-  uint64_t* pdone = xfull + kRowBars;                             // control warp finished
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + M.bars);  // [CW][KD]
+  uint64_t* sfull = wfull + CW * KD;                              // [CW][2]
+  uint64_t* xfull = sfull + 2 * CW;                               // [kRowBars]
   int* flags = reinterpret_cast<int*>(smem + M.flags);
   const uint8_t* zero16 = reinterpret_cast<const uint8_t*>(flags + 8);
   RouteTables tb;
@@ -479,10 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   if (tid < 16) flags[tid] = 0;
   if (tid == 0) {
-    for (int i = 0; i < kCW * kD; ++i) mbar_init(&wfull[i], 1);
-    for (int i = 0; i < kScaleSlots; ++i) mbar_init(&sfull[i], 1);
+    for (int i = 0; i < CW * KD; ++i) mbar_init(&wfull[i], 1);
+    for (int i = 0; i < 2 * CW; ++i) mbar_init(&sfull[i], 1);
     for (int i = 0; i < kRowBars; ++i) mbar_init(&xfull[i], 1);
-    mbar_init(pdone, 1);
     fence_barrier_init();
     prefetch_tensormap(&P.tmap1);
     prefetch_tensormap(&P.tmap2);
@@ -520,57 +542,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const RowPlan rp2 = row_plan(v2, P.xs_rows_cap);
   int* gbar = a.gbar;   // [0] phase arrivals (two per CTA and call), [1] CTAs done
 
-  // ======================= control warp =======================
-  if (warp == 0) {
-    if (lane == 0) {
-      int fail = 0;
-      for (int phase = 1; phase <= 2; ++phase) {
-        const PhaseView& v = phase == 1 ? v1 : v2;
-        const RowPlan& rp = phase == 1 ? rp1 : rp2;
-        if (phase == 2) {
-          if (!grid_wait(gbar, (uint32_t)nCta)) {
-            fail = 64;
-            break;
-          }
-          fence_proxy_async_global();
-        }
-        // activation rows -> shared memory (converted by the consumers)
-        for (int r0 = 0; r0 < rp.xs_rows; r0 += rp.rows_per_bar) {
-          const int r1 = min(rp.xs_rows, r0 + rp.rows_per_bar);
-          uint64_t* bar = &xfull[r0 / rp.rows_per_bar];
-          mbar_arrive_expect_tx(bar, (uint32_t)(r1 - r0) * v.kred * 2);
-          for (int r = r0; r < r1; ++r)
-            bulk_load_split(xs + (size_t)r * xs_stride, act_row(phase, a, tb, v.p_lo + r),
-                            (uint32_t)v.kred * 2, bar);
-        }
-      }
-      if (fail != 0 && a.status != nullptr) {
-        atomicOr(&a.status[2], fail);
-        atomicCAS(&a.status[3], 0, blockIdx.x + 1);
-      }
-      mbar_arrive(pdone);   // past its grid wait: the counters may be reset
-    }
-    return;
-  }
-
-  // ======================= consumer warps =======================
-  const int cw = warp - 1;
-  const int ctid = tid - 32;
+  // ======================= all warps: consumers =======================
+  const int cw = warp;
+  const int ctid = tid;
+  if (ctid == 0) issue_rows(1, v1, rp1, a, tb, xs, xs_stride, xfull);
   const int g = lane >> 2, t = lane & 3;
   int xo[8];   // byte offset of this lane's word of block u (0..7) in a 128-byte column
 #pragma unroll
   for (int u = 0; u < 8; ++u) xo[u] = g * 128 + (((u ^ g) << 4) + (t << 2));
-  uint8_t* ring_w = ring + (size_t)cw * kD * kStageBytes;
-  uint64_t* full_w = wfull + cw * kD;
+  uint8_t* ring_w = ring + (size_t)cw * KD * kStageBytes;
+  uint64_t* full_w = wfull + cw * KD;
   uint64_t* sfull_w = sfull + cw * 2;
   uint8_t* scale_w = scales + (size_t)cw * 2 * M.slot_bytes;
-  const int n1 = warp_items(cw, v1.n), n2 = warp_items(cw, v2.n);
+  const int n1 = warp_items<CW>(cw, v1.n), n2 = warp_items<CW>(cw, v2.n);
   bool ok = true;
   int fail = 0;
   int s = 0;                 // running stage number of this warp
   int kitems = 0;            // items this warp has started
   uint32_t rows_used = 0;    // staged-row barriers used in phase 1
-  // stage and scale pipelines: the first kD - 1 stages and the first item's scales
+  // stage and scale pipelines: the first KD - 1 stages and the first item's scales
   StageIssuer is;
   is.cur.phase = 1;
   is.cur.k = 0;
@@ -578,25 +568,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   is.count = 0;
   is.row0 = is.row1 = 0;
   is.cur.j = is.cur.rb = 0;
-  cursor_locate(is.cur, v1, v2, cw);
-  cursor_skip_empty(is.cur, n1, n2, v1, v2, cw);
+  cursor_locate<CW>(is.cur, v1, v2, cw);
+  cursor_skip_empty<CW>(is.cur, n1, n2, v1, v2, cw);
   ItemCursor sc_next = is.cur;   // next item whose scale rows are to be issued
   int sc_count = 0;              // scale copies issued (lane 0)
   if (lane == 0) {
-    for (int i = 0; i < kD - 1; ++i) issue_stage(is, P, v1, v2, n1, n2, eb, cw, ring_w, full_w);
+    for (int i = 0; i < KD - 1; ++i) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, ring_w, full_w);
     if (sc_next.phase <= 2) {
       issue_scales(sc_next, a, v1, v2, eb, cw, scale_w, &sfull_w[0]);
       ++sc_count;
     }
   }
-  cursor_next(sc_next, n1, n2, v1, v2, cw);
+  cursor_next<CW>(sc_next, n1, n2, v1, v2, cw);
 
   for (int phase = 1; phase <= 2; ++phase) {
     const PhaseView& v = phase == 1 ? v1 : v2;
     const RowPlan& rp = phase == 1 ? rp1 : rp2;
     if (phase == 2) {   // h of every CTA is complete (also for rows read from global)
-      if (ctid == 0) flags[1] = grid_wait(gbar, (uint32_t)nCta) ? 1 : 0;
-      named_barrier(kBarConsumers, kConsumerThreads);
+      if (ctid == 0) {
+        flags[1] = grid_wait(gbar, (uint32_t)nCta) ? 1 : 0;
+        if (flags[1] != 0) {
+          fence_proxy_async_global();
+          issue_rows(2, v2, rp2, a, tb, xs, xs_stride, xfull);
+        }
+      }
+      named_barrier(kBarConsumers, kThreadsCW);
       if (flags[1] == 0 && ok) {
         ok = false;
         fail |= 2;
@@ -609,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       if (!ok) fail |= 4;
     }
     if (phase == 1) rows_used = (1u << rp.nbars) - 1u;
-    for (int r = cw; r < v.n_need && ok; r += kCW) {
+    for (int r = cw; r < v.n_need && ok; r += CW) {
       const bool staged = r < rp.xs_rows;
       uint4* row = reinterpret_cast<uint4*>(xs + (size_t)r * xs_stride);
       const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
@@ -632,12 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         for (int c16 = lane; c16 < v.kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
       }
     }
-    named_barrier(kBarConsumers, kConsumerThreads);
+    named_barrier(kBarConsumers, kThreadsCW);
 
-    // -- this warp's items of the phase: item k of the warp is CTA item ib + k kCW + cw
+    // -- this warp's items of the phase: item k of the warp is CTA item ib + k CW + cw
     const int my_n = phase == 1 ? n1 : n2;
     for (int k = 0; k < my_n && ok; ++k) {
-      const int it = v.ib + k * kCW + cw;
+      const int it = v.ib + k * CW + cw;
       const ItemRoutes ir = item_routes(tb, eb, it / v.NB);
       const int rb = it % v.NB;
       const int sx = kitems & 1;
@@ -647,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         issue_scales(sc_next, a, v1, v2, eb, cw, scale_w + (sx ^ 1) * M.slot_bytes, &sfull_w[sx ^ 1]);
         ++sc_count;
       }
-      cursor_next(sc_next, n1, n2, v1, v2, cw);
+      cursor_next<CW>(sc_next, n1, n2, v1, v2, cw);
       ok = __all_sync(0xffffffffu, mbar_wait(&sfull_w[sx], (uint32_t)(kitems >> 1) & 1u));
       if (!ok) {
         fail |= 8;
@@ -698,13 +694,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
       if (!special && !glob)
-        ok = item_stages<true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+        ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
                                       n1, n2, eb, cw);
       else if (!special)
-        ok = item_stages<true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+        ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
                                      n1, n2, eb, cw);
       else
-        ok = item_stages<false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
+        ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
                                       n1, n2, eb, cw);
       if (!ok) {
         fail |= 16;
@@ -739,13 +735,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // -- grid arrival: this CTA's outputs of the phase are written
     if (phase == 1) fence_proxy_async_global();   // h is read next by bulk copies
     __threadfence();
-    named_barrier(kBarConsumers, kConsumerThreads);
+    named_barrier(kBarConsumers, kThreadsCW);
     if (ctid == 0) atomicAdd(gbar, 1);
   }
 
   // -- combine: y [T, K] (this CTA's slice), once every route output exists
   if (ctid == 0) flags[0] = grid_wait(gbar, 2u * nCta) ? 1 : 0;
-  named_barrier(kBarConsumers, kConsumerThreads);
+  named_barrier(kBarConsumers, kThreadsCW);
   if (flags[0] == 0) {
     ok = false;
     fail |= 32;
@@ -754,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const int total = a.T * per_row;
     const int c0 = range_begin(blockIdx.x, total, nCta);
     const int c1 = range_begin(blockIdx.x + 1, total, nCta);
-    for (int i = c0 + ctid; i < c1; i += kConsumerThreads) {
+    for (int i = c0 + ctid; i < c1; i += kThreadsCW) {
       const int tt = i / per_row, m8 = (i - tt * per_row) * 8;
       float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       for (int j = 0; j < a.topk; ++j) {
@@ -779,14 +775,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       *reinterpret_cast<uint4*>(a.y + (size_t)tt * a.K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
-  // the last CTA out leaves the grid counters at zero for the next call (once
-  // this CTA's control warp no longer reads them)
-  named_barrier(kBarConsumers, kConsumerThreads);
+  // the last CTA out leaves the grid counters at zero for the next call
+  named_barrier(kBarConsumers, kThreadsCW);
   if (ctid == 0) {
-    if (!mbar_wait(pdone, 0)) {
-      ok = false;
-      fail |= 64;
-    }
     __threadfence();
     if (atomicAdd(&gbar[1], 1) == nCta - 1) {
       atomicExch(&gbar[0], 0);
@@ -796,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // stages issued ahead but never consumed (only after a failed wait) must
   // land before the CTA exits
   if (lane == 0) {
-    for (int n = s; n < is.count; ++n) mbar_wait(&full_w[n & (kD - 1)], (uint32_t)(n / kD) & 1u);
+    for (int n = s; n < is.count; ++n) mbar_wait(&full_w[n % KD], (uint32_t)(n / KD) & 1u);
     for (int n = kitems; n < sc_count; ++n) mbar_wait(&sfull_w[n & 1], (uint32_t)(n >> 1) & 1u);
   }
   if (!ok && lane == 0 && a.status != nullptr) {
@@ -805,47 +796,43 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   }
 }
 
-size_t decode_smem_bytes(int K, int I, int E, int R, int xs_rows, int xs_stride) {
-  return decode_smem_plan(K, I, E, R, xs_rows, xs_stride).total + 1024;
+size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs_stride) {
+  return decode_smem_plan(cw, K, I, E, R, xs_rows, xs_stride).total + 1024;
 }
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-bool decode_fits(int K, int I, int E, int R, int max_smem) {
-  // one staged row at least (rows past the staged ones are read from global memory)
-  return decode_smem_bytes(K, I, E, R, 1, decode_row_stride(K, I)) <= (size_t)max_smem;
+// Warps per CTA: 12 when their rings, scale slots and a few staged rows fit,
+// else 8 (large K); 0 when even 8 do not fit.
+int decode_warps(int K, int I, int E, int R, int max_smem) {
+  const int stride = decode_row_stride(K, I);
+  const size_t rows4 = (size_t)(R < 4 ? R : 4) * stride;
+  if (decode_smem_bytes(12, K, I, E, R, 0, stride) + rows4 <= (size_t)max_smem) return 12;
+  if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
+  return 0;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
-                          int num_sms, int max_smem, cudaStream_t stream) {
+bool decode_fits(int K, int I, int E, int R, int max_smem) {
+  return decode_warps(K, I, E, R, max_smem) != 0;
+}
+
+template <int CW>
+static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cudaStream_t stream) {
   static size_t granted = 0;
-  DecodeParams p;
-  p.tmap1 = tmap1;
-  p.tmap2 = tmap2;
-  p.a = a;
-  const int R = a.T * a.topk;
-  p.xs_stride = decode_row_stride(a.K, a.I);
-  const size_t fixed = decode_smem_bytes(a.K, a.I, a.E, R, 0, p.xs_stride);
-  if (fixed + p.xs_stride > (size_t)max_smem) return cudaErrorInvalidValue;
-  size_t rows = ((size_t)max_smem - fixed) / p.xs_stride;
-  if (rows > (size_t)R) rows = R;
-  p.xs_rows_cap = (int)rows;
-  p.stages = kD;
-  const size_t smem = decode_smem_bytes(a.K, a.I, a.E, R, (int)rows, p.xs_stride);
   if (smem > granted) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     granted = smem;
   }
   // every CTA must be resident at once (grid barriers): one per SM, cooperative launch
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<CW>, CW * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(CW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -853,7 +840,26 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const C
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<CW>, p);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
+                          int num_sms, int max_smem, cudaStream_t stream) {
+  DecodeParams p;
+  p.tmap1 = tmap1;
+  p.tmap2 = tmap2;
+  p.a = a;
+  const int R = a.T * a.topk;
+  const int cw = decode_warps(a.K, a.I, a.E, R, max_smem);
+  if (cw == 0) return cudaErrorInvalidValue;
+  p.xs_stride = decode_row_stride(a.K, a.I);
+  const size_t fixed = decode_smem_bytes(cw, a.K, a.I, a.E, R, 0, p.xs_stride);
+  size_t rows = ((size_t)max_smem - fixed) / p.xs_stride;
+  if (rows > (size_t)R) rows = R;
+  p.xs_rows_cap = (int)rows;
+  p.stages = ring_depth(cw);
+  const size_t smem = decode_smem_bytes(cw, a.K, a.I, a.E, R, (int)rows, p.xs_stride);
+  return cw == 12 ? launch_cw<12>(p, smem, num_sms, stream) : launch_cw<8>(p, smem, num_sms, stream);
 }
 
 }  // namespace mxmoe
