@@ -15,10 +15,10 @@ line carries the same measurement, shorter, under ``prefill``.
 
 Printed: one JSON line (rank 0). ``value`` is microseconds per MoE call
 (whole job: all calls of all ranks / time), taken from CUDA-graph replays of
-the step with events on the replay stream. ``roofline`` is the decode kernel
-(one cooperative launch per call: w13 + SwiGLU, w2, combine) timed with CUDA
-events around each launch over a second timed pass, against the touched
-experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
+the step with events on the replay stream. ``per_T`` and ``roofline`` come
+from a second pass in which each layer's call (one cooperative decode launch:
+w13 + SwiGLU, w2, combine) is its own graph, replayed alone between CUDA
+events, against the touched experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
 with host buffers (pinned host -> device copies of each call's activations and
 routing, device -> host copy of its output, inside the timed region).
 ``--impl reference`` times the CPU oracle on the same workload instead.
@@ -407,6 +407,64 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
     return out
 
 
+def measure_configs(dev, hbm_gbs: float, reps: int = 10):
+    """The other decode workload shapes (the 32-expert single layer at T = 1,
+    the 6144 x 2048 256-expert layer at T = 1, 8, 32 and the wide-K skewed
+    layer at T = 1 .. 32): microseconds per call and GB/s of the touched
+    experts' packed bytes, from CUDA-graph replays of single calls that
+    alternate between two layers of weights (inputs larger than L2)."""
+    from mxfp4_mixture_experts_gb300 import moe
+    out = {}
+    stream = torch.cuda.Stream()
+    for name in ("single32", "glm256", "widek256"):
+        sh = synth.SHAPES[name]
+        Ts = (1, 4, 16, 32) if name == "single32" else sh.tokens
+        layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev) for l in range(2)]
+        res = {}
+        for T in Ts:
+            ws = moe.new_workspace(T, sh.K, sh.I, sh.E, sh.topk, dev)
+            calls = []
+            for l, (w13, s13, w2, s2) in enumerate(layers):
+                rng = np.random.Generator(np.random.PCG64(1000 * T + l))
+                hidden, _, ids, w = synth.draw_activations(sh, T, rng)
+                x, ids, w = hidden.to(dev), ids.to(dev), w.to(dev)
+                y = torch.empty(T, sh.K, dtype=torch.bfloat16, device=dev)
+                args = (x, ids, w, w13, s13, w2, s2)
+                with torch.cuda.stream(stream):
+                    moe.forward(*args, out=y, workspace=ws)
+                stream.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    moe.forward(*args, out=y, workspace=ws)
+                D = touched_experts(ids, sh.E)
+                calls.append((g, D * expert_bytes(sh.K, sh.I) + 4 * T * sh.K, D, args, y))
+            times, bytes_ = [], []
+            with torch.cuda.stream(stream):
+                for r in range(reps + 2):
+                    for g, b, D, _, _ in calls:
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        stream.synchronize()
+                        if r >= 2:
+                            times.append(e0.elapsed_time(e1))
+                            bytes_.append(b)
+            ms = statistics.median(times)
+            b = statistics.mean(bytes_)
+            res[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
+                           "touched": [c[2] for c in calls],
+                           "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                           "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
+                           "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_gbs, 3)}
+            del calls, ws
+        out[name] = {"K": sh.K, "I": sh.I, "E": sh.E, "topk": sh.topk, "per_T": res}
+        del layers
+        torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     """Headline timing: each step is captured once as a CUDA graph (two graphs
@@ -450,26 +508,39 @@ def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
 
 
 def time_phases(wl, steps: int, warmup: int):
-    """Per-call kernel durations: events recorded by the library around the
-    decode kernel (one cooperative launch per call)."""
-    from mxfp4_mixture_experts_gb300 import moe
+    """Per-call kernel time: each layer's call is captured as its own CUDA
+    graph (one cooperative decode launch) and replayed alone, with CUDA events
+    on the replay stream; the layers rotate, so no call finds its weights in
+    L2 from the previous replay."""
     stream = torch.cuda.Stream()
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for l, ly in enumerate(wl.L):
+            wl.call(ly)
+    stream.synchronize()
+    for l, ly in enumerate(wl.L):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            wl.call(ly)
+        graphs[l] = g
     per_T = {T: [] for T in wl.tokens}
     launches = []          # (algorithmic bytes, ms) per launch
     with torch.cuda.stream(stream):
         for s in range(warmup + steps):
-            recs = []
-            for ly in wl.step_layers(s):
-                ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-                moe.set_phase_events(ev)
-                wl.call(ly)
-                recs.append((ly, ev))
-            moe.set_phase_events(None)
+            evs = []
+            for l in range(len(wl.L)):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graphs[l].replay()
+                e1.record(stream)
+                evs.append((l, e0, e1))
             stream.synchronize()
             if s < warmup:
                 continue
-            for ly, ev in recs:
-                ms = ev[0].elapsed_time(ev[1])
+            for l, e0, e1 in evs:
+                ly = wl.L[l]
+                ms = e0.elapsed_time(e1)
                 per_T[ly["T"]].append((ms, ly))
                 launches.append((wl.alg_bytes(ly), ms))
     return per_T, launches
@@ -581,9 +652,11 @@ def run_ours(args, dist: Dist):
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_oracle_sample(wl)
+    del wl
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        out["configs"] = measure_configs(dev, hbm)
     if not args.no_prefill:
-        del wl
-        torch.cuda.empty_cache()
         pf = run_prefill(args, dist, 10, 3, False)
         out["prefill"] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "config",
                                              "phase_ms", "gemm_tflops", "roofline", "e2e",
@@ -670,6 +743,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gptoss128", choices=["gptoss128", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="leave the other decode workload shapes out of the default line")
     ap.add_argument("--no-prefill", action="store_true",
                     help="leave the shorter prefill measurement out of the default line")
     ap.add_argument("--profile-case", default=None,

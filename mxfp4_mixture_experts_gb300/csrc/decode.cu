@@ -269,10 +269,12 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
 // latencies overlap. xo[u] is this lane's byte offset of block (8k + u) inside
 // a 128-byte column (row g, 128-byte swizzle); brow / scg / scg8 point at
 // block b0's activation chunk and scale bytes.
-template <bool FAST, int NBAT, int B0>
+// GLOB: lanes whose token row is not staged (bsrc != nullptr) read their bf16
+// chunks from global memory (all NBAT loads issued first) and convert them.
+template <bool FAST, bool GLOB, int NBAT, int B0>
 __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, const int (&xo)[8],
                                            const uint8_t* scg, const uint8_t* scg8,
-                                           const uint8_t* brow) {
+                                           const uint8_t* brow, const uint16_t* bsrc, float bmul) {
   uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
   uint4 bv[NBAT];
 #pragma unroll
@@ -282,7 +284,14 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
     w1[u] = *reinterpret_cast<const uint32_t*>(p + 8 * 128);
     s0[u] = scg[u];
     s1[u] = scg8[u];
-    bv[u] = *reinterpret_cast<const uint4*>(brow + u * 64);
+    if (GLOB && bsrc != nullptr)
+      bv[u] = ldcg16(bsrc + u * 32);
+    else
+      bv[u] = *reinterpret_cast<const uint4*>(brow + u * 64);
+  }
+  if (GLOB && bsrc != nullptr) {
+#pragma unroll
+    for (int u = 0; u < NBAT; ++u) bv[u] = bf16x8_to_f16x8(bv[u], bmul);
   }
 #pragma unroll
   for (int u = 0; u < NBAT; ++u) {
@@ -299,6 +308,72 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
     acc[2] = fmaf(d[2], f1, acc[2]);
     acc[3] = fmaf(d[3], f1, acc[3]);
   }
+}
+
+// As blocks_mma for an item with NG token groups (batches of NBAT blocks):
+// the A words and scales of the batch are loaded once, each group's
+// activation chunks per block (staged, or global with on-the-fly conversion).
+template <bool FAST, bool GLOB, int NG, int NBAT, int B0>
+__device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], const uint8_t* stg,
+                                                  const int (&xo)[8], const uint8_t* scg,
+                                                  const uint8_t* scg8, int bg, int t,
+                                                  const BRows& br) {
+  uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
+  uint4 bv[NBAT][NG];
+#pragma unroll
+  for (int u = 0; u < NBAT; ++u) {
+    const uint8_t* p = stg + ((B0 + u) >> 3) * kColBytes + xo[(B0 + u) & 7];
+    w0[u] = *reinterpret_cast<const uint32_t*>(p);
+    w1[u] = *reinterpret_cast<const uint32_t*>(p + 8 * 128);
+    s0[u] = scg[u];
+    s1[u] = scg8[u];
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      if (GLOB && br.src[gr] != nullptr)
+        bv[u][gr] = ldcg16(br.src[gr] + (bg + u) * 32 + t * 8);
+      else
+        bv[u][gr] = *reinterpret_cast<const uint4*>(br.row[gr] + (bg + u) * br.step[gr]);
+    }
+  }
+  if (GLOB) {
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr)
+      if (br.src[gr] != nullptr) {
+#pragma unroll
+        for (int u = 0; u < NBAT; ++u) bv[u][gr] = bf16x8_to_f16x8(bv[u][gr], br.mul[gr]);
+      }
+  }
+#pragma unroll
+  for (int u = 0; u < NBAT; ++u) {
+    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+    e2m1x8_to_f16x2(w0[u], a0, a1, a2, a3);
+    e2m1x8_to_f16x2(w1[u], c0, c1, c2, c3);
+    const float f0 = FAST ? e8m0_to_f32_normal(s0[u]) : e8m0_to_f32(s0[u]);
+    const float f1 = FAST ? e8m0_to_f32_normal(s1[u]) : e8m0_to_f32(s1[u]);
+#pragma unroll
+    for (int gr = 0; gr < NG; ++gr) {
+      float d[4];
+      mma_f16_16816_z(d, a0, c0, a1, c1, bv[u][gr].x, bv[u][gr].y);
+      mma_f16_16816(d, a2, c2, a3, c3, bv[u][gr].z, bv[u][gr].w);
+      acc[gr][0] = fmaf(d[0], f0, acc[gr][0]);
+      acc[gr][1] = fmaf(d[1], f0, acc[gr][1]);
+      acc[gr][2] = fmaf(d[2], f1, acc[gr][2]);
+      acc[gr][3] = fmaf(d[3], f1, acc[gr][3]);
+    }
+  }
+}
+
+// All 16 blocks of a full stage for NG token groups: batches of 4 blocks for
+// two groups, of 2 for three or four (register budget).
+template <bool FAST, bool GLOB, int NG, int B0 = 0>
+__device__ __forceinline__ void stage_groups(float (&acc)[kMaxGroups][4], const uint8_t* stg,
+                                             const int (&xo)[8], const uint8_t* sc_g,
+                                             const uint8_t* sc_g8, int bg, int t, const BRows& br) {
+  constexpr int NBAT = NG <= 2 ? 4 : 2;
+  blocks_mma_groups<FAST, GLOB, NG, NBAT, B0>(acc, stg, xo, sc_g + bg + B0, sc_g8 + bg + B0,
+                                              bg + B0, t, br);
+  if constexpr (B0 + NBAT < kChunkBlocks)
+    stage_groups<FAST, GLOB, NG, B0 + NBAT>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
 }
 
 // The item sequence of one consumer warp across both phases (items k =
@@ -422,22 +497,34 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     const uint8_t* stg = ring_w + slot * kStageBytes;
     const int nb = min(kChunkBlocks, v.nblk - c * kChunkBlocks);
     const int bg = c * kChunkBlocks;   // first block of the stage in the row
-    if (!GLOB && ng == 1 && nb == kChunkBlocks) {
-      blocks_mma<FAST, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, br.row[0] + bg * 64);
-      blocks_mma<FAST, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8,
-                             br.row[0] + (bg + 8) * 64);
-    } else if (!GLOB && ng == 1) {   // partial last stage: batches of 8, 4, then single blocks
+    // this lane's activation chunk of block bg: staged row (64 bytes a block)
+    // or bf16 row in global memory (32 values a block)
+    const uint8_t* brow0 = br.row[0] + bg * 64;
+    const uint16_t* bsrc0 = (GLOB && br.src[0] != nullptr) ? br.src[0] + bg * 32 + t * 8 : nullptr;
+    if (ng == 1 && nb == kChunkBlocks) {
+      blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0, br.mul[0]);
+      blocks_mma<FAST, GLOB, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8, brow0 + 8 * 64,
+                                   bsrc0 != nullptr ? bsrc0 + 8 * 32 : nullptr, br.mul[0]);
+    } else if (ng == 1) {   // partial last stage: a batch of 8, then single blocks
       int b = 0;
       if (nb >= 8) {
-        blocks_mma<FAST, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, br.row[0] + bg * 64);
+        blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0,
+                                     br.mul[0]);
         b = 8;
       }
       for (; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+    } else if (nb == kChunkBlocks && CW < 12) {   // (the 12-warp form has no registers to spare)
+      if (ng == 2)
+        stage_groups<FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+      else if (ng == 3)
+        stage_groups<FAST, GLOB, 3>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+      else
+        stage_groups<FAST, GLOB, 4>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
     } else if (nb == kChunkBlocks) {
 #pragma unroll 4
       for (int b = 0; b < kChunkBlocks; ++b)
-        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, c * kChunkBlocks + b, ng, br);
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
     } else {
       for (int b = 0; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, c * kChunkBlocks + b, ng, br);
@@ -693,15 +780,25 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       for (int gr = 0; gr < kMaxGroups; ++gr)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
+      // (the 12-warp form runs only when every route's row is staged)
+      constexpr bool kGlobPath = CW < 12;
+      if (!kGlobPath && glob) {
+        ok = false;
+        fail |= 256;
+        break;
+      }
       if (!special && !glob)
-        ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
-                                      n1, n2, eb, cw);
+        ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
+                                          v1, v2, n1, n2, eb, cw);
+      else if (special && !glob)
+        ok = item_stages<CW, false, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
+                                           v1, v2, n1, n2, eb, cw);
       else if (!special)
-        ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
-                                     n1, n2, eb, cw);
+        ok = item_stages<CW, true, kGlobPath>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+                                              P, v1, v2, n1, n2, eb, cw);
       else
-        ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P, v1, v2,
-                                      n1, n2, eb, cw);
+        ok = item_stages<CW, false, kGlobPath>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+                                               P, v1, v2, n1, n2, eb, cw);
       if (!ok) {
         fail |= 16;
         break;
@@ -802,12 +899,13 @@ size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-// Warps per CTA: 12 when their rings, scale slots and a few staged rows fit,
-// else 8 (large K); 0 when even 8 do not fit.
+// Warps per CTA: 12 (3-deep rings) when their rings, scale slots and a
+// staged row for every route fit, else 8 (4-deep rings, more room for rows:
+// rows that are not staged are read from global memory, more slowly); 0 when
+// even 8 do not fit.
 int decode_warps(int K, int I, int E, int R, int max_smem) {
   const int stride = decode_row_stride(K, I);
-  const size_t rows4 = (size_t)(R < 4 ? R : 4) * stride;
-  if (decode_smem_bytes(12, K, I, E, R, 0, stride) + rows4 <= (size_t)max_smem) return 12;
+  if (decode_smem_bytes(12, K, I, E, R, R, stride) <= (size_t)max_smem) return 12;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
