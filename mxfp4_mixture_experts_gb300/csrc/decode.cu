@@ -39,6 +39,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "route.cuh"
 #include "kernels.h"
 
@@ -96,12 +97,6 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int cw, int K, int I, int
   return m;
 }
 
-// Balanced split of U units over n CTAs (the first U % n CTAs get one more).
-__device__ __forceinline__ int range_begin(int v, int U, int n) {
-  const int q = U / n, rem = U % n;
-  return v * q + (v < rem ? v : rem);
-}
-
 // Items a warp owns among n items dealt round-robin to CW warps.
 template <int CW>
 __device__ __forceinline__ int warp_items(int w, int n) { return n / CW + (w < n % CW ? 1 : 0); }
@@ -121,31 +116,6 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float mul) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(o[i]) : "f"(hi), "f"(lo));
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const int* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Order this thread's generic global writes before later async-proxy (bulk
-// copy) reads of them by any CTA.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Bounded wait until the grid counter reaches target; false when it gave up.
-__device__ __forceinline__ bool grid_wait(const int* ctr, uint32_t target) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (ld_acquire_gpu(ctr) >= target) return true;
-    __nanosleep(64);
-  }
-  return false;
 }
 
 // An item's routes: expert e, route-list positions q0 .. q0 + cnt - 1 (a batch
@@ -843,34 +813,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     ok = false;
     fail |= 32;
   } else {
-    const int per_row = a.K / 8;
-    const int total = a.T * per_row;
-    const int c0 = range_begin(blockIdx.x, total, nCta);
-    const int c1 = range_begin(blockIdx.x + 1, total, nCta);
-    for (int i = c0 + ctid; i < c1; i += kThreadsCW) {
-      const int tt = i / per_row, m8 = (i - tt * per_row) * 8;
-      float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < a.topk; ++j) {
-        const int r = tt * a.topk + j;
-        const int e = a.ids[r];
-        if (e < 0 || e >= E) continue;
-        const uint4 lo = ldcg16(a.P + (size_t)r * a.K + m8);
-        const uint4 hi = ldcg16(a.P + (size_t)r * a.K + m8 + 4);
-        sum[0] += __uint_as_float(lo.x);
-        sum[1] += __uint_as_float(lo.y);
-        sum[2] += __uint_as_float(lo.z);
-        sum[3] += __uint_as_float(lo.w);
-        sum[4] += __uint_as_float(hi.x);
-        sum[5] += __uint_as_float(hi.y);
-        sum[6] += __uint_as_float(hi.z);
-        sum[7] += __uint_as_float(hi.w);
-      }
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(sum[2 * q + 1]), "f"(sum[2 * q]));
-      *reinterpret_cast<uint4*>(a.y + (size_t)tt * a.K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+    combine_share(a, blockIdx.x, nCta, ctid, kThreadsCW);
   }
   // the last CTA out leaves the grid counters at zero for the next call
   named_barrier(kBarConsumers, kThreadsCW);

@@ -1,0 +1,82 @@
+// Pieces shared by the two decode kernels (tensor-core decode_tc.cu and the
+// CUDA-core decode.cu): the balanced split of work over CTAs, the grid-wide
+// counters of the cooperative launch, and the slot-order combine.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mxmoe {
+
+// Balanced split of U units over n CTAs (the first U % n CTAs get one more).
+__device__ __forceinline__ int range_begin(int v, int U, int n) {
+  const int q = U / n, rem = U % n;
+  return v * q + (v < rem ? v : rem);
+}
+// The CTA whose range_begin range holds unit u (0 <= u < U).
+__device__ __forceinline__ int range_owner(int u, int U, int n) {
+  const int q = U / n, rem = U % n;
+  const int big = rem * (q + 1);
+  return u < big ? u / (q + 1) : rem + (u - big) / q;
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const int* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Order this thread's generic global writes before later async-proxy (bulk
+// copy) reads of them by any CTA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until the grid counter reaches target; false when it gave up.
+__device__ __forceinline__ bool grid_wait(const int* ctr, uint32_t target) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+// y [T, K] = bf16 of the slot-order (j = 0 .. topk-1) fp32 sum of the
+// weighted route outputs P [R, K] of each token's valid routes ("MXFP4 MoE
+// decode kernels", Design, "Fused epilogues": the weighted top-k sum). This
+// CTA writes an equal contiguous share of the 8-column groups; threads
+// tid0, tid0 + nthr, ... of the CTA take part.
+__device__ __forceinline__ void combine_share(const DecodeArgs& a, int cta, int nCta, int tid0,
+                                              int nthr) {
+  const int per_row = a.K / 8;
+  const int total = a.T * per_row;
+  const int c0 = range_begin(cta, total, nCta);
+  const int c1 = range_begin(cta + 1, total, nCta);
+  for (int i = c0 + tid0; i < c1; i += nthr) {
+    const int tt = i / per_row, m8 = (i - tt * per_row) * 8;
+    float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < a.topk; ++j) {
+      const int r = tt * a.topk + j;
+      const int e = a.ids[r];
+      if (e < 0 || e >= a.E) continue;
+      const uint4 lo = ldcg16(a.P + (size_t)r * a.K + m8);
+      const uint4 hi = ldcg16(a.P + (size_t)r * a.K + m8 + 4);
+      sum[0] += __uint_as_float(lo.x);
+      sum[1] += __uint_as_float(lo.y);
+      sum[2] += __uint_as_float(lo.z);
+      sum[3] += __uint_as_float(lo.w);
+      sum[4] += __uint_as_float(hi.x);
+      sum[5] += __uint_as_float(hi.y);
+      sum[6] += __uint_as_float(hi.z);
+      sum[7] += __uint_as_float(hi.w);
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(sum[2 * q + 1]), "f"(sum[2 * q]));
+    *reinterpret_cast<uint4*>(a.y + (size_t)tt * a.K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+}  // namespace mxmoe

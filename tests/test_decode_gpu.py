@@ -205,3 +205,23 @@ def test_full_size_sampled_tokens(moe, full_weights, name, T):
     assert int(status[1]) == len(rt["touched"]) and int(status[0]) == 0
     tokens = sorted({0, T - 1})
     assert_close(y, case, tokens)
+
+
+def test_wide_activation_range_in_every_block(moe):
+    """Hidden values spread over 2^-24 .. 2^24 inside every 32-value block (the
+    per-row power-of-two prescale to f16 keeps every element within 2^-31 of
+    the row maximum exact)."""
+    shape = synth.custom_shape(K=1024, I=256, E=8, topk=2)
+    case = synth.make_case(shape, 6, seed=30)
+    gen = torch.Generator().manual_seed(9)
+    mag = torch.pow(2.0, torch.randint(-24, 25, case.hidden.shape, generator=gen).float())
+    case.hidden = (case.hidden.float() * mag).to(torch.bfloat16)
+    assert_close(run(moe, case), case)
+
+
+def test_one_token_one_expert_full_width(moe):
+    """One token on one expert with K = I = 2880: the smallest real decode
+    call, every CTA's items belong to the same expert."""
+    shape = synth.custom_shape(K=2880, I=2880, E=4, topk=1)
+    case = synth.make_case(shape, 1, seed=31)
+    assert_close(run(moe, case), case)
