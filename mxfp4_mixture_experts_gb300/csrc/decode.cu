@@ -471,7 +471,10 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     // or bf16 row in global memory (32 values a block)
     const uint8_t* brow0 = br.row[0] + bg * 64;
     const uint16_t* bsrc0 = (GLOB && br.src[0] != nullptr) ? br.src[0] + bg * 32 + t * 8 : nullptr;
-    if (ng == 1 && nb == kChunkBlocks) {
+    if (GLOB && CW >= 12) {   // rows read from global memory: one block at a time (registers)
+      for (int b = 0; b < nb; ++b)
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+    } else if (ng == 1 && nb == kChunkBlocks) {
       blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0, br.mul[0]);
       blocks_mma<FAST, GLOB, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8, brow0 + 8 * 64,
                                    bsrc0 != nullptr ? bsrc0 + 8 * 32 : nullptr, br.mul[0]);
@@ -750,13 +753,6 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       for (int gr = 0; gr < kMaxGroups; ++gr)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
-      // (the 12-warp form runs only when every route's row is staged)
-      constexpr bool kGlobPath = CW < 12;
-      if (!kGlobPath && glob) {
-        ok = false;
-        fail |= 256;
-        break;
-      }
       if (!special && !glob)
         ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
                                           v1, v2, n1, n2, eb, cw);
@@ -764,10 +760,10 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
         ok = item_stages<CW, false, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
                                            v1, v2, n1, n2, eb, cw);
       else if (!special)
-        ok = item_stages<CW, true, kGlobPath>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+        ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
                                               P, v1, v2, n1, n2, eb, cw);
       else
-        ok = item_stages<CW, false, kGlobPath>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+        ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
                                                P, v1, v2, n1, n2, eb, cw);
       if (!ok) {
         fail |= 16;
@@ -842,13 +838,21 @@ size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-// Warps per CTA: 12 (3-deep rings) when their rings, scale slots and a
-// staged row for every route fit, else 8 (4-deep rings, more room for rows:
-// rows that are not staged are read from global memory, more slowly); 0 when
-// even 8 do not fit.
+// Warps per CTA: 12 (3-deep rings; 50% more warps to hide the latency of the
+// conversion and MMA chain) when their rings, scale slots and the activation
+// rows a CTA is expected to need all fit, else 8 (4-deep rings, room for more
+// rows); 0 when even 8 do not fit. A CTA's items span one or two expert
+// batches, so it needs the rows of those experts' routes; with R routes over E
+// experts the expected routes per touched expert is rho = R / (E (1 - (1 -
+// 1/E)^R)), and 3 rho + 3 rows covered the largest need of every CTA on the
+// workload shapes. Rows beyond the staged ones are read from global memory
+// (correct for any routing, only slower).
 int decode_warps(int K, int I, int E, int R, int max_smem) {
   const int stride = decode_row_stride(K, I);
-  if (decode_smem_bytes(12, K, I, E, R, R, stride) <= (size_t)max_smem) return 12;
+  const double rho = (double)R / ((double)E * (1.0 - pow(1.0 - 1.0 / E, (double)R)));
+  int want = (int)ceil(3.0 * rho + 3.0);
+  if (want > R) want = R;
+  if (decode_smem_bytes(12, K, I, E, R, want, stride) <= (size_t)max_smem) return 12;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
