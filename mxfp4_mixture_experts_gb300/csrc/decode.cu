@@ -14,27 +14,30 @@
 //   combine:       y [T, K] = bf16 of the slot-order sum of each token's route
 //                  outputs.
 //
-// CTA = 1 control warp + 8 consumer warps, one CTA per SM.
+// One CTA per SM; every warp is a consumer: 12 or 10 warps with 3-deep rings
+// when the activation rows a CTA is expected to need fit in shared memory
+// next to the rings, else 8 warps with 4-deep rings (decode_warps).
 //  * Work item = 16 weight rows of one touched expert over the whole
 //    reduction (phase 1: gate rows i0..i0+7 and the matching up rows; phase 2:
-//    16 w2 rows). A phase's items are split into equal contiguous ranges, one
-//    per CTA, and a CTA's items are dealt round-robin to its consumer warps:
-//    a warp owns whole items, so no partial sums cross warps or CTAs, and the
-//    SwiGLU of a gate/up pair happens in the thread that holds both.
-//  * Each consumer warp streams its own items: lane 0 keeps 3 stages of 16
-//    rows x 256 bytes in flight in the warp's 4-stage ring (2-D TMA, 128-byte
+//    16 w2 rows) times up to 32 of the expert's routes. A phase's items are
+//    split into equal contiguous ranges, one per CTA, and a CTA's items are
+//    dealt round-robin to its warps: a warp owns whole items, so no partial
+//    sums cross warps or CTAs, and the SwiGLU of a gate/up pair happens in the
+//    thread that holds both.
+//  * Each warp streams its own items: lane 0 keeps the next stages of 16 rows
+//    x 256 bytes in flight in the warp's private ring (2-D TMA, 128-byte
 //    swizzle), running on into its phase-2 items before h exists, and
 //    bulk-copies each item's E8M0 rows into one of the warp's two scale slots.
-//    Spreading the issue over 8 warps keeps enough bytes in flight per SM.
+//    Spreading the issue over all warps keeps enough bytes in flight per SM.
 //  * Consumers decode E2M1 with the hardware e2m1x2 -> f16x2 conversion
 //    (exact), run one m16n8k16 f16 MMA pair per 32-value block into a fresh
 //    fp32 fragment and fold it into the accumulator with one FFMA by
 //    2^(s-127) (exact for every scale byte, 0 and 255 included).
 //  * Activations (hidden rows for phase 1, h rows for phase 2) are staged in
-//    shared memory by the control warp and converted to f16 after an exact
-//    power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
+//    shared memory by thread 0 (bulk copies) and converted to f16 after an
+//    exact power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
 //    epilogue multiplies it back. Rows that do not fit are read from global
-//    memory and converted on the fly. The control warp waits for the grid
+//    memory and converted on the fly. Thread 0 also waits for the grid
 //    between the phases.
 #include <cuda.h>
 
@@ -45,8 +48,8 @@
 
 namespace mxmoe {
 
-// stages in each warp's ring: 4 with 8 warps, 3 with 12 (shared memory)
-__host__ __device__ constexpr int ring_depth(int cw) { return cw >= 12 ? 3 : 4; }
+// stages in each warp's ring: 4 with 8 warps, 3 with 10 or 12 (shared memory)
+__host__ __device__ constexpr int ring_depth(int cw) { return cw >= 10 ? 3 : 4; }
 constexpr int kRows = 16;                    // weight rows per item (one m16 tile)
 constexpr int kChunk = 256;                  // packed bytes per row per stage
 constexpr int kChunkBlocks = kChunk / 16;    // 16 scale blocks per stage
@@ -471,7 +474,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     // or bf16 row in global memory (32 values a block)
     const uint8_t* brow0 = br.row[0] + bg * 64;
     const uint16_t* bsrc0 = (GLOB && br.src[0] != nullptr) ? br.src[0] + bg * 32 + t * 8 : nullptr;
-    if (GLOB && CW >= 12) {   // rows read from global memory: one block at a time (registers)
+    if (GLOB && CW >= 10) {   // rows read from global memory: one block at a time (registers)
       for (int b = 0; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
     } else if (ng == 1 && nb == kChunkBlocks) {
@@ -487,7 +490,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
       }
       for (; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
-    } else if (nb == kChunkBlocks && CW < 12) {   // (the 12-warp form has no registers to spare)
+    } else if (nb == kChunkBlocks && CW < 10) {   // (the 10- and 12-warp forms have no registers to spare)
       if (ng == 2)
         stage_groups<FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
       else if (ng == 3)
@@ -838,21 +841,24 @@ size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-// Warps per CTA: 12 (3-deep rings; 50% more warps to hide the latency of the
-// conversion and MMA chain) when their rings, scale slots and the activation
-// rows a CTA is expected to need all fit, else 8 (4-deep rings, room for more
-// rows); 0 when even 8 do not fit. A CTA's items span one or two expert
-// batches, so it needs the rows of those experts' routes; with R routes over E
-// experts the expected routes per touched expert is rho = R / (E (1 - (1 -
-// 1/E)^R)), and 3 rho + 3 rows covered the largest need of every CTA on the
-// workload shapes. Rows beyond the staged ones are read from global memory
-// (correct for any routing, only slower).
+// Warps per CTA: the most of 12 or 10 (3-deep rings; more warps hide more of
+// the latency of the conversion and MMA chain) whose rings, scale slots and
+// the activation rows a CTA is expected to need all fit, else 8 (4-deep rings
+// and the batched paths for rows read from global memory and for items with
+// several token groups, the better choice when rows overflow); 0 when even 8
+// do not fit. A CTA's items span one or two expert batches, so it needs the
+// rows of those experts' routes; with R routes over E experts the expected
+// routes per touched expert is rho = R / (E (1 - (1 - 1/E)^R)), and 3 rho + 3
+// rows covered the largest need of every CTA on the workload shapes. Rows
+// beyond the staged ones are read from global memory (correct for any
+// routing, only slower).
 int decode_warps(int K, int I, int E, int R, int max_smem) {
   const int stride = decode_row_stride(K, I);
   const double rho = (double)R / ((double)E * (1.0 - pow(1.0 - 1.0 / E, (double)R)));
   int want = (int)ceil(3.0 * rho + 3.0);
   if (want > R) want = R;
   if (decode_smem_bytes(12, K, I, E, R, want, stride) <= (size_t)max_smem) return 12;
+  if (decode_smem_bytes(10, K, I, E, R, want, stride) <= (size_t)max_smem) return 10;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
@@ -904,7 +910,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const C
   p.xs_rows_cap = (int)rows;
   p.stages = ring_depth(cw);
   const size_t smem = decode_smem_bytes(cw, a.K, a.I, a.E, R, (int)rows, p.xs_stride);
-  return cw == 12 ? launch_cw<12>(p, smem, num_sms, stream) : launch_cw<8>(p, smem, num_sms, stream);
+  if (cw == 12) return launch_cw<12>(p, smem, num_sms, stream);
+  if (cw == 10) return launch_cw<10>(p, smem, num_sms, stream);
+  return launch_cw<8>(p, smem, num_sms, stream);
 }
 
 }  // namespace mxmoe
