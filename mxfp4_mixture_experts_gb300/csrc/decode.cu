@@ -14,7 +14,7 @@
 //   combine:       y [T, K] = bf16 of the slot-order sum of each token's route
 //                  outputs.
 //
-// One CTA per SM; every warp is a consumer: 12 or 10 warps with 3-deep rings
+// One CTA per SM; every warp is a consumer: 10 to 12 warps with 3-deep rings
 // when the activation rows a CTA is expected to need fit in shared memory
 // next to the rings, else 8 warps with 4-deep rings (decode_warps).
 //  * Work item = 16 weight rows of one touched expert over the whole
@@ -48,7 +48,7 @@
 
 namespace mxmoe {
 
-// stages in each warp's ring: 4 with 8 warps, 3 with 10 or 12 (shared memory)
+// stages in each warp's ring: 4 with 8 warps, 3 with 10 to 12 (shared memory)
 __host__ __device__ constexpr int ring_depth(int cw) { return cw >= 10 ? 3 : 4; }
 constexpr int kRows = 16;                    // weight rows per item (one m16 tile)
 constexpr int kChunk = 256;                  // packed bytes per row per stage
@@ -490,7 +490,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
       }
       for (; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
-    } else if (nb == kChunkBlocks && CW < 10) {   // (the 10- and 12-warp forms have no registers to spare)
+    } else if (nb == kChunkBlocks && CW < 10) {   // (the 10- to 12-warp forms have no registers to spare)
       if (ng == 2)
         stage_groups<FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
       else if (ng == 3)
@@ -841,7 +841,7 @@ size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-// Warps per CTA: the most of 12 or 10 (3-deep rings; more warps hide more of
+// Warps per CTA: the most of 12, 11 or 10 (3-deep rings; more warps hide more of
 // the latency of the conversion and MMA chain) whose rings, scale slots and
 // the activation rows a CTA is expected to need all fit, else 8 (4-deep rings
 // and the batched paths for rows read from global memory and for items with
@@ -857,8 +857,8 @@ int decode_warps(int K, int I, int E, int R, int max_smem) {
   const double rho = (double)R / ((double)E * (1.0 - pow(1.0 - 1.0 / E, (double)R)));
   int want = (int)ceil(3.0 * rho + 3.0);
   if (want > R) want = R;
-  if (decode_smem_bytes(12, K, I, E, R, want, stride) <= (size_t)max_smem) return 12;
-  if (decode_smem_bytes(10, K, I, E, R, want, stride) <= (size_t)max_smem) return 10;
+  for (int cw = 12; cw >= 10; --cw)
+    if (decode_smem_bytes(cw, K, I, E, R, want, stride) <= (size_t)max_smem) return cw;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
@@ -911,6 +911,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const C
   p.stages = ring_depth(cw);
   const size_t smem = decode_smem_bytes(cw, a.K, a.I, a.E, R, (int)rows, p.xs_stride);
   if (cw == 12) return launch_cw<12>(p, smem, num_sms, stream);
+  if (cw == 11) return launch_cw<11>(p, smem, num_sms, stream);
   if (cw == 10) return launch_cw<10>(p, smem, num_sms, stream);
   return launch_cw<8>(p, smem, num_sms, stream);
 }
