@@ -104,7 +104,7 @@ Layout layout(int T, int K, int I, int E, int topk) {
   L.roffset = take((size_t)(E + 1) * sizeof(int));
   L.rlist = take(R * sizeof(int));
   L.rinv = take(R * sizeof(int));
-  L.xp = take(R * K * 2);
+  L.xp = take(R * (size_t)(K > I ? K : I) * 2);   // (decode: the f16 row scratch)
   L.total = o;
   return L;
 }
@@ -175,7 +175,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   if (!decode && (K % 64 || I % 64)) return MXFP4_MOE_ERR_SHAPE;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
-  if (decode && !decode_fits(K, I, E, T * topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
+  if (decode && !decode_fits(K, I, E, T, topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
 
@@ -194,6 +194,7 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     a.E = E;
     a.topk = topk;
     a.h = reinterpret_cast<uint16_t*>(ws + L.h);
+    a.xf = reinterpret_cast<uint16_t*>(ws + L.xp);
     a.P = reinterpret_cast<float*>(ws + L.P);
     a.y = static_cast<uint16_t*>(out);
     a.gbar = reinterpret_cast<int*>(ws + L.gbar);

@@ -192,12 +192,12 @@ __device__ __forceinline__ RowPlan row_plan(const PhaseView& v, int xs_rows_cap)
 
 // B operand of one token group for this lane (token column g): a staged f16
 // row (advanced 64 bytes per block; 0 for padding columns, which read a zero
-// chunk), or a bf16 row in global memory converted on the fly.
+// chunk), or an f16 row of the scratch in global memory (rows with no room in
+// shared memory, converted once with the same prescale).
 struct BRows {
   const uint8_t* row[kMaxGroups];
   int step[kMaxGroups];
   const uint16_t* src[kMaxGroups];
-  float mul[kMaxGroups];
 };
 
 // One 32-value block of one item for one warp: both m16 rows' 4-byte words,
@@ -221,7 +221,7 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
     // B: token column g of the group, physical k = 32 bglob + 8t .. +7 (f16)
     uint4 bv;
     if (GLOB && br.src[gr] != nullptr)
-      bv = bf16x8_to_f16x8(ldcg16(br.src[gr] + bglob * 32 + t * 8), br.mul[gr]);
+      bv = ldcg16(br.src[gr] + bglob * 32 + t * 8);
     else
       bv = *reinterpret_cast<const uint4*>(br.row[gr] + bglob * br.step[gr]);
     float d[4];
@@ -242,12 +242,12 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
 // latencies overlap. xo[u] is this lane's byte offset of block (8k + u) inside
 // a 128-byte column (row g, 128-byte swizzle); brow / scg / scg8 point at
 // block b0's activation chunk and scale bytes.
-// GLOB: lanes whose token row is not staged (bsrc != nullptr) read their bf16
-// chunks from global memory (all NBAT loads issued first) and convert them.
+// GLOB: lanes whose token row is not staged (bsrc != nullptr) read their f16
+// chunks from the scratch in global memory (all NBAT loads issued first).
 template <bool FAST, bool GLOB, int NBAT, int B0>
 __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, const int (&xo)[8],
                                            const uint8_t* scg, const uint8_t* scg8,
-                                           const uint8_t* brow, const uint16_t* bsrc, float bmul) {
+                                           const uint8_t* brow, const uint16_t* bsrc) {
   uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
   uint4 bv[NBAT];
 #pragma unroll
@@ -261,10 +261,6 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
       bv[u] = ldcg16(bsrc + u * 32);
     else
       bv[u] = *reinterpret_cast<const uint4*>(brow + u * 64);
-  }
-  if (GLOB && bsrc != nullptr) {
-#pragma unroll
-    for (int u = 0; u < NBAT; ++u) bv[u] = bf16x8_to_f16x8(bv[u], bmul);
   }
 #pragma unroll
   for (int u = 0; u < NBAT; ++u) {
@@ -308,14 +304,6 @@ __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], c
         bv[u][gr] = *reinterpret_cast<const uint4*>(br.row[gr] + (bg + u) * br.step[gr]);
     }
   }
-  if (GLOB) {
-#pragma unroll
-    for (int gr = 0; gr < NG; ++gr)
-      if (br.src[gr] != nullptr) {
-#pragma unroll
-        for (int u = 0; u < NBAT; ++u) bv[u][gr] = bf16x8_to_f16x8(bv[u][gr], br.mul[gr]);
-      }
-  }
 #pragma unroll
   for (int u = 0; u < NBAT; ++u) {
     uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
@@ -338,7 +326,7 @@ __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], c
 
 // All 16 blocks of a full stage for NG token groups: batches of 4 blocks for
 // two groups, of 2 for three or four (register budget).
-template <bool FAST, bool GLOB, int NG, int B0 = 0>
+template <int CW, bool FAST, bool GLOB, int NG, int B0 = 0>
 __device__ __forceinline__ void stage_groups(float (&acc)[kMaxGroups][4], const uint8_t* stg,
                                              const int (&xo)[8], const uint8_t* sc_g,
                                              const uint8_t* sc_g8, int bg, int t, const BRows& br) {
@@ -346,7 +334,7 @@ __device__ __forceinline__ void stage_groups(float (&acc)[kMaxGroups][4], const 
   blocks_mma_groups<FAST, GLOB, NG, NBAT, B0>(acc, stg, xo, sc_g + bg + B0, sc_g8 + bg + B0,
                                               bg + B0, t, br);
   if constexpr (B0 + NBAT < kChunkBlocks)
-    stage_groups<FAST, GLOB, NG, B0 + NBAT>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+    stage_groups<CW, FAST, GLOB, NG, B0 + NBAT>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
 }
 
 // The item sequence of one consumer warp across both phases (items k =
@@ -474,29 +462,28 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     // or bf16 row in global memory (32 values a block)
     const uint8_t* brow0 = br.row[0] + bg * 64;
     const uint16_t* bsrc0 = (GLOB && br.src[0] != nullptr) ? br.src[0] + bg * 32 + t * 8 : nullptr;
-    if (GLOB && CW >= 10) {   // rows read from global memory: one block at a time (registers)
+    if (GLOB && CW >= 11) {   // rows read from global memory: one block at a time (registers)
       for (int b = 0; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
     } else if (ng == 1 && nb == kChunkBlocks) {
-      blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0, br.mul[0]);
+      blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0);
       blocks_mma<FAST, GLOB, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8, brow0 + 8 * 64,
-                                   bsrc0 != nullptr ? bsrc0 + 8 * 32 : nullptr, br.mul[0]);
+                                   bsrc0 != nullptr ? bsrc0 + 8 * 32 : nullptr);
     } else if (ng == 1) {   // partial last stage: a batch of 8, then single blocks
       int b = 0;
       if (nb >= 8) {
-        blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0,
-                                     br.mul[0]);
+        blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0);
         b = 8;
       }
       for (; b < nb; ++b)
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
     } else if (nb == kChunkBlocks && CW < 10) {   // (the 10- to 12-warp forms have no registers to spare)
       if (ng == 2)
-        stage_groups<FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
       else if (ng == 3)
-        stage_groups<FAST, GLOB, 3>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 3>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
       else
-        stage_groups<FAST, GLOB, 4>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 4>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
     } else if (nb == kChunkBlocks) {
 #pragma unroll 4
       for (int b = 0; b < kChunkBlocks; ++b)
@@ -558,6 +545,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   int* eb = reinterpret_cast<int*>(smem + M.eb);                  // [nEB] (expert << 8) | batch
   uint8_t* xs = smem + M.xs;
   const int xs_stride = P.xs_stride;
+  const size_t xf_stride = (size_t)(a.K > a.I ? a.K : a.I);   // f16 scratch row, elements
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -686,9 +674,12 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
       const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
       if (lane == 0) row_sh[r] = sh;
+      const float mul = pow2f(-sh);
       if (staged) {
-        const float mul = pow2f(-sh);
         for (int c16 = lane; c16 < v.kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
+      } else {   // rows with no room here: converted once into the f16 scratch
+        uint4* dst = reinterpret_cast<uint4*>(a.xf + (size_t)(v.p_lo + r) * xf_stride);
+        for (int c16 = lane; c16 < v.kred / 8; c16 += 32) dst[c16] = bf16x8_to_f16x8(ldcg16(src + c16), mul);
       }
     }
     named_barrier(kBarConsumers, kThreadsCW);
@@ -737,15 +728,13 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
         br.row[gr] = first_staged ? xs + (size_t)q_first * xs_stride + t * 16 : zero16;
         br.step[gr] = first_staged ? 64 : 0;
         br.src[gr] = nullptr;
-        br.mul[gr] = 1.f;
         if (gr < ng && gr * kGroup + g < cnt) {
           const int q = ir.q0 + gr * kGroup + g - v.p_lo;
           if (q < rp.xs_rows) {
             br.row[gr] = xs + (size_t)q * xs_stride + t * 16;
             br.step[gr] = 64;
           } else {
-            br.src[gr] = act_row(phase, a, tb, v.p_lo + q);
-            br.mul[gr] = pow2f(-row_sh[q]);
+            br.src[gr] = a.xf + (size_t)(v.p_lo + q) * xf_stride;
             glob = true;
           }
         }
@@ -841,30 +830,50 @@ size_t decode_smem_bytes(int cw, int K, int I, int E, int R, int xs_rows, int xs
 
 int decode_row_stride(int K, int I) { return (int)round_up((size_t)(K > I ? K : I) * 2, 128) + 64; }
 
-// Warps per CTA: the most of 12, 11 or 10 (3-deep rings; more warps hide more of
-// the latency of the conversion and MMA chain) whose rings, scale slots and
-// the activation rows a CTA is expected to need all fit, else 8 (4-deep rings
-// and the batched paths for rows read from global memory and for items with
-// several token groups, the better choice when rows overflow); 0 when even 8
-// do not fit. A CTA's items span one or two expert batches, so it needs the
-// rows of those experts' routes; with R routes over E experts the expected
-// routes per touched expert is rho = R / (E (1 - (1 - 1/E)^R)), and 3 rho + 3
-// rows covered the largest need of every CTA on the workload shapes. Rows
-// beyond the staged ones are read from global memory (correct for any
-// routing, only slower).
-int decode_warps(int K, int I, int E, int R, int max_smem) {
+// The smallest m with P(max over E experts of routes per expert <= m) >= 0.99
+// when each of T tokens names an expert with probability topk / E
+// (binomial counts, independent across experts).
+static int routes_per_expert_p99(int T, int topk, int E) {
+  const double p = (double)topk / E;
+  double cdf = 0.0, pmf = pow(1.0 - p, (double)T);   // P(X = 0)
+  for (int m = 0; m <= T; ++m) {
+    cdf += pmf;
+    if (pow(cdf > 1.0 ? 1.0 : cdf, (double)E) >= 0.99) return m;
+    pmf *= (double)(T - m) / (m + 1) * p / (1.0 - p);
+  }
+  return T;
+}
+
+// Warps per CTA: the most of 12, 11 or 10 (3-deep rings; more warps hide more
+// of the latency of the conversion and MMA chain) whose rings, scale slots and
+// the activation rows a CTA is expected to need all fit. A CTA's items span
+// one or two expert batches, so it needs the rows of those experts' routes:
+// at most 2 m99 (m99 from routes_per_expert_p99), and 3 rho + 3 covered the
+// largest need of every CTA on the workload shapes (rho = R / (E (1 - (1 -
+// 1/E)^R)), the expected routes per touched expert). When those rows do not
+// fit next to any of them: 10 warps anyway (its batched reads of the f16
+// scratch) if experts with more than 8 routes are unlikely (m99 <= 5; their
+// items would take the per-block path of that form), else 8 warps (4-deep rings, batched paths for rows read from
+// the f16 scratch and for items with several token groups). 0 when even 8
+// warps do not fit. Rows beyond the staged ones are read from the f16 scratch
+// in global memory (correct for any routing, only slower).
+int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
+  const int R = T * topk;
   const int stride = decode_row_stride(K, I);
   const double rho = (double)R / ((double)E * (1.0 - pow(1.0 - 1.0 / E, (double)R)));
+  const int m99 = routes_per_expert_p99(T, topk, E);
   int want = (int)ceil(3.0 * rho + 3.0);
+  if (want > 2 * m99) want = 2 * m99;
   if (want > R) want = R;
   for (int cw = 12; cw >= 10; --cw)
     if (decode_smem_bytes(cw, K, I, E, R, want, stride) <= (size_t)max_smem) return cw;
+  if (m99 <= 5 && decode_smem_bytes(10, K, I, E, R, 1, stride) <= (size_t)max_smem) return 10;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
 
-bool decode_fits(int K, int I, int E, int R, int max_smem) {
-  return decode_warps(K, I, E, R, max_smem) != 0;
+bool decode_fits(int K, int I, int E, int T, int topk, int max_smem) {
+  return decode_warps(K, I, E, T, topk, max_smem) != 0;
 }
 
 template <int CW>
@@ -901,7 +910,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const C
   p.tmap2 = tmap2;
   p.a = a;
   const int R = a.T * a.topk;
-  const int cw = decode_warps(a.K, a.I, a.E, R, max_smem);
+  const int cw = decode_warps(a.K, a.I, a.E, a.T, a.topk, max_smem);
   if (cw == 0) return cudaErrorInvalidValue;
   p.xs_stride = decode_row_stride(a.K, a.I);
   const size_t fixed = decode_smem_bytes(cw, a.K, a.I, a.E, R, 0, p.xs_stride);

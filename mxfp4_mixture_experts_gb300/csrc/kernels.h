@@ -16,6 +16,8 @@ struct DecodeArgs {
   const uint8_t *w13, *s13, *w2, *s2;
   int T, K, I, E, topk;
   uint16_t* h;            // bf16 [R, I] (SwiGLU output)
+  uint16_t* xf;           // f16 [R, max(K, I)]: prescaled activation rows that have no
+                          // room in shared memory, by route-list position
   float* P;               // weighted route outputs, fp32 [R, K]
   uint16_t* y;            // bf16 [T, K]
   int* gbar;              // [2] grid-barrier counters, zero between calls
@@ -34,7 +36,7 @@ struct DecodeParams {
 };
 
 // Whether the decode kernel's shared-memory plan fits for these sizes.
-bool decode_fits(int K, int I, int E, int R, int max_smem);
+bool decode_fits(int K, int I, int E, int T, int topk, int max_smem);
 
 // One cooperative launch (one CTA per SM, all resident) per decode call.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
