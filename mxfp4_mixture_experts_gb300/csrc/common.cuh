@@ -44,6 +44,14 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
 }
 
 // 16-byte load that skips L1, for data other SMs wrote during this kernel.
+// 16 bytes through a generic address (shared or global memory), not cached in
+// L1 when global.
+__device__ __forceinline__ uint4 ld_cg_generic16(const void* p) {
+  uint4 v;
+  asm volatile("ld.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ uint4 ldcg16(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -36,8 +36,9 @@
 //  * Activations (hidden rows for phase 1, h rows for phase 2) are staged in
 //    shared memory by thread 0 (bulk copies) and converted to f16 after an
 //    exact power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
-//    epilogue multiplies it back. Rows that do not fit are read from global
-//    memory and converted on the fly. Thread 0 also waits for the grid
+//    epilogue multiplies it back. Rows that do not fit are converted once, with
+//    the same prescale, into an f16 scratch in global memory and read from
+//    there (generic loads that bypass L1). Thread 0 also waits for the grid
 //    between the phases.
 #include <cuda.h>
 
@@ -86,7 +87,7 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int cw, int K, int I, int
   m.bars = o;
   o += round_up((size_t)(cw * ring_depth(cw) + 2 * cw + kRowBars) * 8, 16);
   m.flags = o;
-  o += 64;   // int flags[8] + a 16-byte zero chunk + spare
+  o += 64;   // int flags[16]
   m.ints = o;
   o += (size_t)(5 * E + R + 6) * sizeof(int);
   m.eb = o;
@@ -190,22 +191,37 @@ __device__ __forceinline__ RowPlan row_plan(const PhaseView& v, int xs_rows_cap)
   return r;
 }
 
-// B operand of one token group for this lane (token column g): a staged f16
-// row (advanced 64 bytes per block; 0 for padding columns, which read a zero
-// chunk), or an f16 row of the scratch in global memory (rows with no room in
-// shared memory, converted once with the same prescale).
+// B operand of one token group for this lane (token column g), at block 0:
+// the byte offset of its staged f16 row in the activation area (every row of
+// an item staged), or a generic pointer to the row's chunk in shared memory or
+// in the f16 scratch in global memory (rows with no room in shared memory,
+// converted once with the same prescale). Either advances 64 bytes per block.
+// Padding columns (tokens past the item's) read the item's first row; their
+// columns are never stored.
 struct BRows {
-  const uint8_t* row[kMaxGroups];
-  int step[kMaxGroups];
-  const uint16_t* src[kMaxGroups];
+  uint32_t off[kMaxGroups];
+  const uint8_t* gp[kMaxGroups];
 };
+
+// This lane's activation chunk of token group gr at block b: a shared-memory
+// load when every row of the item is staged, else a generic load that stays
+// out of L1 (the scratch is rewritten between the phases).
+template <bool GLOB>
+__device__ __forceinline__ const uint8_t* brow_ptr(const BRows& br, const uint8_t* xs, int gr, int b) {
+  return GLOB ? br.gp[gr] + b * 64 : xs + br.off[gr] + b * 64;
+}
+template <bool GLOB>
+__device__ __forceinline__ uint4 load_b16(const uint8_t* p) {
+  if constexpr (GLOB) return ld_cg_generic16(p);
+  else return *reinterpret_cast<const uint4*>(p);
+}
 
 // One 32-value block of one item for one warp: both m16 rows' 4-byte words,
 // their scales, and one MMA pair per token group.
 template <bool FAST, bool GLOB>
 __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uint8_t* stg, int b,
                                           int g, int t, const uint8_t* sc_g, const uint8_t* sc_g8,
-                                          int bglob, int ng, const BRows& br) {
+                                          int bglob, int ng, const BRows& br, const uint8_t* xs) {
   const int off = (b >> 3) * kColBytes + g * 128 + ((((b & 7) ^ g) << 4) + (t << 2));
   const uint32_t w0 = *reinterpret_cast<const uint32_t*>(stg + off);
   const uint32_t w1 = *reinterpret_cast<const uint32_t*>(stg + off + 8 * 128);
@@ -219,11 +235,7 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
   for (int gr = 0; gr < kMaxGroups; ++gr) {
     if (gr >= ng) break;
     // B: token column g of the group, physical k = 32 bglob + 8t .. +7 (f16)
-    uint4 bv;
-    if (GLOB && br.src[gr] != nullptr)
-      bv = ldcg16(br.src[gr] + bglob * 32 + t * 8);
-    else
-      bv = *reinterpret_cast<const uint4*>(br.row[gr] + bglob * br.step[gr]);
+    const uint4 bv = load_b16<GLOB>(brow_ptr<GLOB>(br, xs, gr, bglob));
     float d[4];
     // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
     mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
@@ -237,17 +249,15 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
 
 // NBAT consecutive 32-value blocks b0 .. b0+NBAT-1 of a stage (b0 a
 // compile-time multiple of 8) for an item with a single token group,
-// software-pipelined: every shared-memory load of the batch is issued before
-// the first conversion, and the blocks' MMA chains are independent, so their
-// latencies overlap. xo[u] is this lane's byte offset of block (8k + u) inside
-// a 128-byte column (row g, 128-byte swizzle); brow / scg / scg8 point at
-// block b0's activation chunk and scale bytes.
-// GLOB: lanes whose token row is not staged (bsrc != nullptr) read their f16
-// chunks from the scratch in global memory (all NBAT loads issued first).
+// software-pipelined: every load of the batch is issued before the first
+// conversion, and the blocks' MMA chains are independent, so their latencies
+// overlap. xo[u] is this lane's byte offset of block (8k + u) inside a
+// 128-byte column (row g, 128-byte swizzle); brow / scg / scg8 point at block
+// b0's activation chunk (shared memory, or generic when GLOB) and scale bytes.
 template <bool FAST, bool GLOB, int NBAT, int B0>
 __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, const int (&xo)[8],
                                            const uint8_t* scg, const uint8_t* scg8,
-                                           const uint8_t* brow, const uint16_t* bsrc) {
+                                           const uint8_t* brow) {
   uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
   uint4 bv[NBAT];
 #pragma unroll
@@ -257,10 +267,7 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
     w1[u] = *reinterpret_cast<const uint32_t*>(p + 8 * 128);
     s0[u] = scg[u];
     s1[u] = scg8[u];
-    if (GLOB && bsrc != nullptr)
-      bv[u] = ldcg16(bsrc + u * 32);
-    else
-      bv[u] = *reinterpret_cast<const uint4*>(brow + u * 64);
+    bv[u] = load_b16<GLOB>(brow + u * 64);
   }
 #pragma unroll
   for (int u = 0; u < NBAT; ++u) {
@@ -281,12 +288,12 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
 
 // As blocks_mma for an item with NG token groups (batches of NBAT blocks):
 // the A words and scales of the batch are loaded once, each group's
-// activation chunks per block (staged, or global with on-the-fly conversion).
+// activation chunk per block.
 template <bool FAST, bool GLOB, int NG, int NBAT, int B0>
 __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], const uint8_t* stg,
                                                   const int (&xo)[8], const uint8_t* scg,
-                                                  const uint8_t* scg8, int bg, int t,
-                                                  const BRows& br) {
+                                                  const uint8_t* scg8, int bg, const BRows& br,
+                                                  const uint8_t* xs) {
   uint32_t w0[NBAT], w1[NBAT], s0[NBAT], s1[NBAT];
   uint4 bv[NBAT][NG];
 #pragma unroll
@@ -297,12 +304,7 @@ __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], c
     s0[u] = scg[u];
     s1[u] = scg8[u];
 #pragma unroll
-    for (int gr = 0; gr < NG; ++gr) {
-      if (GLOB && br.src[gr] != nullptr)
-        bv[u][gr] = ldcg16(br.src[gr] + (bg + u) * 32 + t * 8);
-      else
-        bv[u][gr] = *reinterpret_cast<const uint4*>(br.row[gr] + (bg + u) * br.step[gr]);
-    }
+    for (int gr = 0; gr < NG; ++gr) bv[u][gr] = load_b16<GLOB>(brow_ptr<GLOB>(br, xs, gr, bg + u));
   }
 #pragma unroll
   for (int u = 0; u < NBAT; ++u) {
@@ -329,12 +331,13 @@ __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], c
 template <int CW, bool FAST, bool GLOB, int NG, int B0 = 0>
 __device__ __forceinline__ void stage_groups(float (&acc)[kMaxGroups][4], const uint8_t* stg,
                                              const int (&xo)[8], const uint8_t* sc_g,
-                                             const uint8_t* sc_g8, int bg, int t, const BRows& br) {
+                                             const uint8_t* sc_g8, int bg, const BRows& br,
+                                             const uint8_t* xs) {
   constexpr int NBAT = NG <= 2 ? 4 : 2;
   blocks_mma_groups<FAST, GLOB, NG, NBAT, B0>(acc, stg, xo, sc_g + bg + B0, sc_g8 + bg + B0,
-                                              bg + B0, t, br);
+                                              bg + B0, br, xs);
   if constexpr (B0 + NBAT < kChunkBlocks)
-    stage_groups<CW, FAST, GLOB, NG, B0 + NBAT>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+    stage_groups<CW, FAST, GLOB, NG, B0 + NBAT>(acc, stg, xo, sc_g, sc_g8, bg, br, xs);
 }
 
 // The item sequence of one consumer warp across both phases (items k =
@@ -442,7 +445,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
                                             const uint8_t* ring_w,
                                             uint64_t* full_w, int& s, const PhaseView& v,
                                             int lane, const uint8_t* sc, int ng, const BRows& br,
-                                            StageIssuer& is, const DecodeParams& P,
+                                            const uint8_t* xs, StageIssuer& is, const DecodeParams& P,
                                             const PhaseView& v1, const PhaseView& v2, int n1,
                                             int n2, const int* eb, int cw) {
   constexpr int KD = ring_depth(CW);
@@ -458,39 +461,47 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     const uint8_t* stg = ring_w + slot * kStageBytes;
     const int nb = min(kChunkBlocks, v.nblk - c * kChunkBlocks);
     const int bg = c * kChunkBlocks;   // first block of the stage in the row
-    // this lane's activation chunk of block bg: staged row (64 bytes a block)
-    // or bf16 row in global memory (32 values a block)
-    const uint8_t* brow0 = br.row[0] + bg * 64;
-    const uint16_t* bsrc0 = (GLOB && br.src[0] != nullptr) ? br.src[0] + bg * 32 + t * 8 : nullptr;
-    if (GLOB && CW >= 11) {   // rows read from global memory: one block at a time (registers)
-      for (int b = 0; b < nb; ++b)
-        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+    // this lane's activation chunk of block bg (token group 0)
+    const uint8_t* brow0 = brow_ptr<GLOB>(br, xs, 0, bg);
+    if (ng == 1 && nb == kChunkBlocks && GLOB && CW >= 11) {   // (registers: batches of 4)
+#pragma unroll 1
+      for (int col = 0; col < 2; ++col) {
+        const int b8 = bg + 8 * col;
+        blocks_mma<FAST, GLOB, 4, 0>(acc[0], stg + col * kColBytes, xo, sc_g + b8, sc_g8 + b8,
+                                     brow0 + col * 8 * 64);
+        blocks_mma<FAST, GLOB, 4, 4>(acc[0], stg + col * kColBytes, xo, sc_g + b8 + 4, sc_g8 + b8 + 4,
+                                     brow0 + col * 8 * 64 + 4 * 64);
+      }
     } else if (ng == 1 && nb == kChunkBlocks) {
-      blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0);
-      blocks_mma<FAST, GLOB, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8, brow0 + 8 * 64,
-                                   bsrc0 != nullptr ? bsrc0 + 8 * 32 : nullptr);
-    } else if (ng == 1) {   // partial last stage: a batch of 8, then single blocks
+      blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0);
+      blocks_mma<FAST, GLOB, 8, 8>(acc[0], stg, xo, sc_g + bg + 8, sc_g8 + bg + 8, brow0 + 8 * 64);
+    } else if (ng == 1) {   // partial last stage: a batch of 8 (2 x 4), then single blocks
       int b = 0;
       if (nb >= 8) {
-        blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0, bsrc0);
+        if (GLOB && CW >= 11) {
+          blocks_mma<FAST, GLOB, 4, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0);
+          blocks_mma<FAST, GLOB, 4, 4>(acc[0], stg, xo, sc_g + bg + 4, sc_g8 + bg + 4, brow0 + 4 * 64);
+        } else {
+          blocks_mma<FAST, GLOB, 8, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0);
+        }
         b = 8;
       }
       for (; b < nb; ++b)
-        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br, xs);
     } else if (nb == kChunkBlocks && CW < 10) {   // (the 10- to 12-warp forms have no registers to spare)
       if (ng == 2)
-        stage_groups<CW, FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 2>(acc, stg, xo, sc_g, sc_g8, bg, br, xs);
       else if (ng == 3)
-        stage_groups<CW, FAST, GLOB, 3>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 3>(acc, stg, xo, sc_g, sc_g8, bg, br, xs);
       else
-        stage_groups<CW, FAST, GLOB, 4>(acc, stg, xo, sc_g, sc_g8, bg, t, br);
+        stage_groups<CW, FAST, GLOB, 4>(acc, stg, xo, sc_g, sc_g8, bg, br, xs);
     } else if (nb == kChunkBlocks) {
 #pragma unroll 4
       for (int b = 0; b < kChunkBlocks; ++b)
-        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br);
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br, xs);
     } else {
       for (int b = 0; b < nb; ++b)
-        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, c * kChunkBlocks + b, ng, br);
+        block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br, xs);
     }
     // the slot is refilled by tensor copies (async proxy): order the generic
     // reads of it before that write
@@ -533,7 +544,6 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   uint64_t* sfull = wfull + CW * KD;                              // [CW][2]
   uint64_t* xfull = sfull + 2 * CW;                               // [kRowBars]
   int* flags = reinterpret_cast<int*>(smem + M.flags);
-  const uint8_t* zero16 = reinterpret_cast<const uint8_t*>(flags + 8);
   RouteTables tb;
   tb.cnt = reinterpret_cast<int*>(smem + M.ints);
   tb.off = tb.cnt + E;
@@ -719,25 +729,16 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       const int ng = (cnt + kGroup - 1) / kGroup;
       BRows br;
       bool glob = false;
-      // padding columns (tokens past the item's) read the item's first row when
-      // it is staged (their columns are never stored), else a zero chunk
       const int q_first = ir.q0 - v.p_lo;
-      const bool first_staged = q_first < rp.xs_rows;
 #pragma unroll
       for (int gr = 0; gr < kMaxGroups; ++gr) {
-        br.row[gr] = first_staged ? xs + (size_t)q_first * xs_stride + t * 16 : zero16;
-        br.step[gr] = first_staged ? 64 : 0;
-        br.src[gr] = nullptr;
-        if (gr < ng && gr * kGroup + g < cnt) {
-          const int q = ir.q0 + gr * kGroup + g - v.p_lo;
-          if (q < rp.xs_rows) {
-            br.row[gr] = xs + (size_t)q * xs_stride + t * 16;
-            br.step[gr] = 64;
-          } else {
-            br.src[gr] = a.xf + (size_t)(v.p_lo + q) * xf_stride;
-            glob = true;
-          }
-        }
+        int q = q_first;   // padding columns: the item's first row
+        if (gr < ng && gr * kGroup + g < cnt) q = q_first + gr * kGroup + g;
+        const bool staged = q < rp.xs_rows;
+        glob |= !staged;
+        br.off[gr] = (uint32_t)q * (uint32_t)xs_stride + t * 16;
+        br.gp[gr] = staged ? xs + br.off[gr]
+                           : reinterpret_cast<const uint8_t*>(a.xf + (size_t)(v.p_lo + q) * xf_stride) + t * 16;
       }
       glob = __any_sync(0xffffffffu, glob);
       float acc[kMaxGroups][4];
@@ -746,16 +747,16 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
       if (!special && !glob)
-        ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
+        ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is, P,
                                           v1, v2, n1, n2, eb, cw);
       else if (special && !glob)
-        ok = item_stages<CW, false, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is, P,
+        ok = item_stages<CW, false, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is, P,
                                            v1, v2, n1, n2, eb, cw);
       else if (!special)
-        ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+        ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is,
                                               P, v1, v2, n1, n2, eb, cw);
       else
-        ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, is,
+        ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is,
                                                P, v1, v2, n1, n2, eb, cw);
       if (!ok) {
         fail |= 16;
