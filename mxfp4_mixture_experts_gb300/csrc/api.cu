@@ -131,6 +131,22 @@ bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  if (!get_encoder() || rank < 2 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides[i];
+  return g_encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), d,
+                        st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
 }  // namespace mxmoe
 
 extern "C" {
@@ -207,8 +223,23 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
         !encode_tiled_2d(&map2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, (uint64_t)I / 2, (uint64_t)E * K,
                          (uint64_t)I / 2, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
       return MXFP4_MOE_ERR_CUDA;
+    // whole stages (two 128-byte chunks of 8 gate + 8 up rows / 16 w2 rows) in
+    // one copy; the chunk extent counts only whole chunks of a row, so a box
+    // never reaches past a row (the last, partial stage takes the 2-D maps)
+    CUtensorMap map1q, map2q;
+    const uint64_t nc1 = (uint64_t)K / 2 / 128, nc2 = (uint64_t)I / 2 / 128;
+    // (rows with fewer than two whole chunks never take these maps)
+    const uint64_t d1[4] = {128, (uint64_t)E * 2 * I, 2, nc1 > 2 ? nc1 : 2};
+    const uint64_t st1[3] = {(uint64_t)K / 2, (uint64_t)I * K / 2, 128};
+    const uint32_t b1[4] = {128, 8, 2, 2};
+    const uint64_t d2[3] = {128, (uint64_t)E * K, nc2 > 2 ? nc2 : 2};
+    const uint64_t st2[2] = {(uint64_t)I / 2, 128};
+    const uint32_t b2[3] = {128, 16, 2};
+    if (!encode_tiled_u8(&map1q, w13, 4, d1, st1, b1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled_u8(&map2q, w2, 3, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MXFP4_MOE_ERR_CUDA;
     record_phase(0, s);
-    const cudaError_t e = launch_decode(a, map1, map2, d->num_sms, d->max_smem, s);
+    const cudaError_t e = launch_decode(a, map1, map2, map1q, map2q, d->num_sms, d->max_smem, s);
     if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     record_phase(1, s);
     return MXFP4_MOE_OK;

@@ -387,11 +387,27 @@ __device__ __forceinline__ void cursor_rows(const ItemCursor& c, const DecodeArg
   r1 = item_row(c.phase, a, e, c.rb, 1);
 }
 
+// Position in a warp's KD-stage ring: stage n sits in slot n % KD and is the
+// (n / KD)-th use of that slot (phase parity), kept incrementally.
+struct RingPos {
+  int n, slot;
+  uint32_t par;
+};
+template <int KD>
+__device__ __forceinline__ void ring_advance(RingPos& r) {
+  ++r.n;
+  if (++r.slot == KD) {
+    r.slot = 0;
+    r.par ^= 1u;
+  }
+}
+
 // Lane 0 of a consumer warp: issues the warp's weight stages in order into
-// its KD-stage ring (stage n goes to slot n % KD, tracked by full[n % KD]).
+// its KD-stage ring (tracked by full[slot]).
 struct StageIssuer {
   ItemCursor cur;
-  int c, count, row0, row1;
+  RingPos q;
+  int c, row0, row1;
 };
 template <int CW>
 __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams& P,
@@ -402,21 +418,29 @@ __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams&
   const PhaseView& v = is.cur.phase == 1 ? v1 : v2;
   if (is.c == 0) cursor_rows(is.cur, P.a, eb, is.row0, is.row1);
   constexpr int KD = ring_depth(CW);
-  const int slot = is.count % KD;
+  const int slot = is.q.slot;
   uint8_t* dst = ring_w + slot * kStageBytes;
   uint64_t* bar = &full_w[slot];
   const int x0 = is.c * kChunk;
-  const int ncols = min(2, (v.kred / 2 - x0 + 127) / 128);
-  mbar_arrive_expect_tx(bar, (uint32_t)ncols * kColBytes);
-  for (int col = 0; col < ncols; ++col) {
-    if (is.cur.phase == 1) {   // 8 gate rows, then the 8 matching up rows
-      tma_load_2d(dst + col * kColBytes, &P.tmap1, x0 + col * 128, is.row0, bar);
-      tma_load_2d(dst + col * kColBytes + 8 * 128, &P.tmap1, x0 + col * 128, is.row1, bar);
-    } else {                   // 16 consecutive rows
-      tma_load_2d(dst + col * kColBytes, &P.tmap2, x0 + col * 128, is.row0, bar);
+  if (x0 + kChunk <= v.kred / 2) {   // a whole stage: one copy
+    mbar_arrive_expect_tx(bar, (uint32_t)kStageBytes);
+    if (is.cur.phase == 1)   // [chunk][gate, up][8 rows][128 bytes]
+      tma_load_4d(dst, &P.tmap1q, 0, is.row0, 0, 2 * is.c, bar);
+    else                     // [chunk][16 rows][128 bytes]
+      tma_load_3d(dst, &P.tmap2q, 0, is.row0, 2 * is.c, bar);
+  } else {                           // the last, partial stage: 2-D copies
+    const int ncols = min(2, (v.kred / 2 - x0 + 127) / 128);
+    mbar_arrive_expect_tx(bar, (uint32_t)ncols * kColBytes);
+    for (int col = 0; col < ncols; ++col) {
+      if (is.cur.phase == 1) {   // 8 gate rows, then the 8 matching up rows
+        tma_load_2d(dst + col * kColBytes, &P.tmap1, x0 + col * 128, is.row0, bar);
+        tma_load_2d(dst + col * kColBytes + 8 * 128, &P.tmap1, x0 + col * 128, is.row1, bar);
+      } else {                   // 16 consecutive rows
+        tma_load_2d(dst + col * kColBytes, &P.tmap2, x0 + col * 128, is.row0, bar);
+      }
     }
   }
-  ++is.count;
+  ring_advance<KD>(is.q);
   if (++is.c == v.nc) {
     is.c = 0;
     cursor_next<CW>(is.cur, n1, n2, v1, v2, cw);
@@ -443,7 +467,7 @@ __device__ __forceinline__ void issue_scales(const ItemCursor& cur, const Decode
 template <int CW, bool FAST, bool GLOB>
 __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const int (&xo)[8],
                                             const uint8_t* ring_w,
-                                            uint64_t* full_w, int& s, const PhaseView& v,
+                                            uint64_t* full_w, RingPos& s, const PhaseView& v,
                                             int lane, const uint8_t* sc, int ng, const BRows& br,
                                             const uint8_t* xs, StageIssuer& is, const DecodeParams& P,
                                             const PhaseView& v1, const PhaseView& v2, int n1,
@@ -452,18 +476,18 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
   const int g = lane >> 2, t = lane & 3;
   const uint8_t* sc_g = sc + g * v.nblk;
   const uint8_t* sc_g8 = sc + (g + 8) * v.nblk;
-  for (int c = 0; c < v.nc; ++c, ++s) {
+  for (int c = 0; c < v.nc; ++c, ring_advance<KD>(s)) {
     // keep KD - 1 stages ahead: the slot refilled now held stage s - 1, which
     // every lane has finished reading (fenced below)
     if (lane == 0) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
-    const int slot = s % KD;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], (uint32_t)(s / KD) & 1u))) return false;
+    const int slot = s.slot;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], s.par))) return false;
     const uint8_t* stg = ring_w + slot * kStageBytes;
     const int nb = min(kChunkBlocks, v.nblk - c * kChunkBlocks);
     const int bg = c * kChunkBlocks;   // first block of the stage in the row
     // this lane's activation chunk of block bg (token group 0)
     const uint8_t* brow0 = brow_ptr<GLOB>(br, xs, 0, bg);
-    if (ng == 1 && nb == kChunkBlocks && GLOB && CW >= 11) {   // (registers: batches of 4)
+    if (ng == 1 && nb == kChunkBlocks && GLOB && CW >= 10) {   // (registers: batches of 4)
 #pragma unroll 1
       for (int col = 0; col < 2; ++col) {
         const int b8 = bg + 8 * col;
@@ -478,7 +502,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
     } else if (ng == 1) {   // partial last stage: a batch of 8 (2 x 4), then single blocks
       int b = 0;
       if (nb >= 8) {
-        if (GLOB && CW >= 11) {
+        if (GLOB && CW >= 10) {
           blocks_mma<FAST, GLOB, 4, 0>(acc[0], stg, xo, sc_g + bg, sc_g8 + bg, brow0);
           blocks_mma<FAST, GLOB, 4, 4>(acc[0], stg, xo, sc_g + bg + 4, sc_g8 + bg + 4, brow0 + 4 * 64);
         } else {
@@ -567,6 +591,8 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     for (int i = 0; i < 2 * CW; ++i) mbar_init(&sfull[i], 1);
     for (int i = 0; i < kRowBars; ++i) mbar_init(&xfull[i], 1);
     fence_barrier_init();
+    prefetch_tensormap(&P.tmap1q);
+    prefetch_tensormap(&P.tmap2q);
     prefetch_tensormap(&P.tmap1);
     prefetch_tensormap(&P.tmap2);
   }
@@ -618,7 +644,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   const int n1 = warp_items<CW>(cw, v1.n), n2 = warp_items<CW>(cw, v2.n);
   bool ok = true;
   int fail = 0;
-  int s = 0;                 // running stage number of this warp
+  RingPos s = {0, 0, 0u};    // running stage of this warp
   int kitems = 0;            // items this warp has started
   uint32_t rows_used = 0;    // staged-row barriers used in phase 1
   // stage and scale pipelines: the first KD - 1 stages and the first item's scales
@@ -626,7 +652,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   is.cur.phase = 1;
   is.cur.k = 0;
   is.c = 0;
-  is.count = 0;
+  is.q = {0, 0, 0u};
   is.row0 = is.row1 = 0;
   is.cur.j = is.cur.rb = 0;
   cursor_locate<CW>(is.cur, v1, v2, cw);
@@ -816,7 +842,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   // stages issued ahead but never consumed (only after a failed wait) must
   // land before the CTA exits
   if (lane == 0) {
-    for (int n = s; n < is.count; ++n) mbar_wait(&full_w[n % KD], (uint32_t)(n / KD) & 1u);
+    for (int n = s.n; n < is.q.n; ++n) mbar_wait(&full_w[n % KD], (uint32_t)(n / KD) & 1u);
     for (int n = kitems; n < sc_count; ++n) mbar_wait(&sfull_w[n & 1], (uint32_t)(n >> 1) & 1u);
   }
   if (!ok && lane == 0 && a.status != nullptr) {
@@ -905,10 +931,13 @@ static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cu
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
-                          int num_sms, int max_smem, cudaStream_t stream) {
+                          const CUtensorMap& tmap1q, const CUtensorMap& tmap2q, int num_sms,
+                          int max_smem, cudaStream_t stream) {
   DecodeParams p;
   p.tmap1 = tmap1;
   p.tmap2 = tmap2;
+  p.tmap1q = tmap1q;
+  p.tmap2q = tmap2q;
   p.a = a;
   const int R = a.T * a.topk;
   const int cw = decode_warps(a.K, a.I, a.E, a.T, a.topk, max_smem);

@@ -29,6 +29,11 @@ struct DecodeArgs {
 struct DecodeParams {
   CUtensorMap tmap1;      // w13 packed as 2-D u8 [E*2I rows][K/2], box {128, 8}
   CUtensorMap tmap2;      // w2 packed as 2-D u8 [E*K rows][I/2], box {128, 16}
+  // whole 4 KB stages in one copy: w13 as 4-D u8 {128 bytes, E*2I rows, 2 halves
+  // (gate, up: I rows apart), whole 128-byte chunks of a row}, box {128, 8, 2, 2};
+  // w2 as 3-D u8 {128 bytes, E*K rows, whole chunks}, box {128, 16, 2}
+  CUtensorMap tmap1q;
+  CUtensorMap tmap2q;
   DecodeArgs a;
   int stages;             // weight ring depth (4 KB stages)
   int xs_rows_cap;        // activation rows staged in shared memory
@@ -40,13 +45,20 @@ bool decode_fits(int K, int I, int E, int T, int topk, int max_smem);
 
 // One cooperative launch (one CTA per SM, all resident) per decode call.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,
-                          int num_sms, int max_smem, cudaStream_t stream);
+                          const CUtensorMap& tmap1q, const CUtensorMap& tmap2q, int num_sms,
+                          int max_smem, cudaStream_t stream);
 
 // 2-D tiled tensor map [dim1 rows][dim0 elements] with the given row pitch,
 // box {box0, box1}; reads past the tensor return zeros (api.cu).
 bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0,
                      uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
                      CUtensorMapSwizzle swizzle);
+
+// Tiled u8 tensor map of the given rank (2..5): dims and box innermost first,
+// strides[i] = bytes between consecutive coordinates of dimension i + 1 (any
+// order; the views may overlap); reads past a dimension return zeros (api.cu).
+bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                     const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);
