@@ -203,6 +203,20 @@ struct BRows {
   const uint8_t* gp[kMaxGroups];
 };
 
+// Token group GR's B row for this lane (token column g of the group, padding
+// columns: the item's first row q_first); glob is set when it is not staged.
+template <int GR>
+__device__ __forceinline__ void set_group(BRows& br, bool& glob, int q_first, int cnt, int g, int t,
+                                          int xs_rows, int xs_stride, const uint8_t* xs,
+                                          const uint8_t* xf_lo, size_t xf_stride) {
+  int q = q_first;
+  if (GR * kGroup + g < cnt) q = q_first + GR * kGroup + g;
+  const bool staged = q < xs_rows;
+  glob |= !staged;
+  br.off[GR] = (uint32_t)q * (uint32_t)xs_stride + t * 16;
+  br.gp[GR] = staged ? xs + br.off[GR] : xf_lo + (size_t)q * xf_stride * 2;
+}
+
 // This lane's activation chunk of token group gr at block b: a shared-memory
 // load when every row of the item is staged, else a generic load that stays
 // out of L1 (the scratch is rewritten between the phases).
@@ -722,10 +736,20 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
 
     // -- this warp's items of the phase: item k of the warp is CTA item ib + k CW + cw
     const int my_n = phase == 1 ? n1 : n2;
+    int cj = 0, crb = 0;   // expert batch and row block of the warp's next item
+    if (my_n > 0) {
+      const int it0 = v.ib + cw;
+      cj = it0 / v.NB;
+      crb = it0 - cj * v.NB;
+    }
     for (int k = 0; k < my_n && ok; ++k) {
-      const int it = v.ib + k * CW + cw;
-      const ItemRoutes ir = item_routes(tb, eb, it / v.NB);
-      const int rb = it % v.NB;
+      const ItemRoutes ir = item_routes(tb, eb, cj);
+      const int rb = crb;
+      crb += CW;
+      while (crb >= v.NB) {
+        crb -= v.NB;
+        ++cj;
+      }
       const int sx = kitems & 1;
       // the next item's scale rows go to the other slot, which the previous
       // item (finished and fenced) no longer reads
@@ -740,31 +764,35 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
         break;
       }
       const uint8_t* sc = scale_w + sx * M.slot_bytes;
-      // E8M0 bytes 0 / 255 in this item: take the exact general conversion
-      bool bad = false;
-      const uint32_t* sw = reinterpret_cast<const uint32_t*>(sc);
-      for (int i = lane; i < (kRows * v.nblk) / 4; i += 32) {
-        const uint32_t x = sw[i];
-        const uint32_t z = (x - 0x01010101u) & ~x & 0x80808080u;     // some byte == 0
-        const uint32_t f = (~x - 0x01010101u) & x & 0x80808080u;     // some byte == 0xFF
-        bad |= (z | f) != 0u;
+      // E8M0 bytes 0 / 255 in this item: take the exact general conversion.
+      // A byte is 0x00 or 0xFF exactly when its bits are all equal, i.e. when
+      // b ^ (b >> 1) is 0 in bits 0..6; subtracting 1 from each such 7-bit
+      // value sets bit 7 of some byte exactly when one of them is 0.
+      uint32_t hit = 0;
+      const uint4* sw = reinterpret_cast<const uint4*>(sc);
+      for (int i = lane; i < v.nblk; i += 32) {   // 16 rows x nblk bytes = nblk 16-byte words
+        const uint4 x = sw[i];
+        hit |= ((x.x ^ (x.x >> 1)) & 0x7F7F7F7Fu) - 0x01010101u;
+        hit |= ((x.y ^ (x.y >> 1)) & 0x7F7F7F7Fu) - 0x01010101u;
+        hit |= ((x.z ^ (x.z >> 1)) & 0x7F7F7F7Fu) - 0x01010101u;
+        hit |= ((x.w ^ (x.w >> 1)) & 0x7F7F7F7Fu) - 0x01010101u;
       }
-      const bool special = __any_sync(0xffffffffu, bad);
+      const bool special = __any_sync(0xffffffffu, (hit & 0x80808080u) != 0u);
       // B rows of the item's token groups for this lane's token column g
       const int cnt = ir.cnt;
       const int ng = (cnt + kGroup - 1) / kGroup;
+      // (groups past ng are never read)
       BRows br;
       bool glob = false;
       const int q_first = ir.q0 - v.p_lo;
-#pragma unroll
-      for (int gr = 0; gr < kMaxGroups; ++gr) {
-        int q = q_first;   // padding columns: the item's first row
-        if (gr < ng && gr * kGroup + g < cnt) q = q_first + gr * kGroup + g;
-        const bool staged = q < rp.xs_rows;
-        glob |= !staged;
-        br.off[gr] = (uint32_t)q * (uint32_t)xs_stride + t * 16;
-        br.gp[gr] = staged ? xs + br.off[gr]
-                           : reinterpret_cast<const uint8_t*>(a.xf + (size_t)(v.p_lo + q) * xf_stride) + t * 16;
+      const uint8_t* xf_lo = reinterpret_cast<const uint8_t*>(a.xf + (size_t)v.p_lo * xf_stride) + t * 16;
+      set_group<0>(br, glob, q_first, cnt, g, t, rp.xs_rows, xs_stride, xs, xf_lo, xf_stride);
+      if (ng > 1) {
+        set_group<1>(br, glob, q_first, cnt, g, t, rp.xs_rows, xs_stride, xs, xf_lo, xf_stride);
+        if (ng > 2) {
+          set_group<2>(br, glob, q_first, cnt, g, t, rp.xs_rows, xs_stride, xs, xf_lo, xf_stride);
+          if (ng > 3) set_group<3>(br, glob, q_first, cnt, g, t, rp.xs_rows, xs_stride, xs, xf_lo, xf_stride);
+        }
       }
       glob = __any_sync(0xffffffffu, glob);
       float acc[kMaxGroups][4];
