@@ -36,6 +36,13 @@ library matmul per projection):
 All arithmetic is float64; products of E2M1 values, powers of two and bf16
 activations are exact there, so the only roundings are the sums (float64) and
 the optional bf16 rounding of h.
+
+``forward_oai`` is the gpt-oss form of the same layer ("MXFP4 MoE decode
+kernels", Design, "Read the served layout" and "Fused epilogues"): the w13 rows
+of each expert interleave gate and up (row 2i = gate i, row 2i + 1 = up i),
+f32 biases are added to g, u and o, the activation is SwiGLU-OAI (gate capped
+at 7, up clamped to [-7, 7], gate * sigmoid(1.702 gate) * (up + 1)), and the
+w2 bias enters each route's output before the routing weight.
 """
 from __future__ import annotations
 
@@ -188,6 +195,68 @@ def forward(hidden_bits, topk_ids, topk_weights, w13, s13, w2, s2,
             h = round_to_bf16(h)
         W2 = dequant(w2[e], s2[e])                    # [K, I]
         o[r] = h @ W2.T
+    y = np.zeros((T, K), dtype=np.float64)
+    E_ok = (ids >= 0) & (ids < E)
+    for j in range(k):                                # slot order j = 0 .. k-1
+        rows = np.arange(T) * k + j
+        contrib = wts[:, j:j + 1] * o[rows]
+        y += np.where(E_ok[:, j:j + 1], contrib, 0.0)
+    return y
+
+
+# --- the gpt-oss form ---------------------------------------------------------
+OAI_GATE_CAP = 7.0      # gate capped above at 7
+OAI_UP_CLAMP = 7.0      # up clamped to [-7, 7]
+OAI_ALPHA = 1.702       # gate * sigmoid(1.702 * gate)
+
+
+def swiglu_oai(g, u):
+    """SwiGLU-OAI ("MXFP4 MoE decode kernels", Design, Fused epilogues):
+    gate capped at 7 (no lower bound), up clamped to [-7, 7], then
+    gate * sigmoid(1.702 * gate) * (up + 1). NaN inputs stay NaN."""
+    g = np.minimum(np.asarray(g, dtype=np.float64), OAI_GATE_CAP)
+    u = np.clip(np.asarray(u, dtype=np.float64), -OAI_UP_CLAMP, OAI_UP_CLAMP)
+    return g * (1.0 / (1.0 + np.exp(-OAI_ALPHA * g))) * (u + 1.0)
+
+
+def forward_oai(hidden_bits, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2,
+                intermediate: str = "bf16", tokens=None) -> np.ndarray:
+    """The gpt-oss MoE layer output y [T', K] in float64 (not rounded to bf16).
+
+    As ``forward``, with w13 rows interleaved per expert (row 2i = gate i,
+    row 2i + 1 = up i; "Read the served layout": gate and up rows
+    interleaved), b13 float32 [E, 2I] in the same row order, b2 float32 [E, K].
+    g = W_gate x + b_gate, u = W_up x + b_up (bias added in fp32 before the
+    activation), h = swiglu_oai(g, u) (rounded once to bf16 unless
+    intermediate == "fp32"), o = W2 h + b2, and y_t = sum over slots j of
+    w_tj * o_(t,j): the routing-weighted bias enters once per route.
+    """
+    if intermediate not in ("bf16", "fp32"):
+        raise ValueError(intermediate)
+    ids = np.asarray(topk_ids)
+    wts = np.asarray(topk_weights).astype(np.float64)
+    xs = bf16_bits_to_float(hidden_bits)
+    if tokens is not None:
+        tokens = np.asarray(tokens, dtype=np.int64)
+        ids, wts, xs = ids[tokens], wts[tokens], xs[tokens]
+    T, k = ids.shape
+    E, twoI, _ = w13.shape
+    K = w2.shape[1]
+    bias13 = np.asarray(b13, dtype=np.float64)
+    bias2 = np.asarray(b2, dtype=np.float64)
+    rt = route(ids, E)
+    o = np.zeros((T * k, K), dtype=np.float64)
+    for e in rt["touched"].tolist():
+        r = rt["list"][rt["offset"][e]:rt["offset"][e + 1]]
+        x_e = xs[r // k]                              # [M_e, K]
+        W13 = dequant(w13[e], s13[e])                 # [2I, K], rows gate0, up0, gate1, ...
+        g = x_e @ W13[0::2].T + bias13[e, 0::2]
+        u = x_e @ W13[1::2].T + bias13[e, 1::2]
+        h = swiglu_oai(g, u)
+        if intermediate == "bf16":
+            h = round_to_bf16(h)
+        W2 = dequant(w2[e], s2[e])                    # [K, I]
+        o[r] = h @ W2.T + bias2[e]
     y = np.zeros((T, K), dtype=np.float64)
     E_ok = (ids >= 0) & (ids < E)
     for j in range(k):                                # slot order j = 0 .. k-1
