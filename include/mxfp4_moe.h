@@ -115,6 +115,32 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
                       void* workspace, size_t workspace_bytes,
                       int path, void* stream);
 
+/* The gpt-oss form of the layer ("MXFP4 MoE decode kernels", Design, "Read
+ * the served layout" and "Fused epilogues"):
+ *   y_t = sum_j w_tj * (W2[e] h + b2[e]),  h = SwiGLU-OAI(W_gate[e] x + b_gate[e],
+ *                                                     W_up[e] x + b_up[e])
+ *   SwiGLU-OAI(g, u) = min(g, 7) * sigmoid(1.702 min(g, 7)) * (clamp(u, -7, 7) + 1)
+ * with h rounded once to bf16 between the projections and all sums in fp32.
+ *   w13 / s13     uint8 [E, 2I, K/2] / [E, 2I, K/32] with the gate and up rows
+ *                 INTERLEAVED: row 2i is gate row i, row 2i + 1 is up row i
+ *   b13           fp32  [E, 2I] in the same (interleaved) row order
+ *   w2 / s2       as for mxfp4_moe_forward
+ *   b2            fp32  [E, K]; each route adds its expert's b2 before the
+ *                 routing weight, so a token gets sum_j w_tj * b2[e_tj]
+ * Other arguments, limits and errors as mxfp4_moe_forward, except that this
+ * form runs the decode path only: path 2, T > 32 or sizes the decode kernel
+ * does not fit give MXFP4_MOE_ERR_SHAPE. b13 and b2 are device pointers, 4-byte
+ * aligned (MXFP4_MOE_ERR_ALIGN), non-NULL (MXFP4_MOE_ERR_ARG); the caller owns
+ * every buffer. NaN in a pre-activation stays NaN (the cap and clamp do not
+ * replace it). */
+int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                          const uint8_t* w13, const uint8_t* s13, const float* b13,
+                          const uint8_t* w2, const uint8_t* s2, const float* b2,
+                          int T, int K, int I, int E, int topk,
+                          void* out, int32_t* status,
+                          void* workspace, size_t workspace_bytes,
+                          int path, void* stream);
+
 /* The forward call for callers that cannot allocate device memory. The pages
  * have no counterpart of this entry point: it is a convenience of this
  * library. Some callers may not call cudaMalloc at all -- code that runs under

@@ -147,6 +147,73 @@ bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t*
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
+// The decode path (one cooperative launch) of both forward forms: tensor maps
+// over the packed weights, then the kernel.
+int run_decode(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+               const uint8_t* w13, const uint8_t* s13, const float* b13, const uint8_t* w2,
+               const uint8_t* s2, const float* b2, int T, int K, int I, int E, int topk, void* out,
+               int32_t* status, char* ws, const Layout& L, int oai, DeviceInfo* d, cudaStream_t s) {
+  DecodeArgs a = {};
+  a.x = static_cast<const uint16_t*>(hidden);
+  a.ids = topk_ids;
+  a.wts = topk_weights;
+  a.w13 = w13;
+  a.s13 = s13;
+  a.w2 = w2;
+  a.s2 = s2;
+  a.T = T;
+  a.K = K;
+  a.I = I;
+  a.E = E;
+  a.topk = topk;
+  a.h = reinterpret_cast<uint16_t*>(ws + L.h);
+  a.xf = reinterpret_cast<uint16_t*>(ws + L.xp);
+  a.P = reinterpret_cast<float*>(ws + L.P);
+  a.y = static_cast<uint16_t*>(out);
+  a.gbar = reinterpret_cast<int*>(ws + L.gbar);
+  a.status = status;
+  a.b13 = b13;
+  a.b2 = b2;
+  a.oai = oai;
+  // w13 row groups: the gate row of group p and its up row one half-stride
+  // later -- [gate; up] per expert: p = e 2I + i, up I rows later; gpt-oss
+  // (interleaved): p = e I + i, up the next row
+  const uint64_t rb = (uint64_t)K / 2;                       // bytes per packed row
+  const uint64_t groups = oai ? (uint64_t)E * I : (uint64_t)E * 2 * I;
+  const uint64_t group_stride = oai ? 2 * rb : rb;
+  const uint64_t half_stride = oai ? rb : (uint64_t)I * rb;
+  // one 128-byte column of 8 gate + 8 up rows per copy, reads past the row
+  // return zeros (the last, partial stage)
+  CUtensorMap map1, map2;
+  const uint64_t d1c[3] = {rb, groups, 2};
+  const uint64_t st1c[2] = {group_stride, half_stride};
+  const uint32_t b1c[3] = {128, 8, 2};
+  if (!encode_tiled_u8(&map1, w13, 3, d1c, st1c, b1c, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_2d(&map2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, (uint64_t)I / 2, (uint64_t)E * K,
+                       (uint64_t)I / 2, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXFP4_MOE_ERR_CUDA;
+  // whole stages (two 128-byte chunks of 8 gate + 8 up rows / 16 w2 rows) in
+  // one copy; the chunk extent counts only whole chunks of a row, so a box
+  // never reaches past a row (the last, partial stage takes the maps above)
+  CUtensorMap map1q, map2q;
+  const uint64_t nc1 = (uint64_t)K / 2 / 128, nc2 = (uint64_t)I / 2 / 128;
+  // (rows with fewer than two whole chunks never take these maps)
+  const uint64_t d1[4] = {128, groups, 2, nc1 > 2 ? nc1 : 2};
+  const uint64_t st1[3] = {group_stride, half_stride, 128};
+  const uint32_t b1[4] = {128, 8, 2, 2};
+  const uint64_t d2[3] = {128, (uint64_t)E * K, nc2 > 2 ? nc2 : 2};
+  const uint64_t st2[2] = {(uint64_t)I / 2, 128};
+  const uint32_t b2q[3] = {128, 16, 2};
+  if (!encode_tiled_u8(&map1q, w13, 4, d1, st1, b1, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tiled_u8(&map2q, w2, 3, d2, st2, b2q, CU_TENSOR_MAP_SWIZZLE_128B))
+    return MXFP4_MOE_ERR_CUDA;
+  record_phase(0, s);
+  const cudaError_t e = launch_decode(a, map1, map2, map1q, map2q, d->num_sms, d->max_smem, s);
+  if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
+  record_phase(1, s);
+  return MXFP4_MOE_OK;
+}
+
 }  // namespace mxmoe
 
 extern "C" {
@@ -195,55 +262,9 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
 
-  if (decode) {
-    DecodeArgs a = {};
-    a.x = static_cast<const uint16_t*>(hidden);
-    a.ids = topk_ids;
-    a.wts = topk_weights;
-    a.w13 = w13;
-    a.s13 = s13;
-    a.w2 = w2;
-    a.s2 = s2;
-    a.T = T;
-    a.K = K;
-    a.I = I;
-    a.E = E;
-    a.topk = topk;
-    a.h = reinterpret_cast<uint16_t*>(ws + L.h);
-    a.xf = reinterpret_cast<uint16_t*>(ws + L.xp);
-    a.P = reinterpret_cast<float*>(ws + L.P);
-    a.y = static_cast<uint16_t*>(out);
-    a.gbar = reinterpret_cast<int*>(ws + L.gbar);
-    a.status = status;
-    // packed weights as 2-D byte tensors [rows][row bytes], 128-byte swizzled
-    // tiles of 128 bytes x 8 rows (w13: gate and up runs) / x 16 rows (w2)
-    CUtensorMap map1, map2;
-    if (!encode_tiled_2d(&map1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, (uint64_t)K / 2,
-                         (uint64_t)E * 2 * I, (uint64_t)K / 2, 128, 8, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled_2d(&map2, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, (uint64_t)I / 2, (uint64_t)E * K,
-                         (uint64_t)I / 2, 128, 16, CU_TENSOR_MAP_SWIZZLE_128B))
-      return MXFP4_MOE_ERR_CUDA;
-    // whole stages (two 128-byte chunks of 8 gate + 8 up rows / 16 w2 rows) in
-    // one copy; the chunk extent counts only whole chunks of a row, so a box
-    // never reaches past a row (the last, partial stage takes the 2-D maps)
-    CUtensorMap map1q, map2q;
-    const uint64_t nc1 = (uint64_t)K / 2 / 128, nc2 = (uint64_t)I / 2 / 128;
-    // (rows with fewer than two whole chunks never take these maps)
-    const uint64_t d1[4] = {128, (uint64_t)E * 2 * I, 2, nc1 > 2 ? nc1 : 2};
-    const uint64_t st1[3] = {(uint64_t)K / 2, (uint64_t)I * K / 2, 128};
-    const uint32_t b1[4] = {128, 8, 2, 2};
-    const uint64_t d2[3] = {128, (uint64_t)E * K, nc2 > 2 ? nc2 : 2};
-    const uint64_t st2[2] = {(uint64_t)I / 2, 128};
-    const uint32_t b2[3] = {128, 16, 2};
-    if (!encode_tiled_u8(&map1q, w13, 4, d1, st1, b1, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled_u8(&map2q, w2, 3, d2, st2, b2, CU_TENSOR_MAP_SWIZZLE_128B))
-      return MXFP4_MOE_ERR_CUDA;
-    record_phase(0, s);
-    const cudaError_t e = launch_decode(a, map1, map2, map1q, map2q, d->num_sms, d->max_smem, s);
-    if (e != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
-    record_phase(1, s);
-    return MXFP4_MOE_OK;
-  }
+  if (decode)
+    return run_decode(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
+                      topk, out, status, ws, L, 0, d, s);
 
   PrefillArgs p = {};
   p.hidden = static_cast<const uint16_t*>(hidden);
@@ -270,6 +291,34 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
   p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
   p.num_sms = d->num_sms;
   return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));
+}
+
+int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                          const uint8_t* w13, const uint8_t* s13, const float* b13,
+                          const uint8_t* w2, const uint8_t* s2, const float* b2, int T, int K,
+                          int I, int E, int topk, void* out, int32_t* status, void* workspace,
+                          size_t workspace_bytes, int path, void* stream) {
+  if (!shape_ok(T, K, I, E, topk)) return MXFP4_MOE_ERR_SHAPE;
+  if (path < 0 || path > 2) return MXFP4_MOE_ERR_ARG;
+  if (T == 0) return MXFP4_MOE_OK;
+  if (!hidden || !topk_ids || !topk_weights || !w13 || !s13 || !b13 || !w2 || !s2 || !b2 || !out)
+    return MXFP4_MOE_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(s13, 16) || !aligned(s2, 16) || !aligned(b13, 4) || !aligned(b2, 4))
+    return MXFP4_MOE_ERR_ALIGN;
+  if (workspace == nullptr) return MXFP4_MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MXFP4_MOE_ERR_ALIGN;
+  const Layout L = layout(T, K, I, E, topk);
+  if (workspace_bytes < L.total) return MXFP4_MOE_ERR_WORKSPACE;
+  // the gpt-oss form runs the decode path only
+  if (path == 2 || T > kDecodeMaxT || T * topk > kDecodeMaxRoutes || K % 64 || I % 64)
+    return MXFP4_MOE_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  if (!decode_fits(K, I, E, T, topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
+  return run_decode(hidden, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2, T, K, I, E, topk,
+                    out, status, static_cast<char*>(workspace), L, 1, d,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,

@@ -142,6 +142,7 @@ struct PhaseView {
   int kred, nblk, nc, NB;   // reduction length, scale blocks, stages per item, items per batch
   int ib, n;                // first item and count of this CTA
   int p_lo, n_need;         // route-list positions whose activation rows the items use
+  int il;                   // the item's scale rows alternate gate / up (gpt-oss w13)
 };
 
 __device__ __forceinline__ PhaseView phase_view(int phase, const DecodeArgs& a,
@@ -151,6 +152,7 @@ __device__ __forceinline__ PhaseView phase_view(int phase, const DecodeArgs& a,
   v.nblk = v.kred / kScaleBlock;
   v.nc = (v.kred / 2 + kChunk - 1) / kChunk;
   v.NB = phase == 1 ? a.I / 8 : a.K / kRows;
+  v.il = phase == 1 && a.oai != 0;
   const int U = nEB * v.NB;
   v.ib = range_begin(blockIdx.x, U, gridDim.x);
   v.n = range_begin(blockIdx.x + 1, U, gridDim.x) - v.ib;
@@ -174,8 +176,11 @@ __device__ __forceinline__ const uint16_t* act_row(int phase, const DecodeArgs& 
 }
 
 // Weight row of item row 0 (half 0) or item row 8 (half 1) of item (e, rb).
+// Phase 1: the w13 row group of item row 0 (gate row; its up row is one half
+// stride later): row e 2I + i of [gate; up], or pair e I + i of the gpt-oss
+// interleaved rows (half ignored). Phase 2: the w2 row of item row 0 / row 8.
 __device__ __forceinline__ int item_row(int phase, const DecodeArgs& a, int e, int rb, int half) {
-  if (phase == 1) return e * (2 * a.I) + half * a.I + rb * 8;
+  if (phase == 1) return (a.oai ? e * a.I : e * (2 * a.I)) + rb * 8;
   return e * a.K + rb * kRows + half * 8;
 }
 
@@ -447,8 +452,7 @@ __device__ __forceinline__ void issue_stage(StageIssuer& is, const DecodeParams&
     mbar_arrive_expect_tx(bar, (uint32_t)ncols * kColBytes);
     for (int col = 0; col < ncols; ++col) {
       if (is.cur.phase == 1) {   // 8 gate rows, then the 8 matching up rows
-        tma_load_2d(dst + col * kColBytes, &P.tmap1, x0 + col * 128, is.row0, bar);
-        tma_load_2d(dst + col * kColBytes + 8 * 128, &P.tmap1, x0 + col * 128, is.row1, bar);
+        tma_load_3d(dst + col * kColBytes, &P.tmap1, x0 + col * 128, is.row0, 0, bar);
       } else {                   // 16 consecutive rows
         tma_load_2d(dst + col * kColBytes, &P.tmap2, x0 + col * 128, is.row0, bar);
       }
@@ -472,8 +476,13 @@ __device__ __forceinline__ void issue_scales(const ItemCursor& cur, const Decode
   cursor_rows(cur, a, eb, r0, r1);
   const uint32_t run = 8u * v.nblk;   // scale bytes of 8 rows
   mbar_arrive_expect_tx(bar, 2 * run);
-  bulk_load_split(dst, wsc + (size_t)r0 * v.nblk, run, bar);
-  bulk_load_split(dst + run, wsc + (size_t)r1 * v.nblk, run, bar);
+  if (cur.phase == 1 && !a.oai) {     // 8 gate rows, then the 8 matching up rows
+    bulk_load_split(dst, wsc + (size_t)r0 * v.nblk, run, bar);
+    bulk_load_split(dst + run, wsc + ((size_t)r0 + a.I) * v.nblk, run, bar);
+  } else {                            // 16 consecutive rows (w2, or gate/up pairs)
+    const size_t row = cur.phase == 1 ? 2 * (size_t)r0 : (size_t)r0;
+    bulk_load_split(dst, wsc + row * v.nblk, 2 * run, bar);
+  }
 }
 
 // All stages of one item for one warp; false when a wait gave up. s is the
@@ -488,8 +497,9 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
                                             int n2, const int* eb, int cw) {
   constexpr int KD = ring_depth(CW);
   const int g = lane >> 2, t = lane & 3;
-  const uint8_t* sc_g = sc + g * v.nblk;
-  const uint8_t* sc_g8 = sc + (g + 8) * v.nblk;
+  // scale rows of MMA rows g (gate / w2 row g) and g + 8 (up / w2 row g + 8)
+  const uint8_t* sc_g = sc + (v.il ? 2 * g : g) * v.nblk;
+  const uint8_t* sc_g8 = sc + (v.il ? 2 * g + 1 : g + 8) * v.nblk;
   for (int c = 0; c < v.nc; ++c, ring_advance<KD>(s)) {
     // keep KD - 1 stages ahead: the slot refilled now held stage s - 1, which
     // every lane has finished reading (fenced below)
@@ -828,12 +838,27 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
           const int r = tb.lst[qpos];
           const float colmul = pow2f(row_sh[qpos - v.p_lo]);
           if (phase == 1) {
-            const float gate = acc[gr][j] * colmul, up = acc[gr][2 + j] * colmul;
-            a.h[(size_t)r * a.I + rb * 8 + g] = f32_to_bf16_rne(silu_f32(gate) * up);
+            const int i = rb * 8 + g;
+            float gate = acc[gr][j] * colmul, up = acc[gr][2 + j] * colmul;
+            float hv;
+            if (a.oai) {
+              gate += a.b13[((size_t)ir.e * a.I + i) * 2];
+              up += a.b13[((size_t)ir.e * a.I + i) * 2 + 1];
+              hv = swiglu_oai_f32(gate, up);
+            } else {
+              hv = silu_f32(gate) * up;
+            }
+            a.h[(size_t)r * a.I + i] = f32_to_bf16_rne(hv);
           } else {
+            const int m = rb * kRows + g;
             const float wr = a.wts[r];
-            a.P[(size_t)r * a.K + rb * kRows + g] = wr * (acc[gr][j] * colmul);
-            a.P[(size_t)r * a.K + rb * kRows + g + 8] = wr * (acc[gr][2 + j] * colmul);
+            float o0 = acc[gr][j] * colmul, o1 = acc[gr][2 + j] * colmul;
+            if (a.oai) {
+              o0 += a.b2[(size_t)ir.e * a.K + m];
+              o1 += a.b2[(size_t)ir.e * a.K + m + 8];
+            }
+            a.P[(size_t)r * a.K + m] = wr * o0;
+            a.P[(size_t)r * a.K + m + 8] = wr * o1;
           }
         }
       }

@@ -22,6 +22,15 @@ __device__ __forceinline__ int range_owner(int u, int U, int n) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
+// SwiGLU-OAI ("MXFP4 MoE decode kernels", Design, Fused epilogues): gate capped
+// at 7 (no lower cap), up clamped to [-7, 7], gate * sigmoid(1.702 gate) *
+// (up + 1). Comparisons keep a NaN input NaN.
+__device__ __forceinline__ float swiglu_oai_f32(float gate, float up) {
+  gate = gate > 7.0f ? 7.0f : gate;
+  up = up > 7.0f ? 7.0f : (up < -7.0f ? -7.0f : up);
+  return gate / (1.0f + expf(-1.702f * gate)) * (up + 1.0f);
+}
+
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const int* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -22,16 +22,24 @@ struct DecodeArgs {
   uint16_t* y;            // bf16 [T, K]
   int* gbar;              // [2] grid-barrier counters, zero between calls
   int32_t* status;        // [4] or null
+  // gpt-oss form (oai != 0): w13 rows interleaved (row 2i gate i, row 2i + 1
+  // up i), f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI
+  const float* b13;
+  const float* b2;
+  int oai;
 };
 
 // Kernel parameter block: the two weight tensor maps (TMA descriptors,
 // 64-byte aligned) and the launch-time shared-memory plan.
 struct DecodeParams {
-  CUtensorMap tmap1;      // w13 packed as 2-D u8 [E*2I rows][K/2], box {128, 8}
+  // w13 as 3-D u8 {K/2 bytes, row groups, 2 halves}, box {128, 8, 2}: 8 gate
+  // rows then the 8 matching up rows of one 128-byte column (row groups: rows
+  // with the up half I rows later, or gate/up pairs of the gpt-oss form)
+  CUtensorMap tmap1;
   CUtensorMap tmap2;      // w2 packed as 2-D u8 [E*K rows][I/2], box {128, 16}
-  // whole 4 KB stages in one copy: w13 as 4-D u8 {128 bytes, E*2I rows, 2 halves
-  // (gate, up: I rows apart), whole 128-byte chunks of a row}, box {128, 8, 2, 2};
-  // w2 as 3-D u8 {128 bytes, E*K rows, whole chunks}, box {128, 16, 2}
+  // whole 4 KB stages in one copy: w13 as 4-D u8 {128 bytes, row groups, 2
+  // halves, whole 128-byte chunks of a row}, box {128, 8, 2, 2}; w2 as 3-D u8
+  // {128 bytes, E*K rows, whole chunks}, box {128, 16, 2}
   CUtensorMap tmap1q;
   CUtensorMap tmap2q;
   DecodeArgs a;

@@ -44,6 +44,9 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                     vp, vp, vp, sz, i32, vp]
     L.mxfp4_moe_forward.restype = i32
+    L.mxfp4_moe_forward_oai.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                        i32, vp, vp, vp, sz, i32, vp]
+    L.mxfp4_moe_forward_oai.restype = i32
     L.mxfp4_moe_dequant.argtypes = [vp, vp, i32, i32, vp, vp]
     L.mxfp4_moe_dequant.restype = i32
     L.mxfp4_moe_set_phase_events.argtypes = [vp, i32]
@@ -148,6 +151,48 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Te
         workspace.numel() * workspace.element_size(), path, _stream(stream))
     if rc:
         raise MoEError(rc, "mxfp4_moe_forward")
+    return out
+
+
+def forward_oai(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                w13: torch.Tensor, s13: torch.Tensor, b13: torch.Tensor,
+                w2: torch.Tensor, s2: torch.Tensor, b2: torch.Tensor,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, path: int = 0, stream=None) -> torch.Tensor:
+    """The gpt-oss form: w13 rows interleaved (row 2i gate i, row 2i + 1 up i),
+    f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI;
+    y[T, K] bf16 = sum_j w_tj * (W2[e] h + b2[e]). Decode path only (T <= 32)."""
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    for n, t in (("w13", w13), ("s13", s13), ("w2", w2), ("s2", s2)):
+        _need(t, n, torch.uint8, 3)
+    _need(b13, "b13", torch.float32, 2)
+    _need(b2, "b2", torch.float32, 2)
+    T, K = hidden.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    k = topk_ids.shape[1]
+    if tuple(topk_ids.shape) != (T, k) or tuple(topk_weights.shape) != (T, k):
+        raise ValueError("topk_ids / topk_weights must be [T, topk]")
+    if tuple(w13.shape) != (E, 2 * I, K // 2) or tuple(s13.shape) != (E, 2 * I, K // 32):
+        raise ValueError("w13 / s13 shapes must be [E, 2I, K/2] / [E, 2I, K/32]")
+    if tuple(w2.shape) != (E, K, I // 2) or tuple(s2.shape) != (E, K, I // 32):
+        raise ValueError("w2 / s2 shapes must be [E, K, I/2] / [E, K, I/32]")
+    if tuple(b13.shape) != (E, 2 * I) or tuple(b2.shape) != (E, K):
+        raise ValueError("b13 / b2 shapes must be [E, 2I] / [E, K]")
+    if out is None:
+        out = torch.empty(T, K, dtype=torch.bfloat16, device=hidden.device)
+    else:
+        _need(out, "out", torch.bfloat16, 2)
+    if workspace is None:
+        workspace = new_workspace(T, K, I, E, k, hidden.device)
+    rc = lib().mxfp4_moe_forward_oai(
+        _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13), _ptr(s13), _ptr(b13),
+        _ptr(w2), _ptr(s2), _ptr(b2), T, K, I, E, k, _ptr(out), _ptr(status), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), path, _stream(stream))
+    if rc:
+        raise MoEError(rc, "mxfp4_moe_forward_oai")
     return out
 
 

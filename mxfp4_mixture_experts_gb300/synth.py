@@ -180,6 +180,18 @@ def make_case(shape, T: int, seed: int = 0, layer: int = 0,
     return Case(shape, T, hidden, ids, w, w13, s13, w2, s2, logits)
 
 
+def draw_biases(shape, seed: int = 0, layer: int = 0, sigma: float = 0.5):
+    """f32 biases of the gpt-oss form: b13 [E, 2I] (interleaved gate/up row
+    order) and b2 [E, K], N(0, sigma^2), from their own seeded generator (so the
+    other inputs of a case are drawn exactly as without biases)."""
+    if isinstance(shape, str):
+        shape = SHAPES[shape]
+    rng = np.random.Generator(np.random.PCG64(7919 * seed + 104729 * layer + 17))
+    b13 = (sigma * rng.standard_normal((shape.E, 2 * shape.I))).astype(np.float32)
+    b2 = (sigma * rng.standard_normal((shape.E, shape.K))).astype(np.float32)
+    return torch.from_numpy(b13), torch.from_numpy(b2)
+
+
 def hot_routing(T: int, topk: int, E: int, first: int = 0):
     """Every token routed to the same k experts (the pages' "all local"/hot case)."""
     ids = np.tile(np.arange(first, first + topk, dtype=np.int32) % E, (T, 1))

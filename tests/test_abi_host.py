@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxfp4_moe_route", "mxfp4_moe_forward", "mxfp4_moe_dequant",
+    for n in ("mxfp4_moe_route", "mxfp4_moe_forward", "mxfp4_moe_forward_oai", "mxfp4_moe_dequant",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
         assert n in names
 
@@ -109,6 +109,37 @@ def test_forward_rejects_bad_arguments_without_a_gpu(L):
     need = L.mxfp4_moe_workspace_size(4, 64, 64, 4, 2)
     assert fwd(L, ws_bytes=need - 1) == m.ERR_WORKSPACE
     assert fwd(L, T=0) == m.OK                    # nothing to do, nothing enqueued
+
+
+def fwd_oai(L, **kw):
+    a = dict(hidden=VP(0x10000), ids=VP(0x20000), wts=VP(0x30000), w13=VP(0x40000),
+             s13=VP(0x50000), b13=VP(0x58000), w2=VP(0x60000), s2=VP(0x70000), b2=VP(0x78000),
+             T=4, K=64, I=64, E=4, topk=2, out=VP(0x80000), status=None, ws=VP(0x100000),
+             ws_bytes=1 << 40, path=1, stream=None)
+    a.update(kw)
+    return L.mxfp4_moe_forward_oai(a["hidden"], a["ids"], a["wts"], a["w13"], a["s13"], a["b13"],
+                                   a["w2"], a["s2"], a["b2"], a["T"], a["K"], a["I"], a["E"],
+                                   a["topk"], a["out"], a["status"], a["ws"], a["ws_bytes"],
+                                   a["path"], a["stream"])
+
+
+def test_forward_oai_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    assert fwd_oai(L, b13=None) == m.ERR_ARG
+    assert fwd_oai(L, b2=None) == m.ERR_ARG
+    assert fwd_oai(L, hidden=None) == m.ERR_ARG
+    assert fwd_oai(L, path=3) == m.ERR_ARG
+    assert fwd_oai(L, b13=VP(0x58002)) == m.ERR_ALIGN
+    assert fwd_oai(L, b2=VP(0x78001)) == m.ERR_ALIGN
+    assert fwd_oai(L, w13=VP(0x40004)) == m.ERR_ALIGN
+    assert fwd_oai(L, K=65) == m.ERR_SHAPE
+    assert fwd_oai(L, path=2) == m.ERR_SHAPE          # decode path only
+    assert fwd_oai(L, T=33, path=0) == m.ERR_SHAPE
+    assert fwd_oai(L, K=96, I=64) == m.ERR_SHAPE
+    assert fwd_oai(L, ws=None) == m.ERR_WORKSPACE
+    need = L.mxfp4_moe_workspace_size(4, 64, 64, 4, 2)
+    assert fwd_oai(L, ws_bytes=need - 1) == m.ERR_WORKSPACE
+    assert fwd_oai(L, T=0) == m.OK
 
 
 def test_route_and_dequant_reject_bad_arguments(L):
