@@ -410,15 +410,18 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
 def measure_configs(dev, hbm_gbs: float, reps: int = 10):
     """The other decode workload shapes (the 32-expert single layer at T = 1,
     the 6144 x 2048 256-expert layer at T = 1, 8, 32 and the wide-K skewed
-    layer at T = 1 .. 32): microseconds per call and GB/s of the touched
-    experts' packed bytes, from CUDA-graph replays of single calls that
-    alternate between two layers of weights (inputs larger than L2)."""
+    layer at T = 1 .. 32) and the gpt-oss form of the 2880 x 2880 128-expert
+    layer (interleaved gate/up rows, biases, SwiGLU-OAI; T = 1 .. 32):
+    microseconds per call and GB/s of the touched experts' packed bytes, from
+    CUDA-graph replays of single calls that alternate between two layers of
+    weights (inputs larger than L2)."""
     from mxfp4_mixture_experts_gb300 import moe
     out = {}
     stream = torch.cuda.Stream()
-    for name in ("single32", "glm256", "widek256"):
-        sh = synth.SHAPES[name]
-        Ts = (1, 4, 16, 32) if name == "single32" else sh.tokens
+    for name in ("single32", "glm256", "widek256", "gptoss128_oai"):
+        oai = name.endswith("_oai")
+        sh = synth.SHAPES[name[:-4] if oai else name]
+        Ts = (1, 4, 16, 32) if name in ("single32", "gptoss128_oai") else sh.tokens
         layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev) for l in range(2)]
         res = {}
         for T in Ts:
@@ -429,13 +432,19 @@ def measure_configs(dev, hbm_gbs: float, reps: int = 10):
                 hidden, _, ids, w = synth.draw_activations(sh, T, rng)
                 x, ids, w = hidden.to(dev), ids.to(dev), w.to(dev)
                 y = torch.empty(T, sh.K, dtype=torch.bfloat16, device=dev)
-                args = (x, ids, w, w13, s13, w2, s2)
+                if oai:   # the gpt-oss form: the same bytes, interleaved rows, biases
+                    b13, b2 = (b.to(dev) for b in synth.draw_biases(sh, seed=0, layer=l))
+                    args = (x, ids, w, w13, s13, b13, w2, s2, b2)
+                    fwd = moe.forward_oai
+                else:
+                    args = (x, ids, w, w13, s13, w2, s2)
+                    fwd = moe.forward
                 with torch.cuda.stream(stream):
-                    moe.forward(*args, out=y, workspace=ws)
+                    fwd(*args, out=y, workspace=ws)
                 stream.synchronize()
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    moe.forward(*args, out=y, workspace=ws)
+                    fwd(*args, out=y, workspace=ws)
                 D = touched_experts(ids, sh.E)
                 calls.append((g, D * expert_bytes(sh.K, sh.I) + 4 * T * sh.K, D, args, y))
             times, bytes_ = [], []
@@ -460,6 +469,8 @@ def measure_configs(dev, hbm_gbs: float, reps: int = 10):
                            "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_gbs, 3)}
             del calls, ws
         out[name] = {"K": sh.K, "I": sh.I, "E": sh.E, "topk": sh.topk, "per_T": res}
+        if oai:
+            out[name]["form"] = "gpt-oss: interleaved gate/up rows, f32 biases, SwiGLU-OAI"
         del layers
         torch.cuda.empty_cache()
     return out

@@ -127,9 +127,8 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
  *   w2 / s2       as for mxfp4_moe_forward
  *   b2            fp32  [E, K]; each route adds its expert's b2 before the
  *                 routing weight, so a token gets sum_j w_tj * b2[e_tj]
- * Other arguments, limits and errors as mxfp4_moe_forward, except that this
- * form runs the decode path only: path 2, T > 32 or sizes the decode kernel
- * does not fit give MXFP4_MOE_ERR_SHAPE. b13 and b2 are device pointers, 4-byte
+ * Other arguments, paths (decode for T <= 32, else the tensor-core prefill),
+ * limits and errors as mxfp4_moe_forward. b13 and b2 are device pointers, 4-byte
  * aligned (MXFP4_MOE_ERR_ALIGN), non-NULL (MXFP4_MOE_ERR_ARG); the caller owns
  * every buffer. NaN in a pre-activation stays NaN (the cap and clamp do not
  * replace it). */

@@ -214,6 +214,43 @@ int run_decode(const void* hidden, const int32_t* topk_ids, const float* topk_we
   return MXFP4_MOE_OK;
 }
 
+// The prefill path (route, gather, two grouped GEMMs, combine) of both
+// forward forms.
+int run_prefill(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                const uint8_t* w13, const uint8_t* s13, const float* b13, const uint8_t* w2,
+                const uint8_t* s2, const float* b2, int T, int K, int I, int E, int topk,
+                void* out, int32_t* status, char* ws, const Layout& L, int oai, DeviceInfo* d,
+                cudaStream_t s) {
+  PrefillArgs p = {};
+  p.hidden = static_cast<const uint16_t*>(hidden);
+  p.ids = topk_ids;
+  p.wts = topk_weights;
+  p.w13 = w13;
+  p.s13 = s13;
+  p.w2 = w2;
+  p.s2 = s2;
+  p.T = T;
+  p.K = K;
+  p.I = I;
+  p.E = E;
+  p.topk = topk;
+  p.y = static_cast<uint16_t*>(out);
+  p.status = status;
+  p.count = reinterpret_cast<int32_t*>(ws + L.rcount);
+  p.offset = reinterpret_cast<int32_t*>(ws + L.roffset);
+  p.list = reinterpret_cast<int32_t*>(ws + L.rlist);
+  p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
+  p.P = reinterpret_cast<float*>(ws + L.P);
+  p.inv = reinterpret_cast<int32_t*>(ws + L.rinv);
+  p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
+  p.num_sms = d->num_sms;
+  p.b13 = b13;
+  p.b2 = b2;
+  p.oai = oai;
+  return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));
+}
+
 }  // namespace mxmoe
 
 extern "C" {
@@ -266,31 +303,8 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
     return run_decode(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
                       topk, out, status, ws, L, 0, d, s);
 
-  PrefillArgs p = {};
-  p.hidden = static_cast<const uint16_t*>(hidden);
-  p.ids = topk_ids;
-  p.wts = topk_weights;
-  p.w13 = w13;
-  p.s13 = s13;
-  p.w2 = w2;
-  p.s2 = s2;
-  p.T = T;
-  p.K = K;
-  p.I = I;
-  p.E = E;
-  p.topk = topk;
-  p.y = static_cast<uint16_t*>(out);
-  p.status = status;
-  p.count = reinterpret_cast<int32_t*>(ws + L.rcount);
-  p.offset = reinterpret_cast<int32_t*>(ws + L.roffset);
-  p.list = reinterpret_cast<int32_t*>(ws + L.rlist);
-  p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
-  p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
-  p.P = reinterpret_cast<float*>(ws + L.P);
-  p.inv = reinterpret_cast<int32_t*>(ws + L.rinv);
-  p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
-  p.num_sms = d->num_sms;
-  return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));
+  return run_prefill(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
+                     topk, out, status, ws, L, 0, d, s);
 }
 
 int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
@@ -310,15 +324,20 @@ int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const flo
   if (!aligned(workspace, 256)) return MXFP4_MOE_ERR_ALIGN;
   const Layout L = layout(T, K, I, E, topk);
   if (workspace_bytes < L.total) return MXFP4_MOE_ERR_WORKSPACE;
-  // the gpt-oss form runs the decode path only
-  if (path == 2 || T > kDecodeMaxT || T * topk > kDecodeMaxRoutes || K % 64 || I % 64)
+  const bool decode = path == 1 || (path == 0 && T <= kDecodeMaxT);
+  if (decode && (T > kDecodeMaxT || T * topk > kDecodeMaxRoutes || K % 64 || I % 64))
     return MXFP4_MOE_ERR_SHAPE;
+  if (!decode && (K % 64 || I % 64)) return MXFP4_MOE_ERR_SHAPE;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
-  if (!decode_fits(K, I, E, T, topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
-  return run_decode(hidden, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2, T, K, I, E, topk,
-                    out, status, static_cast<char*>(workspace), L, 1, d,
-                    static_cast<cudaStream_t>(stream));
+  if (decode && !decode_fits(K, I, E, T, topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (decode)
+    return run_decode(hidden, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2, T, K, I, E, topk,
+                      out, status, ws, L, 1, d, s);
+  return run_prefill(hidden, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2, T, K, I, E, topk,
+                     out, status, ws, L, 1, d, s);
 }
 
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,

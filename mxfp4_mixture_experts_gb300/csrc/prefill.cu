@@ -59,7 +59,10 @@ static_assert(kMaxTok % kXBox == 0 && kMaxTok % 16 == 0, "token boxes fill a sta
 
 struct GemmParams {
   CUtensorMap tmapX;   // tokens bf16 [R][kred], box {64, 128}, 128-byte swizzle
-  CUtensorMap tmapW;   // packed weights u8 [rows][kred/2], box {32, 64}
+  // packed weights: GEMM1 u8 {K/2 bytes, row groups, 2 halves (gate, up)}, box
+  // {32, 64, 2} (64 gate rows, then the 64 matching up rows); GEMM2 u8
+  // [rows][I/2], box {32, 64}
+  CUtensorMap tmapW;
   const uint8_t* wsc;  // scales u8 [rows][kred/32]
   const int32_t* count;
   const int32_t* offset;
@@ -69,6 +72,8 @@ struct GemmParams {
   float* P;            // GEMM2 output fp32 [R][K] (expert order, unweighted)
   int E, K, I, kred, NT;
   int32_t* status;
+  const float* bias;   // gpt-oss form: GEMM1 b13 [E][2I] (interleaved), GEMM2 b2 [E][K]
+  int oai;             // gpt-oss form: interleaved w13 rows, biases, SwiGLU-OAI
 };
 
 // Token chunks of one expert: nch chunks of cs tokens (cs a multiple of 16,
@@ -115,6 +120,7 @@ template <int PHASE>
 __device__ __forceinline__ int weight_row(int e, int nt, const GemmParams& p, int m) {
   if (PHASE == 1) {
     const int pr = packed_row<1>(m);
+    if (p.oai) return e * (2 * p.I) + 2 * (nt * 64 + (pr & 63)) + (pr >= 64 ? 1 : 0);
     return e * (2 * p.I) + (pr >= 64 ? p.I : 0) + nt * 64 + (pr & 63);
   }
   const int k = nt * kBM + m;
@@ -129,7 +135,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 // of fp32; the product is rounded to bf16 afterwards).
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
-template <int PHASE>
+// SwiGLU-OAI ("MXFP4 MoE decode kernels", Design, Fused epilogues) with the
+// same fast exponential and division: gate capped at 7, up clamped to
+// [-7, 7], gate * sigmoid(1.702 gate) * (up + 1); comparisons keep NaN.
+__device__ __forceinline__ float swiglu_oai_fast(float gate, float up) {
+  gate = gate > 7.0f ? 7.0f : gate;
+  up = up > 7.0f ? 7.0f : (up < -7.0f ? -7.0f : up);
+  return __fdividef(gate, 1.0f + __expf(-1.702f * gate)) * (up + 1.0f);
+}
+
+template <int PHASE, bool OAI>
 __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -214,17 +229,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     uint32_t pp = 0, ppar = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
       const TileId id = decode_tile(t, tile_base, p.count, E);
-      // GEMM1: 64 gate rows then the 64 matching up rows; GEMM2: 128 rows
-      // (past the matrix: other experts' rows or zeros, never stored)
-      const int r0 = PHASE == 1 ? id.e * 2 * p.I + id.nt * 64 : id.e * p.K + id.nt * kBM;
-      const int r1 = PHASE == 1 ? r0 + p.I : r0 + 64;
+      // GEMM1: 64 gate rows then the 64 matching up rows (one copy: row group
+      // e 2I + i of [gate; up], or pair e I + i of the interleaved rows);
+      // GEMM2: 128 rows (past the matrix: other experts' rows or zeros, never
+      // stored)
+      const int r0 = PHASE == 1 ? (OAI ? id.e * p.I : id.e * 2 * p.I) + id.nt * 64
+                                : id.e * p.K + id.nt * kBM;
       for (int kc = 0; kc < nK; ++kc) {
         if (kp >= kSP && !mbar_wait(&p_empty[sp], pp ^ 1u)) { fail = 2; break; }
         ppar = (ppar & ~(1u << sp)) | (pp << sp);
         mbar_arrive_expect_tx(&p_full[sp], kPStage);
-        tma_load_2d(sP + sp * kPStage, &p.tmapW, kc * (kBK / 2), r0, &p_full[sp]);
-        tma_load_2d(sP + sp * kPStage + kPBoxRows * (kBK / 2), &p.tmapW, kc * (kBK / 2), r1,
-                    &p_full[sp]);
+        if (PHASE == 1) {
+          tma_load_3d(sP + sp * kPStage, &p.tmapW, kc * (kBK / 2), r0, 0, &p_full[sp]);
+        } else {
+          tma_load_2d(sP + sp * kPStage, &p.tmapW, kc * (kBK / 2), r0, &p_full[sp]);
+          tma_load_2d(sP + sp * kPStage + kPBoxRows * (kBK / 2), &p.tmapW, kc * (kBK / 2),
+                      r0 + 64, &p_full[sp]);
+        }
         if (++sp == kSP) { sp = 0; pp ^= 1u; }
         ++kp;
       }
@@ -348,6 +369,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           const int g = 2 * q + s;
           const int i = id.nt * 64 + 8 * g + (lane >> 2);
           const uint32_t taddr = tmem + ((uint32_t)(16 * g) << 16);
+          float bg = 0.f, bu = 0.f;   // gpt-oss biases of pair i (interleaved order)
+          if (OAI) {
+            bg = p.bias[((size_t)id.e * p.I + i) * 2];
+            bu = p.bias[((size_t)id.e * p.I + i) * 2 + 1];
+          }
           const int n32 = (id.n + 31) >> 5, lo32 = (n32 + 1) >> 1;
 #pragma unroll 1
           for (int b = (half ? lo32 : 0) * 4; b < (half ? n32 : lo32) * 4; b += 4) {
@@ -358,8 +384,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
 #pragma unroll
               for (int x = 0; x < 2; ++x) {
                 const int n = (b + u) * 8 + 2 * (lane & 3) + x;
-                const float gt = __uint_as_float(v[u][x]), up = __uint_as_float(v[u][2 + x]);
-                if (n < id.n) p.hp[(size_t)(pos0 + n) * p.I + i] = f32_to_bf16_rne(silu_fast(gt) * up);
+                float gt = __uint_as_float(v[u][x]), up = __uint_as_float(v[u][2 + x]);
+                float hv;
+                if (OAI) {
+                  gt += bg;
+                  up += bu;
+                  hv = swiglu_oai_fast(gt, up);
+                } else {
+                  hv = silu_fast(gt) * up;
+                }
+                if (n < id.n) p.hp[(size_t)(pos0 + n) * p.I + i] = f32_to_bf16_rne(hv);
               }
             }
           }
@@ -367,6 +401,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
       } else {
         const int k = id.nt * kBM + q * 32 + lane;
         const bool kvalid = k < p.K;
+        // gpt-oss: the expert's w2 bias, weighted with the route in the combine
+        const float bk = (OAI && kvalid) ? p.bias[(size_t)id.e * p.K + k] : 0.f;
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
         const int n32 = (id.n + 31) >> 5, lo32 = (n32 + 1) >> 1;
 #pragma unroll 1
@@ -379,7 +415,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           if (kvalid) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < nv) dst[(size_t)j * p.K] = v[j];
+              if (j < nv) dst[(size_t)j * p.K] = v[j] + bk;
           }
         }
       }
@@ -468,18 +504,34 @@ static size_t gemm_smem_bytes(int E) {
 
 size_t prefill_counter_bytes(int, int, int, int, int) { return 256; }
 
-template <int PHASE>
-static cudaError_t launch_gemm(const GemmParams& gp, int num_sms, cudaStream_t stream) {
+template <int PHASE, bool OAI>
+static cudaError_t launch_gemm_form(const GemmParams& gp, int num_sms, cudaStream_t stream) {
   static size_t granted = 0;
   const size_t smem = gemm_smem_bytes(gp.E);
   if (smem > granted) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<PHASE>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<PHASE, OAI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     granted = smem;
   }
-  gemm_kernel<PHASE><<<num_sms, kPfThreads, smem, stream>>>(gp);
+  gemm_kernel<PHASE, OAI><<<num_sms, kPfThreads, smem, stream>>>(gp);
   return cudaGetLastError();
+}
+template <int PHASE>
+static cudaError_t launch_gemm(const GemmParams& gp, int num_sms, cudaStream_t stream) {
+  return gp.oai ? launch_gemm_form<PHASE, true>(gp, num_sms, stream)
+                : launch_gemm_form<PHASE, false>(gp, num_sms, stream);
+}
+
+// GEMM1's packed weights as row groups: {K/2 bytes, groups, 2 halves}, box
+// {32, 64, 2}. [gate; up]: group e 2I + i, the up half I rows later;
+// interleaved (gpt-oss): group e I + i (pair), the up half the next row.
+static bool encode_w13_groups(CUtensorMap* m, const PrefillArgs& a) {
+  const uint64_t rb = (uint64_t)a.K / 2;
+  const uint64_t dims[3] = {rb, a.oai ? (uint64_t)a.E * a.I : (uint64_t)a.E * 2 * a.I, 2};
+  const uint64_t strides[2] = {a.oai ? 2 * rb : rb, a.oai ? rb : (uint64_t)a.I * rb};
+  const uint32_t box[3] = {32, kPBoxRows, 2};
+  return encode_tiled_u8(m, a.w13, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* const* phase_events,
@@ -501,9 +553,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   GemmParams g1 = {};
   if (!encode_tiled_2d(&g1.tmapX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.xp, (uint64_t)a.K, (uint64_t)R,
                        (uint64_t)a.K * 2, kBK, kXBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tiled_2d(&g1.tmapW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w13, (uint64_t)a.K / 2,
-                       (uint64_t)a.E * 2 * a.I, (uint64_t)a.K / 2, 32, kPBoxRows,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
+      !encode_w13_groups(&g1.tmapW, a))
     return cudaErrorInvalidValue;
   g1.wsc = a.s13;
   g1.count = a.count;
@@ -518,6 +568,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   g1.kred = a.K;
   g1.NT = a.I / 64;   // 64 gate + 64 up rows a tile
   g1.status = a.status;
+  g1.bias = a.b13;
+  g1.oai = a.oai;
   if ((e = launch_gemm<1>(g1, a.num_sms, stream)) != cudaSuccess) return e;
   rec(2);
 
@@ -529,6 +581,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
                        CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   g2.wsc = a.s2;
+  g2.bias = a.b2;
   g2.kred = a.I;
   g2.NT = (a.K + kBM - 1) / kBM;   // K % 64 == 0: the last tile may hold 64 rows
   if ((e = launch_gemm<2>(g2, a.num_sms, stream)) != cudaSuccess) return e;

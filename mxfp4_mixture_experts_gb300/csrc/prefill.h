@@ -26,6 +26,11 @@ struct PrefillArgs {
   int32_t* inv;             // [R] route -> row of P
   int* counters;            // zero-kept scheduler counters
   int num_sms;
+  // gpt-oss form (oai != 0): w13 rows interleaved (row 2i gate i, row 2i + 1
+  // up i), f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI
+  const float* b13;
+  const float* b2;
+  int oai;
 };
 
 size_t prefill_counter_bytes(int T, int K, int I, int E, int topk);

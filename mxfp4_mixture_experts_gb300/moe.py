@@ -161,7 +161,7 @@ def forward_oai(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torc
                 status: Optional[torch.Tensor] = None, path: int = 0, stream=None) -> torch.Tensor:
     """The gpt-oss form: w13 rows interleaved (row 2i gate i, row 2i + 1 up i),
     f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI;
-    y[T, K] bf16 = sum_j w_tj * (W2[e] h + b2[e]). Decode path only (T <= 32)."""
+    y[T, K] bf16 = sum_j w_tj * (W2[e] h + b2[e]). Paths as forward()."""
     _need(hidden, "hidden", torch.bfloat16, 2)
     _need(topk_ids, "topk_ids", torch.int32, 2)
     _need(topk_weights, "topk_weights", torch.float32, 2)

@@ -133,8 +133,8 @@ def test_forward_oai_rejects_bad_arguments_without_a_gpu(L):
     assert fwd_oai(L, b2=VP(0x78001)) == m.ERR_ALIGN
     assert fwd_oai(L, w13=VP(0x40004)) == m.ERR_ALIGN
     assert fwd_oai(L, K=65) == m.ERR_SHAPE
-    assert fwd_oai(L, path=2) == m.ERR_SHAPE          # decode path only
-    assert fwd_oai(L, T=33, path=0) == m.ERR_SHAPE
+    assert fwd_oai(L, T=33, path=1) == m.ERR_SHAPE    # decode limited to 32 tokens
+    assert fwd_oai(L, K=96, I=96, T=40, path=2) == m.ERR_SHAPE   # prefill needs multiples of 64
     assert fwd_oai(L, K=96, I=64) == m.ERR_SHAPE
     assert fwd_oai(L, ws=None) == m.ERR_WORKSPACE
     need = L.mxfp4_moe_workspace_size(4, 64, 64, 4, 2)

@@ -1,11 +1,12 @@
-"""The gpt-oss form of the decode path ("MXFP4 MoE decode kernels", Design:
+"""The gpt-oss form of the layer ("MXFP4 MoE decode kernels", Design:
 interleaved gate/up rows, f32 biases, SwiGLU-OAI, routing-weighted w2 bias per
-route) vs the CPU oracle's forward_oai.
+route) on the decode and prefill paths vs the CPU oracle's forward_oai.
 
 Small shapes span several row tiles, a ragged last stage, several token groups
-and rows read from the global scratch, compared on every output element; the
+and rows read from the global scratch (decode), one and several m-tiles per
+expert and a half w2 tile (prefill), compared on every output element; the
 gpt-oss-120b layer (K = I = 2880, 128 experts, top-4) runs at full size on
-sampled tokens."""
+sampled tokens on both paths."""
 import numpy as np
 import pytest
 import torch
@@ -161,4 +162,65 @@ def test_oai_gptoss128_full_size_sampled_tokens(moe, T):
     assert int(status[1]) == len(rt["touched"])
     gate(y, case, sorted({0, T - 1}), biases=b)
     del w13, s13, w2, s2
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------
+# the gpt-oss form on the prefill path (tensor-core grouped GEMMs)
+# ---------------------------------------------------------------------------
+def run_oai_path(moe, case, biases, path):
+    g = case.to("cuda")
+    b13, b2 = (b.to("cuda") for b in biases)
+    status = torch.zeros(4, dtype=torch.int32, device="cuda")
+    y = moe.forward_oai(g.hidden, g.topk_ids, g.topk_weights, g.w13, g.s13, b13, g.w2, g.s2, b2,
+                        status=status, path=path)
+    torch.cuda.synchronize()
+    assert int(status[2]) == 0, f"a bounded wait inside a kernel gave up: {int(status[2]):#x}"
+    return y
+
+
+@pytest.mark.parametrize("K,I,E,k,T", [
+    (256, 128, 8, 3, 50),       # one m-tile per expert
+    (384, 192, 4, 2, 300),      # a ragged second m-tile
+    (192, 64, 2, 1, 700),       # K % 128 == 64: a half w2 tile
+    (2880, 2880, 4, 2, 40),     # the gpt-oss-120b expert shape
+])
+def test_oai_prefill_all_elements(moe, K, I, E, k, T):
+    shape = synth.custom_shape(K=K, I=I, E=E, topk=k)
+    case = synth.make_case(shape, T, seed=3 * K + I + T)
+    b = synth.draw_biases(shape, seed=K + T)
+    gate(run_oai_path(moe, case, b, 2), case, biases=b)
+
+
+def test_oai_prefill_and_decode_agree(moe):
+    """Both paths on the same 32 tokens meet the gate against the oracle and
+    lie within twice the gate of each other."""
+    shape = synth.custom_shape(512, 256, 16, 4)
+    case = synth.make_case(shape, 32, seed=270)
+    b = synth.draw_biases(shape, seed=70)
+    yd = run_oai_path(moe, case, b, 1).float()
+    yp = run_oai_path(moe, case, b, 2)
+    gate(yp, case, biases=b)
+    yp = yp.float()
+    assert (torch.linalg.norm(yd - yp) / torch.linalg.norm(yd)).item() <= 2 * 3e-3
+
+
+def test_oai_auto_path_above_32_tokens(moe):
+    shape = synth.custom_shape(K=256, I=128, E=8, topk=3)
+    case = synth.make_case(shape, 40, seed=280)
+    b = synth.draw_biases(shape, seed=80)
+    gate(run_oai_path(moe, case, b, 0), case, biases=b)
+
+
+def test_oai_prefill_gptoss128_full_size_sampled_tokens(moe):
+    shape = synth.SHAPES["gptoss128"]
+    T = 2048
+    hidden, logits, ids, w = synth.draw_activations(shape, T, np.random.Generator(np.random.PCG64(T)))
+    w13, s13, w2, s2 = synth.draw_weights_cuda(shape, seed=0, layer=0)
+    case = synth.Case(shape, T, hidden, ids, w, w13, s13, w2, s2, logits)
+    b = synth.draw_biases(shape, seed=0)
+    y = run_oai_path(moe, case, b, 0)
+    assert torch.isfinite(y).all()
+    gate(y, case, [0, 1023, 2047], biases=b)
+    del case, w13, s13, w2, s2
     torch.cuda.empty_cache()
