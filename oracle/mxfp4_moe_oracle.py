@@ -204,6 +204,42 @@ def forward(hidden_bits, topk_ids, topk_weights, w13, s13, w2, s2,
     return y
 
 
+# --- the router (logits -> top-k ids and weights) ------------------------------
+def topk_route(logits, topk: int, scoring: str, bias=None):
+    """Router step before routing/permute ("MXFP4 MoE decode kernels",
+    Design, "Routing inside the kernel" consumes its top-k ids; the workload
+    shapes fix the scoring: top-k softmax for the gpt-oss shapes, sigmoid
+    scores renormalised over the chosen k for the GLM shapes, an optional
+    per-expert bias added to the logits).
+
+    x = float32(logit + bias) (one float32 addition per element, so both
+    sides of a comparison take the selection decision on the same values);
+    the k largest x in order, ties to the lower expert index (sigmoid is
+    increasing, so this is the top-k by sigmoid score). Weights in float64:
+    softmax over the chosen x ("softmax_topk"), or sigmoid(x) of the chosen
+    divided by their sum ("sigmoid_renorm").
+    Returns ids int32 [T, k] and weights float64 [T, k]."""
+    x = np.asarray(logits, dtype=np.float32)
+    if bias is not None:
+        x = (x + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    T, E = x.shape
+    ids = np.empty((T, topk), dtype=np.int32)
+    for t in range(T):
+        # stable sort on -x: equal values keep ascending expert order
+        order = sorted(range(E), key=lambda e: (-float(x[t, e]), e))
+        ids[t] = order[:topk]
+    chosen = np.take_along_axis(x, ids.astype(np.int64), axis=1).astype(np.float64)
+    if scoring == "softmax_topk":
+        z = np.exp(chosen - chosen.max(axis=1, keepdims=True))
+        w = z / z.sum(axis=1, keepdims=True)
+    elif scoring == "sigmoid_renorm":
+        sc = 1.0 / (1.0 + np.exp(-chosen))
+        w = sc / sc.sum(axis=1, keepdims=True)
+    else:
+        raise ValueError(scoring)
+    return ids, w
+
+
 # --- the gpt-oss form ---------------------------------------------------------
 OAI_GATE_CAP = 7.0      # gate capped above at 7
 OAI_UP_CLAMP = 7.0      # up clamped to [-7, 7]
