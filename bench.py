@@ -476,6 +476,43 @@ def measure_configs(dev, hbm_gbs: float, reps: int = 10):
     return out
 
 
+def measure_router(dev, reps: int = 20):
+    """The router step (logits -> top-k ids and weights) at the gpt-oss decode
+    size (T = 32, E = 128, top-4 softmax) and the prefill chunk (T = 8192,
+    E = 256, top-8 sigmoid): microseconds per call from CUDA-graph replays of
+    single calls with events around each replay."""
+    from mxfp4_mixture_experts_gb300 import moe
+    stream = torch.cuda.Stream()
+    out = {}
+    for name, T, E, k, scoring in (("gptoss128_t32", 32, 128, 4, "softmax_topk"),
+                                   ("prefill256_t8192", 8192, 256, 8, "sigmoid_renorm")):
+        g = torch.Generator(device=dev).manual_seed(T + E)
+        logits = torch.randn(T, E, device=dev, generator=g)
+        ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            moe.router(logits, k, scoring, topk_ids=ids, topk_weights=w)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            moe.router(logits, k, scoring, topk_ids=ids, topk_weights=w)
+        times = []
+        with torch.cuda.stream(stream):
+            for r in range(reps + 3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                stream.synchronize()
+                if r >= 3:
+                    times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        out[name] = {"T": T, "E": E, "topk": k, "scoring": scoring, "us": round(ms * 1000, 2),
+                     "logit_bytes": 4 * T * E}
+    return out
+
+
 # ---------------------------------------------------------------------------
 def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     """Headline timing: each step is captured once as a CUDA graph (two graphs
@@ -709,6 +746,7 @@ def run_ours(args, dist: Dist):
     torch.cuda.empty_cache()
     if not args.no_configs:
         out["configs"] = measure_configs(dev, hbm)
+        out["router"] = measure_router(dev)
     if not args.no_prefill:
         pf = run_prefill(args, dist, 10, 3, False)
         out["prefill"] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "config",

@@ -94,6 +94,26 @@ int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E,
                     int32_t* expert_count, int32_t* expert_offset, int32_t* route_list,
                     int32_t* status, void* stream);
 
+/* Router: the step before routing ("MXFP4 MoE decode kernels", Design, "Routing
+ * inside the kernel" takes its top-k ids; the workload shapes fix the
+ * scoring). Per token t:
+ *   x_e = fp32(logits[t][e] + bias[e])   (bias may be NULL: x_e = logits[t][e];
+ *                                          a NaN x ranks as -inf)
+ *   topk_ids[t][0..k-1]  the k largest x in descending order, ties to the
+ *                        lower expert index (sigmoid is increasing, so this is
+ *                        also the top-k by sigmoid score)
+ *   topk_weights[t][j]   scoring 0 ("softmax_topk"): exp(x_j - x_0) / sum over
+ *                        the chosen; scoring 1 ("sigmoid_renorm"): sigmoid(x_j)
+ *                        / sum of the chosen sigmoids; fp32
+ *   logits fp32 [T, E], bias fp32 [E] or NULL, topk_ids int32 [T, k],
+ *   topk_weights fp32 [T, k]: device pointers owned by the caller, 4-byte
+ *   aligned (MXFP4_MOE_ERR_ALIGN). Limits: 1 <= E <= 1024, 1 <= k <= min(32, E),
+ *   0 <= T (MXFP4_MOE_ERR_SHAPE); scoring 0 or 1 and non-NULL logits/outputs
+ *   (MXFP4_MOE_ERR_ARG). T == 0 enqueues nothing. The outputs feed
+ *   mxfp4_moe_forward directly. */
+int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int topk, int scoring,
+                     int32_t* topk_ids, float* topk_weights, void* stream);
+
 /* The MoE layer, y = sum_j w_tj * W2[e] silu(W_gate[e] x) * (W_up[e] x).
  *   hidden        bf16  [T, K]
  *   topk_ids      int32 [T, topk]   (negative = padding, >= E = invalid, both skipped)

@@ -340,6 +340,22 @@ int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const flo
                      out, status, ws, L, 1, d, s);
 }
 
+int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int topk, int scoring,
+                     int32_t* topk_ids, float* topk_weights, void* stream) {
+  if (T < 0 || E < 1 || E > kRouterMaxExperts || topk < 1 || topk > 32 || topk > E)
+    return MXFP4_MOE_ERR_SHAPE;
+  if (scoring != 0 && scoring != 1) return MXFP4_MOE_ERR_ARG;
+  if (T == 0) return MXFP4_MOE_OK;
+  if (!logits || !topk_ids || !topk_weights) return MXFP4_MOE_ERR_ARG;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
+      (bias != nullptr && !aligned(bias, 4)))
+    return MXFP4_MOE_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  return cuda_status(launch_router(logits, bias, T, E, topk, scoring, topk_ids, topk_weights,
+                                   d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
                       void* stream) {
   if (rows < 0 || cols < 0) return MXFP4_MOE_ERR_ARG;

@@ -71,6 +71,14 @@ bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t*
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);
 
+constexpr int kRouterMaxExperts = 1024;   // 32 per lane of one warp
+
+// Router: logits fp32 [T, E] (+ bias [E] or null) -> top-k ids int32 [T, k]
+// and weights fp32 [T, k]; scoring 0 = softmax over the chosen k, 1 = sigmoid
+// renormalised over the chosen k (router.cu).
+cudaError_t launch_router(const float* logits, const float* bias, int T, int E, int topk,
+                          int scoring, int32_t* ids, float* wts, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
                            uint16_t* out, int num_sms, cudaStream_t stream);
 

@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_forward_oai.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                         i32, vp, vp, vp, sz, i32, vp]
     L.mxfp4_moe_forward_oai.restype = i32
+    L.mxfp4_moe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+    L.mxfp4_moe_router.restype = i32
     L.mxfp4_moe_dequant.argtypes = [vp, vp, i32, i32, vp, vp]
     L.mxfp4_moe_dequant.restype = i32
     L.mxfp4_moe_set_phase_events.argtypes = [vp, i32]
@@ -194,6 +196,34 @@ def forward_oai(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torc
     if rc:
         raise MoEError(rc, "mxfp4_moe_forward_oai")
     return out
+
+
+SCORING = {"softmax_topk": 0, "sigmoid_renorm": 1}
+
+
+def router(logits: torch.Tensor, topk: int, scoring: str = "softmax_topk",
+           bias: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
+           topk_weights: Optional[torch.Tensor] = None, stream=None):
+    """Top-k experts of fp32 logits [T, E] (+ bias [E]) and their weights:
+    int32 [T, k] ids (descending x = logit + bias, ties to the lower index)
+    and fp32 [T, k] weights (softmax over the chosen, or renormalised sigmoid)."""
+    _need(logits, "logits", torch.float32, 2)
+    T, E = logits.shape
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+        if bias.shape[0] != E:
+            raise ValueError("bias must be [E]")
+    if scoring not in SCORING:
+        raise ValueError(f"scoring must be one of {sorted(SCORING)}")
+    if topk_ids is None:
+        topk_ids = torch.empty(T, topk, dtype=torch.int32, device=logits.device)
+    if topk_weights is None:
+        topk_weights = torch.empty(T, topk, dtype=torch.float32, device=logits.device)
+    rc = lib().mxfp4_moe_router(_ptr(logits), _ptr(bias), T, E, topk, SCORING[scoring],
+                                _ptr(topk_ids), _ptr(topk_weights), _stream(stream))
+    if rc:
+        raise MoEError(rc, "mxfp4_moe_router")
+    return topk_ids, topk_weights
 
 
 def dequant(packed: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:

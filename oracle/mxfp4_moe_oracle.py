@@ -213,7 +213,8 @@ def topk_route(logits, topk: int, scoring: str, bias=None):
     per-expert bias added to the logits).
 
     x = float32(logit + bias) (one float32 addition per element, so both
-    sides of a comparison take the selection decision on the same values);
+    sides of a comparison take the selection decision on the same values;
+    a NaN ranks as -inf);
     the k largest x in order, ties to the lower expert index (sigmoid is
     increasing, so this is the top-k by sigmoid score). Weights in float64:
     softmax over the chosen x ("softmax_topk"), or sigmoid(x) of the chosen
@@ -222,6 +223,7 @@ def topk_route(logits, topk: int, scoring: str, bias=None):
     x = np.asarray(logits, dtype=np.float32)
     if bias is not None:
         x = (x + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+    x = np.where(np.isnan(x), np.float32(-np.inf), x)   # NaN ranks as -inf
     T, E = x.shape
     ids = np.empty((T, topk), dtype=np.int32)
     for t in range(T):

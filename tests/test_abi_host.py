@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxfp4_moe_route", "mxfp4_moe_forward", "mxfp4_moe_forward_oai", "mxfp4_moe_dequant",
+    for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
+              "mxfp4_moe_dequant",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
         assert n in names
 
@@ -140,6 +141,28 @@ def test_forward_oai_rejects_bad_arguments_without_a_gpu(L):
     need = L.mxfp4_moe_workspace_size(4, 64, 64, 4, 2)
     assert fwd_oai(L, ws_bytes=need - 1) == m.ERR_WORKSPACE
     assert fwd_oai(L, T=0) == m.OK
+
+
+def test_router_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    R = L.mxfp4_moe_router
+    ok = dict(lg=VP(0x1000), b=None, T=4, E=64, k=4, sc=0, ids=VP(0x2000), w=VP(0x3000))
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return R(a["lg"], a["b"], a["T"], a["E"], a["k"], a["sc"], a["ids"], a["w"], None)
+    assert call(E=0) == m.ERR_SHAPE
+    assert call(E=1025) == m.ERR_SHAPE
+    assert call(k=0) == m.ERR_SHAPE
+    assert call(k=33, E=64) == m.ERR_SHAPE
+    assert call(k=9, E=8) == m.ERR_SHAPE
+    assert call(T=-1) == m.ERR_SHAPE
+    assert call(sc=2) == m.ERR_ARG
+    assert call(lg=None) == m.ERR_ARG
+    assert call(ids=None) == m.ERR_ARG
+    assert call(w=VP(0x3002)) == m.ERR_ALIGN
+    assert call(b=VP(0x4001)) == m.ERR_ALIGN
+    assert call(T=0) == m.OK
 
 
 def test_route_and_dequant_reject_bad_arguments(L):
