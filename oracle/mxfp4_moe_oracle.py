@@ -204,6 +204,62 @@ def forward(hidden_bits, topk_ids, topk_weights, w13, s13, w2, s2,
     return y
 
 
+# --- the encoder (bf16 -> E2M1 codes + E8M0 scales) ----------------------------
+def encode_block(v, rule: str):
+    """One block of 32 values (float64, exact bf16 values) -> (32 codes, scale
+    byte). ("GLM-5.2 and GLM-5.3 (744B) in MXFP4 on Gaudi 2", What was built,
+    "MXFP4 encoder": the OCP shared exponent X = floor(log2(amax)) - 2; the
+    Quark rule raises X by one when amax / 2^X >= 7.)
+    X is clamped to [-127, 127] (an all-zero block gets X = -127, byte 0); a
+    block with a NaN or infinite value gets byte 255 (NaN) and codes 0. Each
+    element: q = v / 2^X, the nearest E2M1 magnitude to |q| found by search
+    over the 8 magnitudes (|q| > 6 gives 6), ties to the even mantissa (code
+    bit 0 clear), and the sign bit of v (-0 stays -0)."""
+    v = np.asarray(v, dtype=np.float64)
+    if not np.all(np.isfinite(v)):
+        return np.zeros(v.shape, dtype=np.uint8), 255
+    amax = float(np.max(np.abs(v)))
+    if amax == 0.0:
+        X = -127
+    else:
+        m, e = math.frexp(amax)            # amax = m 2^e, m in [0.5, 1)
+        X = max(e - 1 - 2, -127)           # floor(log2(amax)) - 2
+        if rule == "quark" and amax / 2.0 ** X >= 7.0:
+            X += 1
+        elif rule not in ("ocp", "quark"):
+            raise ValueError(rule)
+        X = min(X, 127)
+    codes = np.empty(v.shape, dtype=np.uint8)
+    for i, x in enumerate(v.tolist()):
+        q = abs(x) / 2.0 ** X
+        best = None
+        for c in range(8):
+            d = abs(q - E2M1_TABLE[c])
+            if best is None or d < best[0] or (d == best[0] and (c & 1) == 0):
+                best = (d, c)
+        codes[i] = best[1] | (8 if math.copysign(1.0, x) < 0 else 0)
+    return codes, X + 127
+
+
+def encode(hidden_bits, rule: str = "ocp"):
+    """bf16 bit patterns uint16 [rows, cols] (cols % 32 == 0) -> packed uint8
+    [rows, cols/2] (value 2i in the low nibble of byte i) and scales uint8
+    [rows, cols/32], block by block with ``encode_block``."""
+    x = bf16_bits_to_float(hidden_bits)
+    rows, cols = x.shape
+    if cols % SCALE_BLOCK:
+        raise ValueError("cols must be a multiple of 32")
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scale = np.empty((rows, cols // SCALE_BLOCK), dtype=np.uint8)
+    for r in range(rows):
+        for b in range(cols // SCALE_BLOCK):
+            c, s = encode_block(x[r, SCALE_BLOCK * b:SCALE_BLOCK * (b + 1)], rule)
+            codes[r, SCALE_BLOCK * b:SCALE_BLOCK * (b + 1)] = c
+            scale[r, b] = s
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scale
+
+
 # --- the router (logits -> top-k ids and weights) ------------------------------
 def topk_route(logits, topk: int, scoring: str, bias=None):
     """Router step before routing/permute ("MXFP4 MoE decode kernels",
