@@ -513,6 +513,47 @@ def measure_router(dev, reps: int = 20):
     return out
 
 
+def measure_encode(dev, hbm_gbs: float, reps: int = 10):
+    """The MXFP4 encoder on the w13 rows of 16 gpt-oss-120b experts (bf16
+    [16 x 5760, 2880], N(0, 0.02), 531 MB in; larger than L2): microseconds
+    per call from CUDA-graph replays with events around each replay, and GB/s
+    of its algorithmic bytes (2 + 17/32 per value: bf16 in, codes and scales
+    out) against the measured copy bandwidth."""
+    from mxfp4_mixture_experts_gb300 import moe
+    stream = torch.cuda.Stream()
+    rows, cols = 16 * 5760, 2880
+    g = torch.Generator(device=dev).manual_seed(64)
+    x = (0.02 * torch.randn(rows, cols, device=dev, generator=g)).to(torch.bfloat16)
+    out = {"rows": rows, "cols": cols}
+    for rule in ("ocp", "quark"):
+        with torch.cuda.stream(stream):
+            moe.encode(x, rule)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            moe.encode(x, rule)
+        times = []
+        with torch.cuda.stream(stream):
+            for r in range(reps + 3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+                stream.synchronize()
+                if r >= 3:
+                    times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        alg = rows * cols * (2 + 17 / 32)
+        out[rule] = {"us": round(ms * 1000, 1), "alg_bytes": int(alg),
+                     "gbs": round(alg / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured": round(alg / (ms * 1e-3) / 1e9 / hbm_gbs, 3)}
+        del graph
+    del x
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     """Headline timing: each step is captured once as a CUDA graph (two graphs
@@ -747,6 +788,7 @@ def run_ours(args, dist: Dist):
     if not args.no_configs:
         out["configs"] = measure_configs(dev, hbm)
         out["router"] = measure_router(dev)
+        out["encode"] = measure_encode(dev, hbm)
     if not args.no_prefill:
         pf = run_prefill(args, dist, 10, 3, False)
         out["prefill"] = {k: pf[k] for k in ("value", "unit", "ms_per_step", "config",

@@ -189,6 +189,21 @@ int mxfp4_moe_forward_noalloc(const void* hidden, const int32_t* topk_ids,
                               int T, int K, int I, int E, int topk,
                               void* out, int32_t* status, int path, void* stream);
 
+/* MXFP4 encoder ("GLM-5.2 and GLM-5.3 (744B) in MXFP4 on Gaudi 2", What was
+ * built, "MXFP4 encoder"): bf16 rows -> the packed form the forward calls read.
+ *   x       bf16  [rows, cols], cols % 32 == 0 (MXFP4_MOE_ERR_SHAPE), 16-byte aligned
+ *   packed  uint8 [rows, cols/2]  value 2i in the low nibble of byte i, 4-byte aligned
+ *   scale   uint8 [rows, cols/32] E8M0
+ *   rule    0 = OCP: per 32-value block X = floor(log2(amax)) - 2;
+ *           1 = Quark: the same, raised by one when amax / 2^X >= 7
+ * X is clamped to [-127, 127] (an all-zero block gets byte 0); a block with a
+ * NaN or infinite value gets byte 255 and codes 0. Each element v / 2^X is
+ * rounded to the nearest E2M1 value, ties to the even code, saturating at 6,
+ * keeping its sign (-0 stays -0). Device pointers owned by the caller;
+ * rows == 0 enqueues nothing. */
+int mxfp4_moe_encode(const void* x, int rows, int cols, int rule, uint8_t* packed,
+                     uint8_t* scale, void* stream);
+
 /* Dequantise packed rows to bf16 ("MXFP4 MoE decode kernels", Prefill:
  * mxk_deq unpacks an expert's MXFP4 weights straight to bf16).
  *   packed uint8 [rows, cols/2], scale uint8 [rows, cols/32] -> out bf16 [rows, cols]

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmxfp4_moe.so")
-SOURCES = ["api.cu", "route.cu", "router.cu", "decode.cu", "dequant.cu", "prefill.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "router.cu", "decode.cu", "dequant.cu", "encode.cu", "prefill.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                 "-I" + INCLUDE, "-I" + CSRC]

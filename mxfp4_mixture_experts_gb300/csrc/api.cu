@@ -356,6 +356,19 @@ int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int t
                                    d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+int mxfp4_moe_encode(const void* x, int rows, int cols, int rule, uint8_t* packed,
+                     uint8_t* scale, void* stream) {
+  if (rows < 0 || cols < 32 || cols % 32) return MXFP4_MOE_ERR_SHAPE;
+  if (rule != 0 && rule != 1) return MXFP4_MOE_ERR_ARG;
+  if (rows == 0) return MXFP4_MOE_OK;
+  if (!x || !packed || !scale) return MXFP4_MOE_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(packed, 4)) return MXFP4_MOE_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  return cuda_status(launch_encode(static_cast<const uint16_t*>(x), rows, cols, rule, packed, scale,
+                                   d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
                       void* stream) {
   if (rows < 0 || cols < 0) return MXFP4_MOE_ERR_ARG;

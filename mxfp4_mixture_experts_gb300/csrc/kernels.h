@@ -71,6 +71,12 @@ bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t*
 cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
                          int32_t* list, int32_t* status, cudaStream_t stream);
 
+// MXFP4 encoder: bf16 [rows, cols] (cols % 32 == 0) -> packed [rows, cols/2]
+// and E8M0 scales [rows, cols/32]; quark != 0 takes the Quark exponent rule
+// (encode.cu).
+cudaError_t launch_encode(const uint16_t* x, int64_t rows, int64_t cols, int quark,
+                          uint8_t* packed, uint8_t* scale, int num_sms, cudaStream_t stream);
+
 constexpr int kRouterMaxExperts = 1024;   // 32 per lane of one warp
 
 // Router: logits fp32 [T, E] (+ bias [E] or null) -> top-k ids int32 [T, k]

@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_forward_oai.restype = i32
     L.mxfp4_moe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.mxfp4_moe_router.restype = i32
+    L.mxfp4_moe_encode.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+    L.mxfp4_moe_encode.restype = i32
     L.mxfp4_moe_dequant.argtypes = [vp, vp, i32, i32, vp, vp]
     L.mxfp4_moe_dequant.restype = i32
     L.mxfp4_moe_set_phase_events.argtypes = [vp, i32]
@@ -224,6 +226,26 @@ def router(logits: torch.Tensor, topk: int, scoring: str = "softmax_topk",
     if rc:
         raise MoEError(rc, "mxfp4_moe_router")
     return topk_ids, topk_weights
+
+
+RULES = {"ocp": 0, "quark": 1}
+
+
+def encode(x: torch.Tensor, rule: str = "ocp", stream=None):
+    """bf16 [rows, cols] -> (packed uint8 [rows, cols/2], E8M0 scales uint8
+    [rows, cols/32]); rule "ocp" (floor(log2 amax) - 2) or "quark" (raised by
+    one when amax / 2^X >= 7)."""
+    _need(x, "x", torch.bfloat16, 2)
+    if rule not in RULES:
+        raise ValueError(f"rule must be one of {sorted(RULES)}")
+    rows, cols = x.shape
+    packed = torch.empty(rows, cols // 2, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(rows, cols // 32, dtype=torch.uint8, device=x.device)
+    rc = lib().mxfp4_moe_encode(_ptr(x), rows, cols, RULES[rule], _ptr(packed), _ptr(scale),
+                                _stream(stream))
+    if rc:
+        raise MoEError(rc, "mxfp4_moe_encode")
+    return packed, scale
 
 
 def dequant(packed: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:

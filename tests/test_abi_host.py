@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
-              "mxfp4_moe_dequant",
+              "mxfp4_moe_dequant", "mxfp4_moe_encode",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
         assert n in names
 
@@ -163,6 +163,20 @@ def test_router_rejects_bad_arguments_without_a_gpu(L):
     assert call(w=VP(0x3002)) == m.ERR_ALIGN
     assert call(b=VP(0x4001)) == m.ERR_ALIGN
     assert call(T=0) == m.OK
+
+
+def test_encode_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    enc = L.mxfp4_moe_encode
+    assert enc(VP(0x1000), 4, 48, 0, VP(0x2000), VP(0x3000), None) == m.ERR_SHAPE
+    assert enc(VP(0x1000), 4, 16, 0, VP(0x2000), VP(0x3000), None) == m.ERR_SHAPE
+    assert enc(VP(0x1000), -1, 64, 0, VP(0x2000), VP(0x3000), None) == m.ERR_SHAPE
+    assert enc(VP(0x1000), 4, 64, 2, VP(0x2000), VP(0x3000), None) == m.ERR_ARG
+    assert enc(None, 4, 64, 0, VP(0x2000), VP(0x3000), None) == m.ERR_ARG
+    assert enc(VP(0x1000), 4, 64, 1, VP(0x2000), None, None) == m.ERR_ARG
+    assert enc(VP(0x1008), 4, 64, 0, VP(0x2000), VP(0x3000), None) == m.ERR_ALIGN
+    assert enc(VP(0x1000), 4, 64, 0, VP(0x2002), VP(0x3000), None) == m.ERR_ALIGN
+    assert enc(VP(0x1000), 0, 64, 0, VP(0x2000), VP(0x3000), None) == m.OK
 
 
 def test_route_and_dequant_reject_bad_arguments(L):
