@@ -360,6 +360,42 @@ def forward_oai(hidden_bits, topk_ids, topk_weights, w13, s13, b13, w2, s2, b2,
     return y
 
 
+# --- expert-parallel window and per-route outputs --------------------------------
+def forward_window(hidden_bits, topk_ids, topk_weights, w13, s13, w2, s2, expert_base: int = 0,
+                   per_route: bool = False, intermediate: str = "bf16"):
+    """The layer over a window of experts, optionally per route ("MXFP4 MoE
+    decode kernels", Design, "Routing inside the kernel": routes to experts on
+    other expert-parallel ranks are skipped; Beyond gpt-oss: mxk_w2xr, a
+    per-route w2 output for models that apply a per-route operation before the
+    token sum).
+
+    The weights hold the E experts with global ids expert_base .. expert_base
+    + E - 1; a route whose id lies outside that window is skipped (it adds
+    nothing and is not counted as invalid). per_route=False: y [T, K], the sum
+    over the window's routes of w_tj o_(t,j). per_route=True: o [T*k, K], row
+    t*k + j = W2[e] h of route (t, j), unweighted, zero for skipped routes."""
+    ids = np.asarray(topk_ids).astype(np.int64)
+    E = w13.shape[0]
+    local = ids - expert_base
+    inside = (local >= 0) & (local < E)
+    # the window's routes only; everything else becomes padding (-1)
+    local_ids = np.where(inside, local, -1).astype(np.int32)
+    if not per_route:
+        return forward(hidden_bits, local_ids, topk_weights, w13, s13, w2, s2, intermediate)
+    T, k = ids.shape
+    K = w2.shape[1]
+    out = np.zeros((T * k, K), dtype=np.float64)
+    for j in range(k):
+        # slot j alone with weight 1 is route (t, j)'s output
+        ids_j = np.full((T, k), -1, dtype=np.int32)
+        ids_j[:, j] = local_ids[:, j]
+        ones = np.zeros((T, k), dtype=np.float32)
+        ones[:, j] = 1.0
+        out[np.arange(T) * k + j] = forward(hidden_bits, ids_j, ones, w13, s13, w2, s2,
+                                            intermediate)
+    return out
+
+
 def touched_bytes(topk_ids, E: int, K: int, I: int) -> int:
     """Algorithmic HBM bytes of one call: packed bytes + scales of each touched
     expert read once (3*I*K*(1/2 + 1/32) per expert)."""
