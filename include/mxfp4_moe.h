@@ -135,6 +135,32 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
                       void* workspace, size_t workspace_bytes,
                       int path, void* stream);
 
+/* The layer over an expert-parallel window, optionally per route ("MXFP4 MoE
+ * decode kernels", Design, "Routing inside the kernel": routes to experts on
+ * other expert-parallel ranks are skipped and cost nothing; Beyond gpt-oss:
+ * mxk_w2xr, a per-route w2 output for models that apply a per-route operation
+ * before the token sum).
+ *   w13/s13/w2/s2 hold the E local experts, global ids expert_base ..
+ *                 expert_base + E - 1 (expert_base >= 0); a route whose id lies
+ *                 outside that window is skipped silently (no status count)
+ *   per_route 0   out bf16 [T, K]: y_t = sum over the window's routes of
+ *                 w_tj * W2[e] h (this rank's part of the token sums)
+ *   per_route 1   out bf16 [T * topk, K]: row t * topk + j = W2[e] h of route
+ *                 (t, j), unweighted (topk_weights may be NULL), zero rows for
+ *                 skipped routes
+ * Everything else (paths, limits, alignment, workspace, errors) as
+ * mxfp4_moe_forward; path, per_route or expert_base out of range give
+ * MXFP4_MOE_ERR_ARG. */
+int mxfp4_moe_forward_window(const void* hidden, const int32_t* topk_ids,
+                             const float* topk_weights,
+                             const uint8_t* w13, const uint8_t* s13,
+                             const uint8_t* w2, const uint8_t* s2,
+                             int T, int K, int I, int E, int topk,
+                             int expert_base, int per_route,
+                             void* out, int32_t* status,
+                             void* workspace, size_t workspace_bytes,
+                             int path, void* stream);
+
 /* The gpt-oss form of the layer ("MXFP4 MoE decode kernels", Design, "Read
  * the served layout" and "Fused epilogues"):
  *   y_t = sum_j w_tj * (W2[e] h + b2[e]),  h = SwiGLU-OAI(W_gate[e] x + b_gate[e],

@@ -147,12 +147,20 @@ bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t*
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
+// Which routes a forward call computes and what it writes: an expert window
+// (ids outside [ebase, ebase + E) skipped, not counted as invalid) and the
+// per-route output (y [T * topk, K], unweighted) instead of the token sums.
+struct RouteMode {
+  int ebase = 0, window = 0, per_route = 0;
+};
+
 // The decode path (one cooperative launch) of both forward forms: tensor maps
 // over the packed weights, then the kernel.
 int run_decode(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
                const uint8_t* w13, const uint8_t* s13, const float* b13, const uint8_t* w2,
                const uint8_t* s2, const float* b2, int T, int K, int I, int E, int topk, void* out,
-               int32_t* status, char* ws, const Layout& L, int oai, DeviceInfo* d, cudaStream_t s) {
+               int32_t* status, char* ws, const Layout& L, int oai, DeviceInfo* d, cudaStream_t s,
+               RouteMode rm = RouteMode()) {
   DecodeArgs a = {};
   a.x = static_cast<const uint16_t*>(hidden);
   a.ids = topk_ids;
@@ -175,6 +183,9 @@ int run_decode(const void* hidden, const int32_t* topk_ids, const float* topk_we
   a.b13 = b13;
   a.b2 = b2;
   a.oai = oai;
+  a.ebase = rm.ebase;
+  a.window = rm.window;
+  a.per_route = rm.per_route;
   // w13 row groups: the gate row of group p and its up row one half-stride
   // later -- [gate; up] per expert: p = e 2I + i, up I rows later; gpt-oss
   // (interleaved): p = e I + i, up the next row
@@ -220,7 +231,7 @@ int run_prefill(const void* hidden, const int32_t* topk_ids, const float* topk_w
                 const uint8_t* w13, const uint8_t* s13, const float* b13, const uint8_t* w2,
                 const uint8_t* s2, const float* b2, int T, int K, int I, int E, int topk,
                 void* out, int32_t* status, char* ws, const Layout& L, int oai, DeviceInfo* d,
-                cudaStream_t s) {
+                cudaStream_t s, RouteMode rm = RouteMode()) {
   PrefillArgs p = {};
   p.hidden = static_cast<const uint16_t*>(hidden);
   p.ids = topk_ids;
@@ -248,6 +259,9 @@ int run_prefill(const void* hidden, const int32_t* topk_ids, const float* topk_w
   p.b13 = b13;
   p.b2 = b2;
   p.oai = oai;
+  p.ebase = rm.ebase;
+  p.window = rm.window;
+  p.per_route = rm.per_route;
   return cuda_status(launch_prefill(p, s, g_phase_events, g_phase_n));
 }
 
@@ -268,7 +282,7 @@ int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E, int32_t* ex
   if ((int64_t)T * topk >= ((int64_t)1 << 30)) return MXFP4_MOE_ERR_SHAPE;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
-  return cuda_status(launch_route(topk_ids, T * topk, E, expert_count, expert_offset, route_list,
+  return cuda_status(launch_route(topk_ids, T * topk, E, 0, 0, expert_count, expert_offset, route_list,
                                   status, static_cast<cudaStream_t>(stream)));
 }
 
@@ -305,6 +319,45 @@ int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* 
 
   return run_prefill(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
                      topk, out, status, ws, L, 0, d, s);
+}
+
+int mxfp4_moe_forward_window(const void* hidden, const int32_t* topk_ids,
+                             const float* topk_weights, const uint8_t* w13, const uint8_t* s13,
+                             const uint8_t* w2, const uint8_t* s2, int T, int K, int I, int E,
+                             int topk, int expert_base, int per_route, void* out, int32_t* status,
+                             void* workspace, size_t workspace_bytes, int path, void* stream) {
+  if (!shape_ok(T, K, I, E, topk)) return MXFP4_MOE_ERR_SHAPE;
+  if (path < 0 || path > 2 || expert_base < 0 || (per_route != 0 && per_route != 1))
+    return MXFP4_MOE_ERR_ARG;
+  if (T == 0) return MXFP4_MOE_OK;
+  if (!hidden || !topk_ids || (!topk_weights && !per_route) || !w13 || !s13 || !w2 || !s2 || !out)
+    return MXFP4_MOE_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(s13, 16) || !aligned(s2, 16))
+    return MXFP4_MOE_ERR_ALIGN;
+  if (workspace == nullptr) return MXFP4_MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return MXFP4_MOE_ERR_ALIGN;
+  const Layout L = layout(T, K, I, E, topk);
+  if (workspace_bytes < L.total) return MXFP4_MOE_ERR_WORKSPACE;
+  const bool decode = path == 1 || (path == 0 && T <= kDecodeMaxT);
+  if (decode && (T > kDecodeMaxT || T * topk > kDecodeMaxRoutes || K % 64 || I % 64))
+    return MXFP4_MOE_ERR_SHAPE;
+  if (!decode && (K % 64 || I % 64)) return MXFP4_MOE_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  if (decode && !decode_fits(K, I, E, T, topk, d->max_smem)) return MXFP4_MOE_ERR_SHAPE;
+  RouteMode rm;
+  rm.ebase = expert_base;
+  rm.window = 1;
+  rm.per_route = per_route;
+  // per-route outputs ignore the routing weights (the caller applies them)
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (decode)
+    return run_decode(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
+                      topk, out, status, ws, L, 0, d, s, rm);
+  return run_prefill(hidden, topk_ids, topk_weights, w13, s13, nullptr, w2, s2, nullptr, T, K, I, E,
+                     topk, out, status, ws, L, 0, d, s, rm);
 }
 
 int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const float* topk_weights,

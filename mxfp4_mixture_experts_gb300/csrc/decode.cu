@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     prefetch_tensormap(&P.tmap1);
     prefetch_tensormap(&P.tmap2);
   }
-  cta_route_small(a.ids, R, E, tb);   // ends with __syncthreads
+  cta_route_small(a.ids, R, E, a.ebase, a.window, tb);   // ends with __syncthreads
   const int nD = tb.misc[0];
   if (warp == 0) {   // expert-batch table: each touched expert's routes in batches of kBatch
     int carry = 0;
@@ -851,7 +851,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
             a.h[(size_t)r * a.I + i] = f32_to_bf16_rne(hv);
           } else {
             const int m = rb * kRows + g;
-            const float wr = a.wts[r];
+            const float wr = a.per_route ? 1.0f : a.wts[r];   // per-route rows: unweighted
             float o0 = acc[gr][j] * colmul, o1 = acc[gr][2 + j] * colmul;
             if (a.oai) {
               o0 += a.b2[(size_t)ir.e * a.K + m];

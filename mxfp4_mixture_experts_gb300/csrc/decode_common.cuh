@@ -5,6 +5,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace mxmoe {
 
@@ -59,6 +60,25 @@ __device__ __forceinline__ bool grid_wait(const int* ctr, uint32_t target) {
 __device__ __forceinline__ void combine_share(const DecodeArgs& a, int cta, int nCta, int tid0,
                                               int nthr) {
   const int per_row = a.K / 8;
+  if (a.per_route) {   // y [R, K]: each computed route's row, zero rows for skipped routes
+    const int total = a.T * a.topk * per_row;
+    const int c0 = range_begin(cta, total, nCta);
+    const int c1 = range_begin(cta + 1, total, nCta);
+    for (int i = c0 + tid0; i < c1; i += nthr) {
+      const int r = i / per_row, m8 = (i - r * per_row) * 8;
+      uint4 out = make_uint4(0u, 0u, 0u, 0u);
+      if (local_expert(a.ids[r], a.ebase, a.window, a.E) >= 0) {
+        const uint4 lo = ldcg16(a.P + (size_t)r * a.K + m8);
+        const uint4 hi = ldcg16(a.P + (size_t)r * a.K + m8 + 4);
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out.x) : "f"(__uint_as_float(lo.y)), "f"(__uint_as_float(lo.x)));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out.y) : "f"(__uint_as_float(lo.w)), "f"(__uint_as_float(lo.z)));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out.z) : "f"(__uint_as_float(hi.y)), "f"(__uint_as_float(hi.x)));
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(out.w) : "f"(__uint_as_float(hi.w)), "f"(__uint_as_float(hi.z)));
+      }
+      *reinterpret_cast<uint4*>(a.y + (size_t)r * a.K + m8) = out;
+    }
+    return;
+  }
   const int total = a.T * per_row;
   const int c0 = range_begin(cta, total, nCta);
   const int c1 = range_begin(cta + 1, total, nCta);
@@ -67,8 +87,7 @@ __device__ __forceinline__ void combine_share(const DecodeArgs& a, int cta, int 
     float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < a.topk; ++j) {
       const int r = tt * a.topk + j;
-      const int e = a.ids[r];
-      if (e < 0 || e >= a.E) continue;
+      if (local_expert(a.ids[r], a.ebase, a.window, a.E) < 0) continue;
       const uint4 lo = ldcg16(a.P + (size_t)r * a.K + m8);
       const uint4 hi = ldcg16(a.P + (size_t)r * a.K + m8 + 4);
       sum[0] += __uint_as_float(lo.x);

@@ -27,6 +27,10 @@ struct DecodeArgs {
   const float* b13;
   const float* b2;
   int oai;
+  // expert window (window != 0): the weights hold experts ebase .. ebase+E-1,
+  // other ids are skipped; per_route != 0: y is [T * topk, K], each route's
+  // unweighted w2 output (zero rows for skipped routes)
+  int ebase, window, per_route;
 };
 
 // Kernel parameter block: the two weight tensor maps (TMA descriptors,
@@ -68,8 +72,10 @@ bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base,
 bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
                      const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle swizzle);
 
-cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
-                         int32_t* list, int32_t* status, cudaStream_t stream);
+// ids outside [ebase, ebase + E) are skipped; without a window (window == 0,
+// ebase == 0) ids >= E are counted as invalid in status[0].
+cudaError_t launch_route(const int32_t* ids, int R, int E, int ebase, int window, int32_t* count,
+                         int32_t* offset, int32_t* list, int32_t* status, cudaStream_t stream);
 
 // MXFP4 encoder: bf16 [rows, cols] (cols % 32 == 0) -> packed [rows, cols/2]
 // and E8M0 scales [rows, cols/32]; quark != 0 takes the Quark exponent rule

@@ -32,6 +32,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "prefill.h"
+#include "route.cuh"
 
 namespace mxmoe {
 
@@ -464,8 +465,8 @@ __global__ void __launch_bounds__(256) combine_pos_kernel(const float* __restric
                                                           const int32_t* __restrict__ ids,
                                                           const float* __restrict__ wts,
                                                           const int32_t* __restrict__ inv, int T,
-                                                          int K, int E, int topk,
-                                                          uint16_t* __restrict__ y) {
+                                                          int K, int E, int topk, int ebase,
+                                                          int window, uint16_t* __restrict__ y) {
   const int per_row = K / 8;
   const int64_t n = (int64_t)T * per_row;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -474,8 +475,7 @@ __global__ void __launch_bounds__(256) combine_pos_kernel(const float* __restric
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < topk; ++j) {
       const int r = t * topk + j;
-      const int e = ids[r];
-      if (e < 0 || e >= E) continue;
+      if (local_expert(ids[r], ebase, window, E) < 0) continue;
       const float w = wts[r];
       const float* row = P + (size_t)inv[r] * K + m8;
       const uint4 lo = ldcg16(row);
@@ -494,6 +494,32 @@ __global__ void __launch_bounds__(256) combine_pos_kernel(const float* __restric
     for (int q = 0; q < 4; ++q)
       asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[q]) : "f"(s[2 * q + 1]), "f"(s[2 * q]));
     *reinterpret_cast<uint4*>(y + (size_t)t * K + m8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Per-route output: y[r][m] = bf16(P[inv[r]][m]) for the computed routes, zero
+// rows for skipped ones (8 outputs a thread).
+__global__ void __launch_bounds__(256) route_rows_kernel(const float* __restrict__ P,
+                                                         const int32_t* __restrict__ ids,
+                                                         const int32_t* __restrict__ inv, int R,
+                                                         int K, int E, int ebase, int window,
+                                                         uint16_t* __restrict__ y) {
+  const int per_row = K / 8;
+  const int64_t n = (int64_t)R * per_row;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / per_row), m8 = (int)(i - (int64_t)r * per_row) * 8;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (local_expert(ids[r], ebase, window, E) >= 0) {
+      const float* row = P + (size_t)inv[r] * K + m8;
+      const uint4 lo = ldcg16(row);
+      const uint4 hi = ldcg16(row + 4);
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.x) : "f"(__uint_as_float(lo.y)), "f"(__uint_as_float(lo.x)));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.y) : "f"(__uint_as_float(lo.w)), "f"(__uint_as_float(lo.z)));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.z) : "f"(__uint_as_float(hi.y)), "f"(__uint_as_float(hi.x)));
+      asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o.w) : "f"(__uint_as_float(hi.w)), "f"(__uint_as_float(hi.z)));
+    }
+    *reinterpret_cast<uint4*>(y + (size_t)r * K + m8) = o;
   }
 }
 
@@ -542,7 +568,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   };
   const int R = a.T * a.topk;
   rec(0);
-  cudaError_t e = launch_route(a.ids, R, a.E, a.count, a.offset, a.list, a.status, stream);
+  cudaError_t e = launch_route(a.ids, R, a.E, a.ebase, a.window, a.count, a.offset, a.list,
+                               a.status, stream);
   if (e != cudaSuccess) return e;
   int gblocks = a.num_sms * 8;
   gather_kernel<<<gblocks, 256, 0, stream>>>(a.hidden, a.list, a.offset + a.E, a.K, a.topk, a.xp,
@@ -587,11 +614,16 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   if ((e = launch_gemm<2>(g2, a.num_sms, stream)) != cudaSuccess) return e;
   rec(3);
   {
-    const int64_t n = (int64_t)a.T * (a.K / 8);
+    const int64_t n = (int64_t)(a.per_route ? R : a.T) * (a.K / 8);
     int64_t blocks = (n + 255) / 256;
     if (blocks > (int64_t)a.num_sms * 8) blocks = (int64_t)a.num_sms * 8;
-    combine_pos_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a.P, a.ids, a.wts, a.inv, a.T, a.K,
-                                                             a.E, a.topk, a.y);
+    if (a.per_route)
+      route_rows_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a.P, a.ids, a.inv, R, a.K, a.E,
+                                                              a.ebase, a.window, a.y);
+    else
+      combine_pos_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a.P, a.ids, a.wts, a.inv, a.T, a.K,
+                                                               a.E, a.topk, a.ebase, a.window,
+                                                               a.y);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   rec(4);

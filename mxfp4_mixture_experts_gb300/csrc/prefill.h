@@ -31,6 +31,8 @@ struct PrefillArgs {
   const float* b13;
   const float* b2;
   int oai;
+  // expert window and per-route output, as in DecodeArgs
+  int ebase, window, per_route;
 };
 
 size_t prefill_counter_bytes(int T, int K, int I, int E, int topk);

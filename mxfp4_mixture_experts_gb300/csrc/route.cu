@@ -4,6 +4,7 @@
 // the placement pass runs in all 32 warps at once and stays in route order.
 #include "common.cuh"
 #include "kernels.h"
+#include "route.cuh"
 
 namespace mxmoe {
 
@@ -11,8 +12,9 @@ constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 __global__ void __launch_bounds__(kRouteThreads, 1)
-route_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ count,
-             int32_t* __restrict__ offset, int32_t* __restrict__ list, int32_t* status) {
+route_kernel(const int32_t* __restrict__ ids, int R, int E, int ebase, int window,
+             int32_t* __restrict__ count, int32_t* __restrict__ offset,
+             int32_t* __restrict__ list, int32_t* status) {
   extern __shared__ int sm[];
   int* seg = sm;                        // [32][E] per-segment counts, then bases
   int* off = seg + kRouteWarps * E;     // [E+1]
@@ -31,9 +33,9 @@ route_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict_
   int inv = 0;
   for (int base = rb; base < re; base += 32) {
     const int r = base + lane;
-    const int e = r < re ? ids[r] : -1;
-    const bool ok = e >= 0 && e < E;
-    if (r < re && e >= E) ++inv;
+    const int e = r < re ? local_expert(ids[r], ebase, window, E) : -1;
+    const bool ok = e >= 0;
+    if (e == -2) ++inv;
     const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : E + lane);
     if (ok && (grp & lt) == 0) myseg[e] += __popc(grp);
     __syncwarp();
@@ -81,8 +83,8 @@ route_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict_
 
   for (int base = rb; base < re; base += 32) {
     const int r = base + lane;
-    const int e = r < re ? ids[r] : -1;
-    const bool ok = e >= 0 && e < E;
+    const int e = r < re ? local_expert(ids[r], ebase, window, E) : -1;
+    const bool ok = e >= 0;
     const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : E + lane);
     const int rank = __popc(grp & lt);
     const int before = ok ? myseg[e] : 0;
@@ -103,8 +105,8 @@ route_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict_
   }
 }
 
-cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32_t* offset,
-                         int32_t* list, int32_t* status, cudaStream_t stream) {
+cudaError_t launch_route(const int32_t* ids, int R, int E, int ebase, int window, int32_t* count,
+                         int32_t* offset, int32_t* list, int32_t* status, cudaStream_t stream) {
   static size_t granted = 48 * 1024;
   const size_t smem = sizeof(int) * ((size_t)kRouteWarps * E + E + 1);
   if (smem > granted) {
@@ -113,7 +115,8 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int32_t* count, int32
     if (e != cudaSuccess) return e;
     granted = smem;
   }
-  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, count, offset, list, status);
+  route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, ebase, window, count, offset, list,
+                                                   status);
   return cudaGetLastError();
 }
 

@@ -28,9 +28,19 @@ struct RouteTables {
   int* misc;     // [4]   misc[0] = nD, misc[1] = invalid route count
 };
 
+// Local expert of a route id: id - ebase when that lies in [0, E); -1 to skip
+// the route (a negative id is padding; with window != 0 every id outside the
+// window belongs to another expert-parallel rank); -2 for an invalid id
+// (>= E, no window), which is counted.
+__device__ __forceinline__ int local_expert(int id, int ebase, int window, int E) {
+  const int e = id - ebase;
+  if (e >= 0 && e < E) return e;
+  return (!window && id >= E) ? -2 : -1;
+}
+
 // All threads of the CTA must call this. Ends with __syncthreads().
 __device__ __forceinline__ void cta_route_small(const int32_t* __restrict__ ids, int R, int E,
-                                                RouteTables tb) {
+                                                int ebase, int window, RouteTables tb) {
   const int tid = threadIdx.x;
   for (int i = tid; i < E; i += blockDim.x) {
     tb.cnt[i] = 0;
@@ -40,8 +50,8 @@ __device__ __forceinline__ void cta_route_small(const int32_t* __restrict__ ids,
   __syncthreads();
   int inv = 0;
   for (int r = tid; r < R; r += blockDim.x) {
-    const int e = ids[r];
-    if (e >= E) ++inv;
+    const int e = local_expert(ids[r], ebase, window, E);
+    if (e == -2) ++inv;
     else if (e >= 0) atomicAdd(&tb.cnt[e], 1);   // integer counts: order-independent
   }
   if (inv) atomicAdd(&tb.misc[1], inv);
@@ -74,8 +84,8 @@ __device__ __forceinline__ void cta_route_small(const int32_t* __restrict__ ids,
     // stable placement, 32 routes at a time in route order
     for (int base = 0; base < R; base += 32) {
       const int r = base + lane;
-      const int e = r < R ? ids[r] : -1;
-      const bool ok = (e >= 0) && (e < E);
+      const int e = r < R ? local_expert(ids[r], ebase, window, E) : -1;
+      const bool ok = e >= 0;
       const int key = ok ? e : (E + lane);          // invalid lanes stay alone
       const uint32_t grp = __match_any_sync(0xffffffffu, key);
       const int rank = __popc(grp & lt);

@@ -49,6 +49,9 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_forward_oai.restype = i32
     L.mxfp4_moe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.mxfp4_moe_router.restype = i32
+    L.mxfp4_moe_forward_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                           i32, i32, vp, vp, vp, sz, i32, vp]
+    L.mxfp4_moe_forward_window.restype = i32
     L.mxfp4_moe_encode.argtypes = [vp, i32, i32, i32, vp, vp, vp]
     L.mxfp4_moe_encode.restype = i32
     L.mxfp4_moe_dequant.argtypes = [vp, vp, i32, i32, vp, vp]
@@ -155,6 +158,45 @@ def forward(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Te
         workspace.numel() * workspace.element_size(), path, _stream(stream))
     if rc:
         raise MoEError(rc, "mxfp4_moe_forward")
+    return out
+
+
+def forward_window(hidden: torch.Tensor, topk_ids: torch.Tensor,
+                   topk_weights: Optional[torch.Tensor], w13: torch.Tensor, s13: torch.Tensor,
+                   w2: torch.Tensor, s2: torch.Tensor, expert_base: int = 0,
+                   per_route: bool = False, out: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                   path: int = 0, stream=None) -> torch.Tensor:
+    """The layer over the experts expert_base .. expert_base + E - 1 held by
+    w13/s13/w2/s2 (other ids skipped): y [T, K] of the window's routes, or with
+    per_route each route's unweighted w2 output [T * topk, K]."""
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(topk_ids, "topk_ids", torch.int32, 2)
+    if topk_weights is not None:
+        _need(topk_weights, "topk_weights", torch.float32, 2)
+    elif not per_route:
+        raise ValueError("topk_weights are needed unless per_route")
+    for n, t in (("w13", w13), ("s13", s13), ("w2", w2), ("s2", s2)):
+        _need(t, n, torch.uint8, 3)
+    T, K = hidden.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    k = topk_ids.shape[1]
+    rows = T * k if per_route else T
+    if out is None:
+        out = torch.empty(rows, K, dtype=torch.bfloat16, device=hidden.device)
+    else:
+        _need(out, "out", torch.bfloat16, 2)
+        if tuple(out.shape) != (rows, K):
+            raise ValueError(f"out must be [{rows}, {K}]")
+    if workspace is None:
+        workspace = new_workspace(T, K, I, E, k, hidden.device)
+    rc = lib().mxfp4_moe_forward_window(
+        _ptr(hidden), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13), _ptr(s13), _ptr(w2),
+        _ptr(s2), T, K, I, E, k, int(expert_base), int(bool(per_route)), _ptr(out), _ptr(status),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), path, _stream(stream))
+    if rc:
+        raise MoEError(rc, "mxfp4_moe_forward_window")
     return out
 
 

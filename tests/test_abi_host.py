@@ -28,6 +28,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
+              "mxfp4_moe_forward_window",
               "mxfp4_moe_dequant", "mxfp4_moe_encode",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
         assert n in names
@@ -177,6 +178,29 @@ def test_encode_rejects_bad_arguments_without_a_gpu(L):
     assert enc(VP(0x1008), 4, 64, 0, VP(0x2000), VP(0x3000), None) == m.ERR_ALIGN
     assert enc(VP(0x1000), 4, 64, 0, VP(0x2002), VP(0x3000), None) == m.ERR_ALIGN
     assert enc(VP(0x1000), 0, 64, 0, VP(0x2000), VP(0x3000), None) == m.OK
+
+
+def test_forward_window_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+
+    def call(base=0, per_route=0, wts=VP(0x30000), path=1, **kw):
+        a = dict(hidden=VP(0x10000), ids=VP(0x20000), w13=VP(0x40000), s13=VP(0x50000),
+                 w2=VP(0x60000), s2=VP(0x70000), T=4, K=64, I=64, E=4, topk=2, out=VP(0x80000),
+                 ws=VP(0x100000), ws_bytes=1 << 40)
+        a.update(kw)
+        return L.mxfp4_moe_forward_window(a["hidden"], a["ids"], wts, a["w13"], a["s13"], a["w2"],
+                                          a["s2"], a["T"], a["K"], a["I"], a["E"], a["topk"], base,
+                                          per_route, a["out"], None, a["ws"], a["ws_bytes"], path,
+                                          None)
+    assert call(base=-1) == m.ERR_ARG
+    assert call(per_route=2) == m.ERR_ARG
+    assert call(wts=None) == m.ERR_ARG            # weights needed for the token sums
+    assert call(path=3) == m.ERR_ARG
+    assert call(K=65) == m.ERR_SHAPE
+    assert call(T=33, path=1) == m.ERR_SHAPE
+    assert call(out=VP(0x80008)) == m.ERR_ALIGN
+    assert call(ws=None) == m.ERR_WORKSPACE
+    assert call(T=0) == m.OK
 
 
 def test_route_and_dequant_reject_bad_arguments(L):
