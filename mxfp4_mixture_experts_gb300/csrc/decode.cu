@@ -235,6 +235,19 @@ __device__ __forceinline__ uint4 load_b16(const uint8_t* p) {
   else return *reinterpret_cast<const uint4*>(p);
 }
 
+// acc[0..1] += d[0..1] * f0 and acc[2..3] += d[2..3] * f1 as two packed fp32
+// FMAs (each lane of a pair rounds like a single FFMA).
+__device__ __forceinline__ void fold_block(float (&acc)[4], const float (&d)[4], float f0, float f1) {
+  const float2 lo = __ffma2_rn(make_float2(d[0], d[1]), make_float2(f0, f0),
+                               make_float2(acc[0], acc[1]));
+  const float2 hi = __ffma2_rn(make_float2(d[2], d[3]), make_float2(f1, f1),
+                               make_float2(acc[2], acc[3]));
+  acc[0] = lo.x;
+  acc[1] = lo.y;
+  acc[2] = hi.x;
+  acc[3] = hi.y;
+}
+
 // One 32-value block of one item for one warp: both m16 rows' 4-byte words,
 // their scales, and one MMA pair per token group.
 template <bool FAST, bool GLOB>
@@ -259,10 +272,7 @@ __device__ __forceinline__ void block_mma(float (&acc)[kMaxGroups][4], const uin
     // k16 slot 0 <- physical (8t, 8t+1), (8t+2, 8t+3); slot 1 <- (8t+4 .. 8t+7)
     mma_f16_16816_z(d, a0, c0, a1, c1, bv.x, bv.y);
     mma_f16_16816(d, a2, c2, a3, c3, bv.z, bv.w);
-    acc[gr][0] = fmaf(d[0], f0, acc[gr][0]);
-    acc[gr][1] = fmaf(d[1], f0, acc[gr][1]);
-    acc[gr][2] = fmaf(d[2], f1, acc[gr][2]);
-    acc[gr][3] = fmaf(d[3], f1, acc[gr][3]);
+    fold_block(acc[gr], d, f0, f1);
   }
 }
 
@@ -298,10 +308,7 @@ __device__ __forceinline__ void blocks_mma(float (&acc)[4], const uint8_t* stg, 
     float d[4];
     mma_f16_16816_z(d, a0, c0, a1, c1, bv[u].x, bv[u].y);
     mma_f16_16816(d, a2, c2, a3, c3, bv[u].z, bv[u].w);
-    acc[0] = fmaf(d[0], f0, acc[0]);
-    acc[1] = fmaf(d[1], f0, acc[1]);
-    acc[2] = fmaf(d[2], f1, acc[2]);
-    acc[3] = fmaf(d[3], f1, acc[3]);
+    fold_block(acc, d, f0, f1);
   }
 }
 
@@ -337,10 +344,7 @@ __device__ __forceinline__ void blocks_mma_groups(float (&acc)[kMaxGroups][4], c
       float d[4];
       mma_f16_16816_z(d, a0, c0, a1, c1, bv[u][gr].x, bv[u][gr].y);
       mma_f16_16816(d, a2, c2, a3, c3, bv[u][gr].z, bv[u][gr].w);
-      acc[gr][0] = fmaf(d[0], f0, acc[gr][0]);
-      acc[gr][1] = fmaf(d[1], f0, acc[gr][1]);
-      acc[gr][2] = fmaf(d[2], f1, acc[gr][2]);
-      acc[gr][3] = fmaf(d[3], f1, acc[gr][3]);
+      fold_block(acc[gr], d, f0, f1);
     }
   }
 }
