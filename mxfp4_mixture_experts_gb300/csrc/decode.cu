@@ -25,14 +25,16 @@
 //    sums cross warps or CTAs, and the SwiGLU of a gate/up pair happens in the
 //    thread that holds both.
 //  * Each warp streams its own items: lane 0 keeps the next stages of 16 rows
-//    x 256 bytes in flight in the warp's private ring (2-D TMA, 128-byte
-//    swizzle), running on into its phase-2 items before h exists, and
-//    bulk-copies each item's E8M0 rows into one of the warp's two scale slots.
-//    Spreading the issue over all warps keeps enough bytes in flight per SM.
+//    x 256 bytes in flight in the warp's private ring (128-byte swizzle; a
+//    whole stage is one 4-D (w13) or 3-D (w2) tensor copy, the last partial
+//    stage of a row one copy per 128-byte column), running on into its
+//    phase-2 items before h exists, and bulk-copies each item's E8M0 rows
+//    into one of the warp's two scale slots. Spreading the issue over all
+//    warps keeps enough bytes in flight per SM.
 //  * Consumers decode E2M1 with the hardware e2m1x2 -> f16x2 conversion
 //    (exact), run one m16n8k16 f16 MMA pair per 32-value block into a fresh
-//    fp32 fragment and fold it into the accumulator with one FFMA by
-//    2^(s-127) (exact for every scale byte, 0 and 255 included).
+//    fp32 fragment and fold it into the accumulator by 2^(s-127) with two
+//    packed fp32 FMAs (exact scales for every byte, 0 and 255 included).
 //  * Activations (hidden rows for phase 1, h rows for phase 2) are staged in
 //    shared memory by thread 0 (bulk copies) and converted to f16 after an
 //    exact power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
