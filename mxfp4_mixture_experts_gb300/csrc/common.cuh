@@ -20,30 +20,12 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Read-only streaming load of 16 bytes: the data is used once, so it is not
-// kept in L1; L2 fetches 256-byte lines to keep DRAM bursts long.
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ uint32_t ldg_u8(const uint8_t* p) {
   uint32_t v;
   asm volatile("ld.global.nc.u8 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
-// 16-byte load through L1 (small operands reused by many warps of an SM).
-__device__ __forceinline__ uint4 ldg16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-
-// 16-byte load that skips L1, for data other SMs wrote during this kernel.
 // 16 bytes through a generic address (shared or global memory), not cached in
 // L1 when global.
 __device__ __forceinline__ uint4 ld_cg_generic16(const void* p) {
@@ -52,6 +34,7 @@ __device__ __forceinline__ uint4 ld_cg_generic16(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
+// 16-byte load that skips L1, for data other SMs wrote during this kernel.
 __device__ __forceinline__ uint4 ldcg16(const void* p) {
   uint4 v;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -59,30 +42,10 @@ __device__ __forceinline__ uint4 ldcg16(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ float ldcg_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Programmatic dependent launch: wait for the grid this one depends on / let
-// the next grid in the stream begin launching.
+// Programmatic dependent launch: wait until the grid this one depends on has
+// finished (or triggered) before reading its results.
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// D += A * B for one m16n8k16 tile, bf16 inputs, fp32 accumulators.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 // Exact bf16x2 product (inputs and results may be subnormal).
@@ -153,9 +116,6 @@ __device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm
   if (__builtin_expect(sm.two, 0)) v = bf16x2_mul(v, sm.m2);
   return v;
 }
-
-__device__ __forceinline__ float bf16_lo_to_f32(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi_to_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 // fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
 __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
@@ -306,20 +266,6 @@ __device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint
 
 }  // namespace mxmoe
 
-namespace mxmoe {
-// Named barrier over `threads` threads that also ORs a predicate across them.
-__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(threads)
-      : "memory");
-  return r != 0;
-}
-}  // namespace mxmoe
-
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, tensor memory)
 // ---------------------------------------------------------------------------
@@ -346,15 +292,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
-      : "memory");
-}
 // D[tmem] (+)= A[tmem] * B[smem]^T: operand A (M rows = lanes, K values as bf16
 // pairs along columns) read from tensor memory.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,

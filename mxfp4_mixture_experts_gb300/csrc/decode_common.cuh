@@ -1,5 +1,5 @@
-// Pieces shared by the two decode kernels (tensor-core decode_tc.cu and the
-// CUDA-core decode.cu): the balanced split of work over CTAs, the grid-wide
+// Device pieces of the decode kernel kept apart from its main loop: the
+// balanced split of work over CTAs, the SwiGLU activations, the grid-wide
 // counters of the cooperative launch, and the slot-order combine.
 #pragma once
 
@@ -13,12 +13,6 @@ namespace mxmoe {
 __device__ __forceinline__ int range_begin(int v, int U, int n) {
   const int q = U / n, rem = U % n;
   return v * q + (v < rem ? v : rem);
-}
-// The CTA whose range_begin range holds unit u (0 <= u < U).
-__device__ __forceinline__ int range_owner(int u, int U, int n) {
-  const int q = U / n, rem = U % n;
-  const int big = rem * (q + 1);
-  return u < big ? u / (q + 1) : rem + (u - big) / q;
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
