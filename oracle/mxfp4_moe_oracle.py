@@ -261,32 +261,54 @@ def encode(hidden_bits, rule: str = "ocp"):
 
 
 # --- the router (logits -> top-k ids and weights) ------------------------------
-def topk_route(logits, topk: int, scoring: str, bias=None):
+def topk_route(logits, topk: int, scoring: str, bias=None, n_group: int = 1,
+               topk_group: int = 1, bias_in_weights: bool = True):
     """Router step before routing/permute ("MXFP4 MoE decode kernels",
     Design, "Routing inside the kernel" consumes its top-k ids; the workload
     shapes fix the scoring: top-k softmax for the gpt-oss shapes, sigmoid
     scores renormalised over the chosen k for the GLM shapes, an optional
-    per-expert bias added to the logits).
+    per-expert bias added to the logits; "GLM-5.2 and GLM-5.3 (744B) in
+    MXFP4 on Gaudi 2", Why it needed a port, item 4, names grouped top-k
+    without defining it).
 
     x = float32(logit + bias) (one float32 addition per element, so both
     sides of a comparison take the selection decision on the same values;
-    a NaN ranks as -inf);
-    the k largest x in order, ties to the lower expert index (sigmoid is
-    increasing, so this is the top-k by sigmoid score). Weights in float64:
-    softmax over the chosen x ("softmax_topk"), or sigmoid(x) of the chosen
-    divided by their sum ("sigmoid_renorm").
+    a NaN ranks as -inf).
+    Grouped top-k (n_group > 1): the E experts form n_group equal groups of
+    consecutive ids; a group's score is its largest x; only the topk_group
+    highest-scoring groups (ties to the lower group index) stay eligible.
+    The k largest eligible x in order, ties to the lower expert index
+    (sigmoid is increasing, so this is the top-k by sigmoid score).
+    Weights in float64 from v = x of the chosen, or, with
+    bias_in_weights=False (the bias steers the choice only), from their
+    unbiased logits (NaN again as -inf): softmax over the chosen v
+    ("softmax_topk"), or sigmoid(v) of the chosen divided by their sum
+    ("sigmoid_renorm").
     Returns ids int32 [T, k] and weights float64 [T, k]."""
-    x = np.asarray(logits, dtype=np.float32)
+    raw = np.asarray(logits, dtype=np.float32)
+    x = raw
     if bias is not None:
         x = (x + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
     x = np.where(np.isnan(x), np.float32(-np.inf), x)   # NaN ranks as -inf
     T, E = x.shape
+    if E % n_group or not 1 <= topk_group <= n_group:
+        raise ValueError("n_group must divide E and 1 <= topk_group <= n_group")
+    gs = E // n_group
     ids = np.empty((T, topk), dtype=np.int32)
     for t in range(T):
+        eligible = range(E)
+        if n_group > 1:
+            gscore = [max(float(x[t, e]) for e in range(g * gs, (g + 1) * gs))
+                      for g in range(n_group)]
+            kept = sorted(range(n_group), key=lambda g: (-gscore[g], g))[:topk_group]
+            eligible = [e for e in range(E) if e // gs in kept]
         # stable sort on -x: equal values keep ascending expert order
-        order = sorted(range(E), key=lambda e: (-float(x[t, e]), e))
+        order = sorted(eligible, key=lambda e: (-float(x[t, e]), e))
+        if len(order) < topk:
+            raise ValueError("fewer eligible experts than topk")
         ids[t] = order[:topk]
-    chosen = np.take_along_axis(x, ids.astype(np.int64), axis=1).astype(np.float64)
+    v = x if bias_in_weights else np.where(np.isnan(raw), np.float32(-np.inf), raw)
+    chosen = np.take_along_axis(v, ids.astype(np.int64), axis=1).astype(np.float64)
     if scoring == "softmax_topk":
         z = np.exp(chosen - chosen.max(axis=1, keepdims=True))
         w = z / z.sum(axis=1, keepdims=True)

@@ -172,3 +172,170 @@ def test_router_pins_catch_planted_mistakes():
     }
     for name, (fn, check) in cases.items():
         assert check(_with(fn)) != [], f"pin did not catch planted mistake: {name}"
+
+
+# --- grouped top-k and a selection-only bias ----------------------------------
+
+def check_router_grouped_hand(O):
+    """Hand-worked cases of grouped top-k (groups of consecutive ids, a
+    group's score its largest logit):
+    * E = 8 in 4 groups of 2, keep 2 groups, k = 3, logits
+      (10, -1 | 3, 2.9 | 2, 1 | 2.95, 2.8): group scores 10, 3, 2, 2.95 keep
+      groups 0 and 1, so the choice is 0, 2, 3; without groups it is 0, 2, 6;
+    * E = 6 in 3 groups, keep 1, k = 2, logits (5, -4 | 4, 3.5 | 0, 0): the
+      largest logit (5) keeps group 0 (ids 0, 1), although group 1 has the
+      larger sum;
+    * E = 4 in 2 groups, keep 1, k = 1, logits (1, 0 | 0, 1): the groups
+      tie, the lower group wins, expert 0."""
+    bad = []
+    lg = np.array([[10, -1, 3, 2.9, 2, 1, 2.95, 2.8]], dtype=np.float32)
+    for scoring in ("softmax_topk", "sigmoid_renorm"):
+        ids, _ = O.topk_route(lg, 3, scoring, None, 4, 2)
+        if list(ids[0]) != [0, 2, 3]:
+            bad.append(f"grouped {scoring}: {list(ids[0])} != [0, 2, 3]")
+        ids, _ = O.topk_route(lg, 3, scoring)
+        if list(ids[0]) != [0, 2, 6]:
+            bad.append(f"ungrouped {scoring}: {list(ids[0])} != [0, 2, 6]")
+    ids, _ = O.topk_route(np.array([[5, -4, 4, 3.5, 0, 0]], dtype=np.float32), 2,
+                          "sigmoid_renorm", None, 3, 1)
+    if list(ids[0]) != [0, 1]:
+        bad.append(f"group score is the largest logit: {list(ids[0])} != [0, 1]")
+    ids, _ = O.topk_route(np.array([[1, 0, 0, 1]], dtype=np.float32), 1, "softmax_topk",
+                          None, 2, 1)
+    if list(ids[0]) != [0]:
+        bad.append(f"tied groups: {list(ids[0])} != [0]")
+    return bad
+
+
+def brute_grouped(x, k, n_group, topk_group):
+    """Grouped choice by a second formulation: a group is kept when fewer than
+    topk_group groups beat it (a larger score, or an equal score and a lower
+    index); the experts then by enumeration over the kept ones."""
+    E = len(x)
+    gs = E // n_group
+    score = [max(float(v) for v in x[g * gs:(g + 1) * gs]) for g in range(n_group)]
+    kept = [g for g in range(n_group)
+            if sum(1 for h in range(n_group)
+                   if score[h] > score[g] or (score[h] == score[g] and h < g)) < topk_group]
+    elig = [e for e in range(E) if e // gs in kept]
+    sub = brute_ids(np.array([x[e] for e in elig]), k)
+    return [elig[i] for i in sub]
+
+
+def check_router_grouped_bruteforce(O, seed=34):
+    rng = np.random.default_rng(seed)
+    bad = []
+    for E, n_group, topk_group, k in ((6, 3, 1, 2), (8, 4, 2, 3), (8, 2, 1, 4), (9, 3, 2, 4),
+                                      (8, 4, 4, 3), (6, 1, 1, 3)):
+        lg = rng.standard_normal((8, E)).astype(np.float32)
+        lg[0, :] = 0.25                                   # everything tied
+        lg[1] = np.round(lg[1] * 2) / 2                   # coarse grid: ties
+        lg[2, ::2] = lg[2].max() + 1                      # tied group maxima
+        for t in range(lg.shape[0]):
+            ids, _ = O.topk_route(lg[t:t + 1], k, "softmax_topk", None, n_group, topk_group)
+            want = brute_grouped(lg[t], k, n_group, topk_group)
+            if list(ids[0]) != want:
+                bad.append(f"E {E} groups {n_group}/{topk_group} k {k} row {t}: "
+                           f"{list(ids[0])} != {want}")
+    return bad
+
+
+def check_router_grouped_special_cases(O, seed=35):
+    """Keeping every group, or a single group holding all experts, is the
+    ungrouped router."""
+    rng = np.random.default_rng(seed)
+    lg = rng.standard_normal((12, 64)).astype(np.float32)
+    bias = (0.5 * rng.standard_normal(64)).astype(np.float32)
+    ref = O.topk_route(lg, 6, "sigmoid_renorm", bias)
+    bad = []
+    for n_group, topk_group in ((8, 8), (1, 1)):
+        got = O.topk_route(lg, 6, "sigmoid_renorm", bias, n_group, topk_group)
+        if not (np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])):
+            bad.append(f"{n_group}/{topk_group} groups differ from the plain router")
+    return bad
+
+
+def check_router_selection_bias(O):
+    """With the bias steering the choice only, logits (1, 0.5, 0) and bias
+    (0, 1, 0) choose experts 1, 0 (x = 1.5, 1) and weigh them by the unbiased
+    logits (0.5, 1): softmax (1 / (1 + e^0.5), 1 / (1 + e^-0.5)) and sigmoid
+    renorm (s(0.5), s(1)) / (s(0.5) + s(1)); with the bias in the weights,
+    (1 / (1 + e^-0.5), 1 / (1 + e^0.5)) and (s(1.5), s(1)) / sum. Without a
+    bias the two readings agree."""
+    def sg(z):
+        return 1.0 / (1.0 + math.exp(-z))
+    lg = np.array([[1.0, 0.5, 0.0]], dtype=np.float32)
+    bias = np.array([0.0, 1.0, 0.0], dtype=np.float32)
+    want = {
+        ("softmax_topk", False): [sg(-0.5), sg(0.5)],
+        ("softmax_topk", True): [sg(0.5), sg(-0.5)],
+        ("sigmoid_renorm", False): [sg(0.5) / (sg(0.5) + sg(1.0)), sg(1.0) / (sg(0.5) + sg(1.0))],
+        ("sigmoid_renorm", True): [sg(1.5) / (sg(1.5) + sg(1.0)), sg(1.0) / (sg(1.5) + sg(1.0))],
+    }
+    bad = []
+    for (scoring, in_w), wv in want.items():
+        ids, w = O.topk_route(lg, 2, scoring, bias, bias_in_weights=in_w)
+        if list(ids[0]) != [1, 0] or not np.allclose(w[0], wv, rtol=0, atol=1e-15):
+            bad.append(f"{scoring} bias_in_weights={in_w}: {list(ids[0])} {w[0]} != {wv}")
+    rng = np.random.default_rng(36)
+    lg = rng.standard_normal((6, 32)).astype(np.float32)
+    a = O.topk_route(lg, 4, "softmax_topk", None, bias_in_weights=False)
+    b = O.topk_route(lg, 4, "softmax_topk", None)
+    if not (np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])):
+        bad.append("without a bias the selection-only reading changes the result")
+    return bad
+
+
+def test_router_grouped_hand_cases():
+    assert check_router_grouped_hand(O) == []
+
+
+def test_router_grouped_bruteforce():
+    assert check_router_grouped_bruteforce(O) == []
+
+
+def test_router_grouped_special_cases():
+    assert check_router_grouped_special_cases(O) == []
+
+
+def test_router_selection_only_bias():
+    assert check_router_selection_bias(O) == []
+
+
+def test_grouped_pins_catch_planted_mistakes():
+    def grouped(logits, topk, scoring, bias=None, n_group=1, topk_group=1,
+                bias_in_weights=True, score="max", strided=False, tie_high=False):
+        """The oracle's grouped selection with one step changed."""
+        x = np.asarray(logits, dtype=np.float32)
+        if bias is not None:
+            x = (x + np.asarray(bias, dtype=np.float32)[None, :]).astype(np.float32)
+        T, E = x.shape
+        gs = E // n_group
+        grp = (lambda e: e % n_group) if strided else (lambda e: e // gs)
+        ids = np.empty((T, topk), dtype=np.int32)
+        for t in range(T):
+            members = [[e for e in range(E) if grp(e) == g] for g in range(n_group)]
+            agg = max if score == "max" else sum
+            gscore = [agg(float(x[t, e]) for e in m) for m in members]
+            kept = sorted(range(n_group),
+                          key=lambda g: (-gscore[g], -g if tie_high else g))[:topk_group]
+            elig = [e for e in range(E) if grp(e) in kept]
+            ids[t] = sorted(elig, key=lambda e: (-float(x[t, e]), e))[:topk]
+        ref_w = O.topk_route(logits, topk, scoring, bias, n_group, topk_group, bias_in_weights)[1]
+        return ids, ref_w
+
+    def weights_always_biased(logits, topk, scoring, bias=None, n_group=1, topk_group=1,
+                              bias_in_weights=True):
+        return O.topk_route(logits, topk, scoring, bias, n_group, topk_group, True)
+
+    cases = {
+        "group score is the sum": (lambda *a, **kw: grouped(*a, **kw, score="sum"),
+                                   check_router_grouped_hand),
+        "strided groups": (lambda *a, **kw: grouped(*a, **kw, strided=True),
+                           check_router_grouped_hand),
+        "tied groups to the higher index": (lambda *a, **kw: grouped(*a, **kw, tie_high=True),
+                                            check_router_grouped_bruteforce),
+        "bias always in the weights": (weights_always_biased, check_router_selection_bias),
+    }
+    for name, (fn, check) in cases.items():
+        assert check(_with(fn)) != [], f"pin did not catch planted mistake: {name}"
