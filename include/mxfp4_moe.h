@@ -114,6 +114,27 @@ int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E,
 int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int topk, int scoring,
                      int32_t* topk_ids, float* topk_weights, void* stream);
 
+/* Router with grouped top-k and a choice of what the bias moves ("GLM-5.2 and
+ * GLM-5.3 (744B) in MXFP4 on Gaudi 2", Why it needed a port, item 4, names
+ * grouped top-k without defining it). As mxfp4_moe_router, plus:
+ *   n_group       the E experts form n_group equal groups of consecutive ids
+ *                 (group of e = e / (E / n_group)); a group's score is its
+ *                 largest x; only the topk_group highest-scoring groups (ties
+ *                 to the lower group index) stay eligible, and the k largest x
+ *                 among their experts are chosen as above. n_group = 1 is the
+ *                 plain router.
+ *   bias_in_weights  1: the weights use x (the bias moves selection and
+ *                 weights, as mxfp4_moe_router); 0: the bias steers the
+ *                 choice only, the weights use the chosen experts' unbiased
+ *                 logits (a NaN logit as -inf); softmax over the chosen then
+ *                 subtracts their largest value.
+ * Limits (MXFP4_MOE_ERR_SHAPE): those of mxfp4_moe_router, 1 <= n_group <= 32,
+ * E % n_group == 0, 1 <= topk_group <= n_group, k <= topk_group * E / n_group;
+ * bias_in_weights 0 or 1 (MXFP4_MOE_ERR_ARG). */
+int mxfp4_moe_router_grouped(const float* logits, const float* bias, int T, int E, int topk,
+                             int scoring, int n_group, int topk_group, int bias_in_weights,
+                             int32_t* topk_ids, float* topk_weights, void* stream);
+
 /* The MoE layer, y = sum_j w_tj * W2[e] silu(W_gate[e] x) * (W_up[e] x).
  *   hidden        bf16  [T, K]
  *   topk_ids      int32 [T, topk]   (negative = padding, >= E = invalid, both skipped)

@@ -393,11 +393,16 @@ int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const flo
                      out, status, ws, L, 1, d, s);
 }
 
-int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int topk, int scoring,
-                     int32_t* topk_ids, float* topk_weights, void* stream) {
+int mxfp4_moe_router_grouped(const float* logits, const float* bias, int T, int E, int topk,
+                             int scoring, int n_group, int topk_group, int bias_in_weights,
+                             int32_t* topk_ids, float* topk_weights, void* stream) {
   if (T < 0 || E < 1 || E > kRouterMaxExperts || topk < 1 || topk > 32 || topk > E)
     return MXFP4_MOE_ERR_SHAPE;
+  if (n_group < 1 || n_group > 32 || E % n_group || topk_group < 1 || topk_group > n_group ||
+      topk > topk_group * (E / n_group))
+    return MXFP4_MOE_ERR_SHAPE;
   if (scoring != 0 && scoring != 1) return MXFP4_MOE_ERR_ARG;
+  if (bias_in_weights != 0 && bias_in_weights != 1) return MXFP4_MOE_ERR_ARG;
   if (T == 0) return MXFP4_MOE_OK;
   if (!logits || !topk_ids || !topk_weights) return MXFP4_MOE_ERR_ARG;
   if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_weights, 4) ||
@@ -405,8 +410,15 @@ int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int t
     return MXFP4_MOE_ERR_ALIGN;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
-  return cuda_status(launch_router(logits, bias, T, E, topk, scoring, topk_ids, topk_weights,
-                                   d->num_sms, static_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_router(logits, bias, T, E, topk, scoring, n_group, topk_group,
+                                   bias_in_weights, topk_ids, topk_weights, d->num_sms,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_moe_router(const float* logits, const float* bias, int T, int E, int topk, int scoring,
+                     int32_t* topk_ids, float* topk_weights, void* stream) {
+  return mxfp4_moe_router_grouped(logits, bias, T, E, topk, scoring, 1, 1, 1, topk_ids,
+                                  topk_weights, stream);
 }
 
 int mxfp4_moe_encode(const void* x, int rows, int cols, int rule, uint8_t* packed,

@@ -89,7 +89,8 @@ constexpr int kRouterMaxExperts = 1024;   // 32 per lane of one warp
 // and weights fp32 [T, k]; scoring 0 = softmax over the chosen k, 1 = sigmoid
 // renormalised over the chosen k (router.cu).
 cudaError_t launch_router(const float* logits, const float* bias, int T, int E, int topk,
-                          int scoring, int32_t* ids, float* wts, int num_sms, cudaStream_t stream);
+                          int scoring, int n_group, int topk_group, int bias_in_weights,
+                          int32_t* ids, float* wts, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
                            uint16_t* out, int num_sms, cudaStream_t stream);

@@ -49,6 +49,8 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_forward_oai.restype = i32
     L.mxfp4_moe_router.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
     L.mxfp4_moe_router.restype = i32
+    L.mxfp4_moe_router_grouped.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    L.mxfp4_moe_router_grouped.restype = i32
     L.mxfp4_moe_forward_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                            i32, i32, vp, vp, vp, sz, i32, vp]
     L.mxfp4_moe_forward_window.restype = i32
@@ -245,12 +247,7 @@ def forward_oai(hidden: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torc
 SCORING = {"softmax_topk": 0, "sigmoid_renorm": 1}
 
 
-def router(logits: torch.Tensor, topk: int, scoring: str = "softmax_topk",
-           bias: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
-           topk_weights: Optional[torch.Tensor] = None, stream=None):
-    """Top-k experts of fp32 logits [T, E] (+ bias [E]) and their weights:
-    int32 [T, k] ids (descending x = logit + bias, ties to the lower index)
-    and fp32 [T, k] weights (softmax over the chosen, or renormalised sigmoid)."""
+def _router_args(logits, topk, scoring, bias, topk_ids, topk_weights):
     _need(logits, "logits", torch.float32, 2)
     T, E = logits.shape
     if bias is not None:
@@ -263,10 +260,39 @@ def router(logits: torch.Tensor, topk: int, scoring: str = "softmax_topk",
         topk_ids = torch.empty(T, topk, dtype=torch.int32, device=logits.device)
     if topk_weights is None:
         topk_weights = torch.empty(T, topk, dtype=torch.float32, device=logits.device)
+    return T, E, topk_ids, topk_weights
+
+
+def router(logits: torch.Tensor, topk: int, scoring: str = "softmax_topk",
+           bias: Optional[torch.Tensor] = None, topk_ids: Optional[torch.Tensor] = None,
+           topk_weights: Optional[torch.Tensor] = None, stream=None):
+    """Top-k experts of fp32 logits [T, E] (+ bias [E]) and their weights:
+    int32 [T, k] ids (descending x = logit + bias, ties to the lower index)
+    and fp32 [T, k] weights (softmax over the chosen, or renormalised sigmoid)."""
+    T, E, topk_ids, topk_weights = _router_args(logits, topk, scoring, bias, topk_ids,
+                                                topk_weights)
     rc = lib().mxfp4_moe_router(_ptr(logits), _ptr(bias), T, E, topk, SCORING[scoring],
                                 _ptr(topk_ids), _ptr(topk_weights), _stream(stream))
     if rc:
         raise MoEError(rc, "mxfp4_moe_router")
+    return topk_ids, topk_weights
+
+
+def router_grouped(logits: torch.Tensor, topk: int, scoring: str = "sigmoid_renorm",
+                   bias: Optional[torch.Tensor] = None, n_group: int = 1, topk_group: int = 1,
+                   bias_in_weights: bool = True, topk_ids: Optional[torch.Tensor] = None,
+                   topk_weights: Optional[torch.Tensor] = None, stream=None):
+    """``router`` with grouped top-k (n_group groups of consecutive experts
+    scored by their largest x; the experts of the topk_group best groups stay
+    eligible) and, with bias_in_weights=False, a bias that steers the choice
+    only (weights from the unbiased logits)."""
+    T, E, topk_ids, topk_weights = _router_args(logits, topk, scoring, bias, topk_ids,
+                                                topk_weights)
+    rc = lib().mxfp4_moe_router_grouped(_ptr(logits), _ptr(bias), T, E, topk, SCORING[scoring],
+                                        n_group, topk_group, int(bool(bias_in_weights)),
+                                        _ptr(topk_ids), _ptr(topk_weights), _stream(stream))
+    if rc:
+        raise MoEError(rc, "mxfp4_moe_router_grouped")
     return topk_ids, topk_weights
 
 

@@ -27,7 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
+    for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_router_grouped",
+              "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
               "mxfp4_moe_forward_window",
               "mxfp4_moe_dequant", "mxfp4_moe_encode",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
@@ -164,6 +165,32 @@ def test_router_rejects_bad_arguments_without_a_gpu(L):
     assert call(w=VP(0x3002)) == m.ERR_ALIGN
     assert call(b=VP(0x4001)) == m.ERR_ALIGN
     assert call(T=0) == m.OK
+
+
+def test_router_grouped_rejects_bad_arguments_without_a_gpu(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    R = L.mxfp4_moe_router_grouped
+    ok = dict(lg=VP(0x1000), b=None, T=4, E=64, k=4, sc=1, ng=8, tg=2, bw=1, ids=VP(0x2000),
+              w=VP(0x3000))
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return R(a["lg"], a["b"], a["T"], a["E"], a["k"], a["sc"], a["ng"], a["tg"], a["bw"],
+                 a["ids"], a["w"], None)
+    assert call(ng=0) == m.ERR_SHAPE
+    assert call(ng=33, E=66) == m.ERR_SHAPE
+    assert call(ng=6) == m.ERR_SHAPE            # 64 % 6 != 0
+    assert call(tg=0) == m.ERR_SHAPE
+    assert call(tg=9) == m.ERR_SHAPE
+    assert call(k=17, tg=2) == m.ERR_SHAPE      # 2 groups of 8 hold 16 experts
+    assert call(k=0) == m.ERR_SHAPE
+    assert call(E=1025, ng=1, tg=1) == m.ERR_SHAPE
+    assert call(bw=2) == m.ERR_ARG
+    assert call(sc=5) == m.ERR_ARG
+    assert call(lg=None) == m.ERR_ARG
+    assert call(ids=VP(0x2001)) == m.ERR_ALIGN
+    assert call(T=0) == m.OK
+    assert call(T=0, k=16, tg=2, ng=8, bw=0) == m.OK
 
 
 def test_encode_rejects_bad_arguments_without_a_gpu(L):

@@ -97,3 +97,63 @@ def test_router_feeds_the_layer(moe):
     case.topk_ids = torch.from_numpy(rid)
     case.topk_weights = torch.from_numpy(rw.astype(np.float32))
     gate(y, case)
+
+
+def check_grouped(moe, logits, k, scoring, bias, n_group, topk_group, bias_in_weights):
+    ids, w = moe.router_grouped(logits.cuda(), k, scoring, None if bias is None else bias.cuda(),
+                                n_group, topk_group, bias_in_weights)
+    torch.cuda.synchronize()
+    rid, rw = O.topk_route(logits.numpy(), k, scoring, None if bias is None else bias.numpy(),
+                           n_group, topk_group, bias_in_weights)
+    got_ids = ids.cpu().numpy()
+    assert np.array_equal(got_ids, rid), np.argwhere(got_ids != rid)[:5]
+    got_w = w.cpu().numpy().astype(np.float64)
+    ok = np.isfinite(rw)
+    assert np.all(np.abs(got_w[ok] - rw[ok]) <= 1e-6 * np.abs(rw[ok]) + 1e-12)
+    return got_ids, got_w
+
+
+@pytest.mark.parametrize("T,E,k,scoring,n_group,topk_group,bias_sigma,in_w", [
+    (32, 256, 8, "sigmoid_renorm", 8, 4, 0.5, False),      # 8 groups of 32, bias steers only
+    (8192, 256, 8, "sigmoid_renorm", 8, 4, 0.5, False),    # a prefill chunk
+    (64, 128, 4, "softmax_topk", 4, 2, 0.0, True),
+    (100, 160, 6, "softmax_topk", 32, 3, 0.3, True),       # groups of 5
+    (40, 1024, 32, "sigmoid_renorm", 32, 8, 0.2, False),   # the largest E, k and n_group
+    (17, 96, 12, "sigmoid_renorm", 3, 1, 0.0, True),       # one group kept
+    (5, 8, 8, "softmax_topk", 2, 2, 0.0, True),            # k = E
+    (33, 256, 8, "softmax_topk", 1, 1, 0.7, False),        # no groups, bias steers only
+])
+def test_grouped_router_matches_oracle(moe, T, E, k, scoring, n_group, topk_group, bias_sigma,
+                                       in_w):
+    g = torch.Generator().manual_seed(T * 17 + E + n_group)
+    logits = torch.randn(T, E, generator=g)
+    bias = bias_sigma * torch.randn(E, generator=g) if bias_sigma > 0 else None
+    check_grouped(moe, logits, k, scoring, bias, n_group, topk_group, in_w)
+
+
+def test_grouped_router_ties_and_nan(moe):
+    """Coarse logits (tied experts and tied group scores), a group of NaN
+    logits (its score is -inf) and a row of equal logits (the lowest groups
+    and ids win)."""
+    g = torch.Generator().manual_seed(9)
+    logits = torch.round(torch.randn(48, 64, generator=g) * 2) / 2
+    logits[0] = 0.5
+    logits[1, 8:16] = float("nan")
+    logits[2, :] = float("nan")
+    logits[2, 50] = 0.0
+    for scoring in ("softmax_topk", "sigmoid_renorm"):
+        for in_w in (True, False):
+            ids, _ = check_grouped(moe, logits, 6, scoring, None, 8, 3, in_w)
+            assert list(ids[0]) == [0, 1, 2, 3, 4, 5]
+            assert not ((ids[1] >= 8) & (ids[1] < 16)).any()
+            assert ids[2, 0] == 50
+
+
+def test_plain_router_is_grouped_router_with_one_group(moe):
+    g = torch.Generator().manual_seed(10)
+    logits = torch.randn(200, 256, generator=g).cuda()
+    bias = (0.5 * torch.randn(256, generator=g)).cuda()
+    a = moe.router(logits, 8, "sigmoid_renorm", bias)
+    b = moe.router_grouped(logits, 8, "sigmoid_renorm", bias, 1, 1, True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
