@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from mxfp4_mixture_experts_gb300 import synth
-from helpers import TOL_REL_L2, compare, gate, bf16_to_f64, oracle_rows, rel_l2
+from helpers import compare, gate
 from oracle import mxfp4_moe_oracle as O
 
 pytestmark = pytest.mark.gpu

@@ -13,7 +13,6 @@ from fractions import Fraction
 
 import numpy as np
 import pytest
-import torch
 
 from oracle import mxfp4_moe_oracle as O
 from test_oracle_pins import dequant_by_bits, small_case

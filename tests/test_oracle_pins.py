@@ -10,7 +10,6 @@ import os
 from fractions import Fraction
 
 import numpy as np
-import pytest
 import torch
 
 from oracle import mxfp4_moe_oracle as O

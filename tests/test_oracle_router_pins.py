@@ -7,7 +7,6 @@ import math
 import types
 
 import numpy as np
-import pytest
 
 from oracle import mxfp4_moe_oracle as O
 

@@ -5,7 +5,6 @@ through the C ABI, twice in a row. Kept in a file of its own that pytest
 collects last."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
