@@ -10,6 +10,7 @@ constexpr int kScaleBlock = 32;        // E2M1 values per E8M0 scale
 constexpr int kMaxExperts = 1024;
 constexpr int kDecodeMaxTokens = 32;
 constexpr int kDecodeMaxRoutes = 1024;
+constexpr int kGrantDevices = 64;      // devices whose kernel attributes are tracked
 
 // ---------------------------------------------------------------------------
 // Small PTX wrappers
@@ -115,6 +116,26 @@ __device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm
   uint32_t v = bf16x2_mul(raw, sm.m1);
   if (__builtin_expect(sm.two, 0)) v = bf16x2_mul(v, sm.m2);
   return v;
+}
+
+// One 32-value scale block as exact bf16 by integer bit placement and bf16
+// multiplies (the prefill GEMM's operand A): wd holds the 16 packed bytes
+// (value 2i in the low nibble of byte i), sm the block's scale multipliers.
+// o[4c .. 4c+3] = values 8c .. 8c+7 as bf16 pairs (low half first), i.e. the
+// 32 values in row order.
+__device__ __forceinline__ void dequant32_bf16(const uint32_t (&wd)[4], const ScaleMul& sm,
+                                               uint32_t (&o)[16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {   // values 8c .. 8c+7
+    const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(wd[c]), sm);   // (n0, n4)
+    const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(wd[c]), sm);   // (n1, n5)
+    const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(wd[c]), sm);   // (n2, n6)
+    const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(wd[c]), sm);   // (n3, n7)
+    o[4 * c + 0] = prmt(p0, p1, 0x5410u);   // (n0, n1)
+    o[4 * c + 1] = prmt(p2, p3, 0x5410u);   // (n2, n3)
+    o[4 * c + 2] = prmt(p0, p1, 0x7632u);   // (n4, n5)
+    o[4 * c + 3] = prmt(p2, p3, 0x7632u);   // (n6, n7)
+  }
 }
 
 // fp32 -> bf16 bits, round to nearest even (NaN kept quiet).

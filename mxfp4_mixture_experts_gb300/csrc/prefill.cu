@@ -323,20 +323,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_empty[sp]);
           if (++sp == kSP) { sp = 0; pp ^= 1u; }
-          const ScaleMul sm = scale_mul(sc[i]);
           const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
-          uint32_t o[16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {   // values 8c .. 8c+7 of this thread's 32
-            const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(wd[c]), sm);   // (n0, n4)
-            const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(wd[c]), sm);   // (n1, n5)
-            const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(wd[c]), sm);   // (n2, n6)
-            const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(wd[c]), sm);   // (n3, n7)
-            o[4 * c + 0] = prmt(p0, p1, 0x5410u);
-            o[4 * c + 1] = prmt(p2, p3, 0x5410u);
-            o[4 * c + 2] = prmt(p0, p1, 0x7632u);
-            o[4 * c + 3] = prmt(p2, p3, 0x7632u);
-          }
+          uint32_t o[16];   // this thread's 32 values, in row order (bf16 pairs)
+          dequant32_bf16(wd, scale_mul(sc[i]), o);
           if (kw >= kSW) {   // the MMAs that read this ring slot have completed
             if (!warp_wait(&w_empty[sw], pw ^ 1u)) { fail = 32; break; }
             tc_fence_after();
@@ -528,17 +517,20 @@ static size_t gemm_smem_bytes(int E) {
          (size_t)(2 * kSX + 2 * kSP + 2 * kSW + 3) * 8 + 16 + (size_t)(E + 1) * 4;
 }
 
-size_t prefill_counter_bytes(int, int, int, int, int) { return 256; }
-
 template <int PHASE, bool OAI>
 static cudaError_t launch_gemm_form(const GemmParams& gp, int num_sms, cudaStream_t stream) {
-  static size_t granted = 0;
+  // the shared-memory grant is a per-device attribute of the kernel
+  static size_t granted[kGrantDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kGrantDevices) return cudaErrorInvalidDevice;
   const size_t smem = gemm_smem_bytes(gp.E);
-  if (smem > granted) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<PHASE, OAI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > granted[dev]) {
+    e = cudaFuncSetAttribute(gemm_kernel<PHASE, OAI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
-    granted = smem;
+    granted[dev] = smem;
   }
   gemm_kernel<PHASE, OAI><<<num_sms, kPfThreads, smem, stream>>>(gp);
   return cudaGetLastError();

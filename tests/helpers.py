@@ -1,5 +1,8 @@
 """Test helpers: seeded cases on the device, oracle calls on host copies,
 and the comparison metrics (no arithmetic of the layer itself)."""
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -7,6 +10,8 @@ from mxfp4_mixture_experts_gb300 import synth
 from oracle import mxfp4_moe_oracle as O
 
 TOL_REL_L2 = 3e-3   # output gate, rel_l2 over the compared rows, vs both oracle modes
+# Slack over the best bf16 output of the specified computation (below).
+IDEAL_SLACK = 1.1
 
 
 def rel_l2(got, ref) -> float:
@@ -53,27 +58,51 @@ def oracle_rows(case: synth.Case, tokens=None, intermediate="bf16", biases=None)
     return O.forward(hb, sub_ids, wts, w13, s13, w2, s2, intermediate=intermediate)
 
 
-def compare(y_gpu: torch.Tensor, case: synth.Case, tokens=None, with_gap: bool = False,
+def compare(y_gpu: torch.Tensor, case: synth.Case, tokens=None, with_ideal: bool = False,
             biases=None):
     """(rel_l2 vs bf16-intermediate oracle, rel_l2 vs fp32-intermediate, max abs err)
-    and, with_gap, the two oracle modes' own rel_l2 distance."""
+    and, with_ideal, the rel_l2 of the bf16-rounded bf16-intermediate oracle
+    output against the fp32-intermediate one."""
     got = bf16_to_f64(y_gpu)
     if tokens is not None:
         got = got[np.asarray(tokens)]
     ref_a = oracle_rows(case, tokens, "bf16", biases)
     ref_b = oracle_rows(case, tokens, "fp32", biases)
     out = (rel_l2(got, ref_a), rel_l2(got, ref_b), float(np.abs(got - ref_a).max()))
-    return out + (rel_l2(ref_a, ref_b),) if with_gap else out
+    return out + (rel_l2(O.round_to_bf16(ref_a), ref_b),) if with_ideal else out
 
 
-def gate(y_gpu: torch.Tensor, case: synth.Case, tokens=None, biases=None):
-    """The parity gate. Against the pages' reference (fp32 accumulation with a
-    bf16 intermediate h): rel_l2 <= TOL_REL_L2. Against the fp32-intermediate
-    reading: rel_l2 <= max(TOL_REL_L2, gap + rel_l2 vs the first), gap being the
-    distance of the two oracle modes themselves -- the bf16 rounding of h that
-    the layer specifies separates them, by more than the tolerance on short
-    reductions with few tokens (triangle inequality). Returns the figures."""
-    ra, rb, mx, gap = compare(y_gpu, case, tokens, with_gap=True, biases=biases)
-    assert ra <= TOL_REL_L2, (ra, rb, mx, gap)
-    assert rb <= max(TOL_REL_L2, gap + ra), (ra, rb, mx, gap)
+def log_figures(label: str, **fig):
+    """Appends one JSON record of parity figures to $MXFP4_MOE_PARITY_LOG, if set."""
+    path = os.environ.get("MXFP4_MOE_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(case=label, **fig)) + "\n")
+
+
+def gate_figures(ra: float, rb: float, ideal_b: float, strict: bool):
+    """The two-mode parity gate on computed figures.
+
+    Mode A, the pages' reference (fp32 accumulation with a bf16 intermediate
+    h, "MXFP4 MoE decode kernels", Parity): rel_l2 <= TOL_REL_L2 always.
+    Mode B, the unrounded-intermediate reading: rel_l2 <= TOL_REL_L2 as well,
+    except on short-reduction shapes where even the best bf16 output of the
+    specified computation -- the bf16 rounding of the mode-A result -- lies
+    further than that from mode B; there the bound is IDEAL_SLACK times that
+    output's own distance. strict (the full-size workload cases) allows no
+    such exception."""
+    assert ra <= TOL_REL_L2, ("mode A", ra, rb, ideal_b)
+    bound_b = TOL_REL_L2 if strict else max(TOL_REL_L2, IDEAL_SLACK * ideal_b)
+    assert rb <= bound_b, ("mode B", ra, rb, ideal_b)
+
+
+def gate(y_gpu: torch.Tensor, case: synth.Case, tokens=None, biases=None, strict: bool = False,
+         label: str = ""):
+    """The parity gate (gate_figures) against the oracle rows of `tokens`.
+    Returns (rel_l2 mode A, rel_l2 mode B, max abs error vs mode A)."""
+    ra, rb, mx, ideal_b = compare(y_gpu, case, tokens, with_ideal=True, biases=biases)
+    log_figures(label or f"{case.shape.name} T={case.T}", rows=(case.T if tokens is None
+                else len(tokens)), rel_l2_a=ra, rel_l2_b=rb, max_abs=mx, ideal_b=ideal_b,
+                strict=strict)
+    gate_figures(ra, rb, ideal_b, strict)
     return ra, rb, mx

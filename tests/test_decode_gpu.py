@@ -171,6 +171,8 @@ def test_negative_control_swapped_gate_up(moe):
     assert ra > 0.1
 
 
+# full size, the launch configuration the benchmark times; at T = 32 every
+# row of the three large shapes is compared, elsewhere the first and last token
 FULL = [("single32", 1), ("gptoss128", 1), ("gptoss128", 4), ("gptoss128", 16),
         ("gptoss128", 32), ("glm256", 1), ("glm256", 8), ("glm256", 32), ("widek256", 1),
         ("widek256", 2), ("widek256", 4), ("widek256", 8), ("widek256", 16), ("widek256", 32)]
@@ -203,8 +205,8 @@ def test_full_size_sampled_tokens(moe, full_weights, name, T):
     assert torch.isfinite(y).all()
     rt = O.route(ids.numpy(), shape.E)
     assert int(status[1]) == len(rt["touched"]) and int(status[0]) == 0
-    tokens = sorted({0, T - 1})
-    assert_close(y, case, tokens)
+    tokens = None if T == 32 else sorted({0, T - 1})
+    gate(y, case, tokens, strict=True, label=f"{name} T={T} decode")
 
 
 def test_wide_activation_range_in_every_block(moe):

@@ -160,7 +160,7 @@ def test_oai_gptoss128_full_size_sampled_tokens(moe, T):
     assert torch.isfinite(y).all()
     rt = O.route(ids.numpy(), shape.E)
     assert int(status[1]) == len(rt["touched"])
-    gate(y, case, sorted({0, T - 1}), biases=b)
+    gate(y, case, sorted({0, T - 1}), biases=b, strict=True)
     del w13, s13, w2, s2
     torch.cuda.empty_cache()
 
@@ -221,6 +221,6 @@ def test_oai_prefill_gptoss128_full_size_sampled_tokens(moe):
     b = synth.draw_biases(shape, seed=0)
     y = run_oai_path(moe, case, b, 0)
     assert torch.isfinite(y).all()
-    gate(y, case, [0, 1023, 2047], biases=b)
+    gate(y, case, [0, 1023, 2047], biases=b, strict=True)
     del case, w13, s13, w2, s2
     torch.cuda.empty_cache()

@@ -165,7 +165,7 @@ def test_negative_control_swapped_gate_up(moe):
 
 
 @pytest.mark.parametrize("name,T,tokens", [
-    ("prefill256", 8192, (0, 4097, 8191)),
+    ("prefill256", 8192, tuple(range(0, 8192, 32))),   # 256 tokens over all 256 experts
     ("gptoss128", 2048, (0, 2047)),
 ])
 def test_full_size_sampled_tokens(moe, name, T, tokens):
@@ -179,6 +179,6 @@ def test_full_size_sampled_tokens(moe, name, T, tokens):
     assert torch.isfinite(y).all()
     rt = O.route(ids.numpy(), shape.E)
     assert int(status[1]) == len(rt["touched"]) and int(status[0]) == 0
-    assert_close(y, case, list(tokens))
+    gate(y, case, list(tokens), strict=True, label=f"{name} T={T} prefill")
     del case, w13, s13, w2, s2
     torch.cuda.empty_cache()
