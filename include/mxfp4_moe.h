@@ -35,8 +35,10 @@
  *                   output of that call is then not valid; never expected);
  *                   the bits name the wait: bits 0..7 the decode kernel's
  *                   producer, 8..15 its consumers, 16..23 the prefill path's
- *                   first GEMM, 24..31 its second. After such a call the
- *                   workspace must be zeroed again before it is reused
+ *                   first GEMM, 24..31 its second. The workspace stays
+ *                   usable after such a call: the decode kernel's last CTA
+ *                   resets its counters on every exit path, and the prefill
+ *                   path keeps no state in the workspace between calls
  *       status[3] = 1 + the first CTA that reported such a wait, else 0
  *    Negative expert ids are padding and are skipped silently.
  *  - Every call is deterministic: repeating it on the same inputs gives
@@ -75,9 +77,9 @@ typedef enum {
 
 /* Bytes of device workspace a forward call with these sizes needs (either
  * path). The first mxfp4_moe_workspace_size(...) bytes must be zero before
- * the first call that uses a workspace; every completed call leaves the
- * bookkeeping part zero again, so a workspace can be reused without clearing.
- * Returns 0 for invalid sizes. */
+ * the first call that uses a workspace; every call leaves the bookkeeping part
+ * zero again (also one whose bounded wait gave up), so a workspace can be
+ * reused without clearing. Returns 0 for invalid sizes. */
 size_t mxfp4_moe_workspace_size(int T, int K, int I, int E, int topk);
 
 /* Routing / permute ("MXFP4 MoE decode kernels", Design, "Routing inside the
@@ -222,9 +224,16 @@ int mxfp4_moe_forward_oai(const void* hidden, const int32_t* topk_ids, const flo
  *  - Sizes whose mxfp4_moe_workspace_size(T, K, I, E, topk) exceeds
  *    MXFP4_MOE_NOALLOC_BYTES are rejected with MXFP4_MOE_ERR_WORKSPACE (the
  *    decode path of the four workload shapes fits up to T = 32).
- *  - The first call on a device performs the set-up for that device (looks up
- *    the array's device address and clears its bookkeeping part on `stream`);
- *    make that first call before any stream capture.
+ *  - The first call on a device performs the set-up for that device: it looks
+ *    up the array's device address, which makes the CUDA driver load this part
+ *    of the library and place the array on that device (a one-time driver
+ *    allocation that may synchronise), and clears the array's bookkeeping part
+ *    on `stream`. Make that first call in set-up code, before any stream
+ *    capture and before any loop that must not synchronise; the promise that
+ *    nothing is allocated holds for every later call.
+ *  - The library leaves the array's bookkeeping part zero after every call,
+ *    also after one whose bounded wait gave up (status[2] != 0), so the array
+ *    never needs clearing by the caller (who could not reach it anyway).
  *  - All calls share the one array, and it keeps the last call's contents:
  *    calls whose work may overlap on the GPU (different streams without
  *    ordering) race on it; issue them on one stream or order them. */
@@ -256,9 +265,24 @@ int mxfp4_moe_encode(const void* x, int rows, int cols, int rule, uint8_t* packe
  *   packed uint8 [rows, cols/2], scale uint8 [rows, cols/32] -> out bf16 [rows, cols]
  * Each value is E2M1(nibble) * 2^(s - 127) rounded once to bf16, which is
  * exact except that products beyond the bf16 range become +-inf and the
- * scale byte 255 gives NaN. cols % 32 == 0; out 4-byte aligned. */
+ * scale byte 255 gives NaN. cols % 32 == 0 (MXFP4_MOE_ERR_SHAPE); packed
+ * 16-byte and out 4-byte aligned (MXFP4_MOE_ERR_ALIGN). Uses the decode
+ * kernels' conversion (form 1 of mxfp4_moe_dequant_form). */
 int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
                       void* out, void* stream);
+
+/* The same dequantisation through the conversion of one path of the layer,
+ * so that a bit-exact check pins the weights each path computes with:
+ *   form 1  the decode kernels': hardware E2M1 -> f16 (exact), then an exact
+ *           fp32 multiply by 2^(s - 127), rounded once to bf16;
+ *   form 2  the prefill GEMM's operand A: the E2M1 fields placed in a bf16
+ *           bit pattern (magnitude x 2^-126), then exact bf16 multiplies by
+ *           2^(s - 1), or by 2^126 and 2^(s - 127) for bytes above 128 --
+ *           the same device routine that feeds the GEMM's tensor memory.
+ * Both give the value stated for mxfp4_moe_dequant, bit for bit; form
+ * outside {1, 2} gives MXFP4_MOE_ERR_ARG; other rules as mxfp4_moe_dequant. */
+int mxfp4_moe_dequant_form(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
+                           int form, void* out, void* stream);
 
 /* Profiling hook: when events (host array of n cudaEvent_t handles, n >= 2)
  * is non-NULL, each later forward call on this process records events[0]
@@ -268,6 +292,14 @@ int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int
  * turn it off.
  * Not thread-safe; meant for benchmarks. */
 void mxfp4_moe_set_phase_events(void* const* events, int n);
+
+/* Test only: from the next forward call on, the decode kernel's CTA `cta`
+ * does not arrive at the grid barrier between its two phases, so every
+ * bounded wait on that barrier (in all CTAs) runs out and the call reports it
+ * in status[2] and status[3] instead of computing the output; a negative cta
+ * turns this off (the default). It exists so tests can exercise the failure
+ * reporting without faulting or hanging a GPU. Not thread-safe. */
+void mxfp4_moe_test_skip_grid_arrival(int cta);
 
 /* Static description of an error code (never NULL). */
 const char* mxfp4_moe_strerror(int code);

@@ -30,6 +30,7 @@ std::mutex g_dev_mu;
 
 void* const* g_phase_events = nullptr;
 int g_phase_n = 0;
+int g_test_skip_arrival = -1;   // mxfp4_moe_test_skip_grid_arrival
 
 // cuTensorMapEncodeTiled, fetched from the driver at first use (no link-time
 // dependency on libcuda).
@@ -78,7 +79,7 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // Workspace layout. The bookkeeping that must be zero between calls comes
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
-  size_t gbar, pf_ctr;                                     // zero-kept
+  size_t gbar;                                             // zero-kept
   size_t h, P, rcount, roffset, rlist, rinv, xp;           // scratch
   size_t total;
 };
@@ -97,7 +98,6 @@ Layout layout(int T, int K, int I, int E, int topk) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
   L.gbar = take(2 * sizeof(int));
-  L.pf_ctr = take(prefill_counter_bytes(T, K, I, E, topk));
   L.h = take(R * I * 2);
   L.P = take(R * K * sizeof(float));
   L.rcount = take((size_t)E * sizeof(int));
@@ -119,6 +119,10 @@ void record_phase(int i, cudaStream_t s) {
 }  // namespace
 
 namespace mxmoe {
+// Bytes at the start of every workspace that must be zero when a call starts
+// (the decode launch's grid counters; the same for all sizes).
+size_t workspace_zero_kept_bytes() { return layout(1, 64, 64, 1, 1).h; }
+
 bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0,
                      uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
                      CUtensorMapSwizzle swizzle) {
@@ -186,6 +190,7 @@ int run_decode(const void* hidden, const int32_t* topk_ids, const float* topk_we
   a.ebase = rm.ebase;
   a.window = rm.window;
   a.per_route = rm.per_route;
+  a.skip_arrival_cta = g_test_skip_arrival;
   // w13 row groups: the gate row of group p and its up row one half-stride
   // later -- [gate; up] per expert: p = e 2I + i, up I rows later; gpt-oss
   // (interleaved): p = e I + i, up the next row
@@ -254,7 +259,6 @@ int run_prefill(const void* hidden, const int32_t* topk_ids, const float* topk_w
   p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
   p.P = reinterpret_cast<float*>(ws + L.P);
   p.inv = reinterpret_cast<int32_t*>(ws + L.rinv);
-  p.counters = reinterpret_cast<int*>(ws + L.pf_ctr);
   p.num_sms = d->num_sms;
   p.b13 = b13;
   p.b2 = b2;
@@ -434,17 +438,22 @@ int mxfp4_moe_encode(const void* x, int rows, int cols, int rule, uint8_t* packe
                                    d->num_sms, static_cast<cudaStream_t>(stream)));
 }
 
-int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
-                      void* stream) {
-  if (rows < 0 || cols < 0) return MXFP4_MOE_ERR_ARG;
+int mxfp4_moe_dequant_form(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
+                           int form, void* out, void* stream) {
+  if (rows < 0 || cols < 0 || (form != 1 && form != 2)) return MXFP4_MOE_ERR_ARG;
   if (cols % 32) return MXFP4_MOE_ERR_SHAPE;
   if (rows == 0 || cols == 0) return MXFP4_MOE_OK;
   if (!packed || !scale || !out) return MXFP4_MOE_ERR_ARG;
   if (!aligned(packed, 16) || !aligned(out, 4)) return MXFP4_MOE_ERR_ALIGN;
   DeviceInfo* d = nullptr;
   if (int rc = current_device(&d)) return rc;
-  return cuda_status(launch_dequant(packed, scale, rows, cols, static_cast<uint16_t*>(out),
+  return cuda_status(launch_dequant(packed, scale, rows, cols, form, static_cast<uint16_t*>(out),
                                     d->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+int mxfp4_moe_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols, void* out,
+                      void* stream) {
+  return mxfp4_moe_dequant_form(packed, scale, rows, cols, 1, out, stream);
 }
 
 void mxfp4_moe_set_phase_events(void* const* events, int n) {
@@ -456,6 +465,8 @@ void mxfp4_moe_set_phase_events(void* const* events, int n) {
     g_phase_n = n;
   }
 }
+
+void mxfp4_moe_test_skip_grid_arrival(int cta) { g_test_skip_arrival = cta < 0 ? -1 : cta; }
 
 const char* mxfp4_moe_strerror(int code) {
   switch (code) {

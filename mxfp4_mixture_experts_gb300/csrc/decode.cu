@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     if (phase == 1) fence_proxy_async_global();   // h is read next by bulk copies
     __threadfence();
     named_barrier(kBarConsumers, kThreadsCW);
-    if (ctid == 0) atomicAdd(gbar, 1);
+    if (ctid == 0 && !(phase == 1 && (int)blockIdx.x == a.skip_arrival_cta)) atomicAdd(gbar, 1);
   }
 
   // -- combine: y [T, K] (this CTA's slice), once every route output exists
@@ -964,16 +964,21 @@ bool decode_fits(int K, int I, int E, int T, int topk, int max_smem) {
 
 template <int CW>
 static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cudaStream_t stream) {
-  static size_t granted = 0;
-  if (smem > granted) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<CW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the shared-memory grant is a per-device attribute of the kernel
+  static size_t granted[kGrantDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kGrantDevices) return cudaErrorInvalidDevice;
+  if (smem > granted[dev]) {
+    e = cudaFuncSetAttribute(decode_kernel<CW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
-    granted = smem;
+    granted[dev] = smem;
   }
   // every CTA must be resident at once (grid barriers): one per SM, cooperative launch
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<CW>, CW * 32, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<CW>, CW * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};

@@ -31,6 +31,9 @@ struct DecodeArgs {
   // other ids are skipped; per_route != 0: y is [T * topk, K], each route's
   // unweighted w2 output (zero rows for skipped routes)
   int ebase, window, per_route;
+  // test only (-1 = off): this CTA does not arrive at the grid barrier after
+  // phase 1, so every CTA's bounded waits on it run out and report it
+  int skip_arrival_cta;
 };
 
 // Kernel parameter block: the two weight tensor maps (TMA descriptors,
@@ -51,6 +54,10 @@ struct DecodeParams {
   int xs_rows_cap;        // activation rows staged in shared memory
   int xs_stride;          // bytes per staged row (f16), = 64 mod 128
 };
+
+// Bytes at the start of every workspace that must be zero when a call starts
+// (api.cu).
+size_t workspace_zero_kept_bytes();
 
 // Whether the decode kernel's shared-memory plan fits for these sizes.
 bool decode_fits(int K, int I, int E, int T, int topk, int max_smem);
@@ -92,7 +99,8 @@ cudaError_t launch_router(const float* logits, const float* bias, int T, int E, 
                           int scoring, int n_group, int topk_group, int bias_in_weights,
                           int32_t* ids, float* wts, int num_sms, cudaStream_t stream);
 
+// form 1: the decode kernels' conversion; form 2: the prefill GEMM's (dequant.cu).
 cudaError_t launch_dequant(const uint8_t* packed, const uint8_t* scale, int rows, int cols,
-                           uint16_t* out, int num_sms, cudaStream_t stream);
+                           int form, uint16_t* out, int num_sms, cudaStream_t stream);
 
 }  // namespace mxmoe

@@ -7,16 +7,13 @@
 #include <stdint.h>
 
 #include "../../include/mxfp4_moe.h"
+#include "kernels.h"
 
 namespace {
 
 // Workspace of the no-allocation entry point. Every GPU that loads the
 // library holds it until the process exits. Static storage starts zeroed.
 static __device__ __align__(256) unsigned char g_noalloc_ws[MXFP4_MOE_NOALLOC_BYTES];
-
-// The first bytes of any workspace hold counters that must be zero when a
-// call starts (each completed call leaves them zero); cleared at set-up.
-constexpr size_t kBookkeepingBytes = 64 * 1024;
 
 constexpr int kMaxDevices = 64;
 void* g_ws[kMaxDevices] = {};
@@ -33,7 +30,12 @@ int noalloc_workspace(void** ws, cudaStream_t stream) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || p == nullptr)
       return MXFP4_MOE_ERR_CUDA;
-    if (cudaMemsetAsync(p, 0, kBookkeepingBytes, stream) != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
+    // the first bytes of any workspace hold counters that must be zero when a
+    // call starts; every call leaves them zero again, also one whose bounded
+    // wait gave up, so they are cleared once, here
+    const size_t zero_kept = mxmoe::workspace_zero_kept_bytes();
+    if (zero_kept > sizeof(g_noalloc_ws)) return MXFP4_MOE_ERR_WORKSPACE;
+    if (cudaMemsetAsync(p, 0, zero_kept, stream) != cudaSuccess) return MXFP4_MOE_ERR_CUDA;
     g_ws[dev] = p;
   }
   *ws = g_ws[dev];

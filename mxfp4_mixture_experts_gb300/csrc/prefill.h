@@ -24,7 +24,6 @@ struct PrefillArgs {
   uint16_t* hp;             // bf16 [R, I], rows in expert order
   float* P;                 // fp32 [R, K], rows in expert order, unweighted
   int32_t* inv;             // [R] route -> row of P
-  int* counters;            // zero-kept scheduler counters
   int num_sms;
   // gpt-oss form (oai != 0): w13 rows interleaved (row 2i gate i, row 2i + 1
   // up i), f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI
@@ -35,7 +34,6 @@ struct PrefillArgs {
   int ebase, window, per_route;
 };
 
-size_t prefill_counter_bytes(int T, int K, int I, int E, int topk);
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, void* const* phase_events,
                            int n_events);
 

@@ -58,6 +58,10 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_encode.restype = i32
     L.mxfp4_moe_dequant.argtypes = [vp, vp, i32, i32, vp, vp]
     L.mxfp4_moe_dequant.restype = i32
+    L.mxfp4_moe_dequant_form.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+    L.mxfp4_moe_dequant_form.restype = i32
+    L.mxfp4_moe_test_skip_grid_arrival.argtypes = [i32]
+    L.mxfp4_moe_test_skip_grid_arrival.restype = None
     L.mxfp4_moe_set_phase_events.argtypes = [vp, i32]
     L.mxfp4_moe_set_phase_events.restype = None
     L.mxfp4_moe_strerror.argtypes = [i32]
@@ -316,18 +320,27 @@ def encode(x: torch.Tensor, rule: str = "ocp", stream=None):
     return packed, scale
 
 
-def dequant(packed: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:
-    """Packed rows [N, C/2] + scales [N, C/32] -> bf16 [N, C]."""
+DEQUANT_FORMS = {"decode": 1, "prefill": 2}
+
+
+def dequant(packed: torch.Tensor, scale: torch.Tensor, form: str = "decode",
+            stream=None) -> torch.Tensor:
+    """Packed rows [N, C/2] + scales [N, C/32] -> bf16 [N, C], through the
+    weight decode of the decode kernels (form "decode") or of the prefill
+    GEMM (form "prefill")."""
     _need(packed, "packed", torch.uint8, 2)
     _need(scale, "scale", torch.uint8, 2)
+    if form not in DEQUANT_FORMS:
+        raise ValueError(f"form must be one of {sorted(DEQUANT_FORMS)}")
     N, half = packed.shape
     C = 2 * half
     if tuple(scale.shape) != (N, C // 32):
         raise ValueError("scale must be [rows, cols/32]")
     out = torch.empty(N, C, dtype=torch.bfloat16, device=packed.device)
-    rc = lib().mxfp4_moe_dequant(_ptr(packed), _ptr(scale), N, C, _ptr(out), _stream(stream))
+    rc = lib().mxfp4_moe_dequant_form(_ptr(packed), _ptr(scale), N, C, DEQUANT_FORMS[form],
+                                      _ptr(out), _stream(stream))
     if rc:
-        raise MoEError(rc, "mxfp4_moe_dequant")
+        raise MoEError(rc, "mxfp4_moe_dequant_form")
     return out
 
 

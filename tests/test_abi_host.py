@@ -30,7 +30,7 @@ def test_header_declares_the_entry_points():
     for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_router_grouped",
               "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
               "mxfp4_moe_forward_window",
-              "mxfp4_moe_dequant", "mxfp4_moe_encode",
+              "mxfp4_moe_dequant", "mxfp4_moe_dequant_form", "mxfp4_moe_encode",
               "mxfp4_moe_workspace_size", "mxfp4_moe_strerror"):
         assert n in names
 
@@ -242,3 +242,25 @@ def test_route_and_dequant_reject_bad_arguments(L):
     assert L.mxfp4_moe_dequant(VP(0x1008), VP(0x2000), 4, 64, VP(0x3000), None) == m.ERR_ALIGN
     assert L.mxfp4_moe_dequant(None, VP(0x2000), 4, 64, VP(0x3000), None) == m.ERR_ARG
     assert L.mxfp4_moe_dequant(VP(0x1000), VP(0x2000), 0, 64, VP(0x3000), None) == m.OK
+    for form in (1, 2):
+        f = L.mxfp4_moe_dequant_form
+        assert f(VP(0x1000), VP(0x2000), 4, 48, form, VP(0x3000), None) == m.ERR_SHAPE
+        assert f(VP(0x1008), VP(0x2000), 4, 64, form, VP(0x3000), None) == m.ERR_ALIGN
+        assert f(VP(0x1000), VP(0x2000), 0, 64, form, VP(0x3000), None) == m.OK
+    for form in (0, 3, -1):
+        assert L.mxfp4_moe_dequant_form(VP(0x1000), VP(0x2000), 4, 64, form, VP(0x3000),
+                                        None) == m.ERR_ARG
+
+
+def test_noalloc_array_holds_the_decode_workspace_of_every_workload_shape(L):
+    """The fixed array of mxfp4_moe_forward_noalloc fits the decode path of
+    the four decode workload shapes at their largest token count (T = 32)."""
+    from mxfp4_mixture_experts_gb300 import synth
+    src = open(HEADER).read()
+    m = re.search(r"#define\s+MXFP4_MOE_NOALLOC_BYTES\s+\((\d+)u\s*\*\s*(\d+)u\s*\*\s*(\d+)u\)", src)
+    assert m, "MXFP4_MOE_NOALLOC_BYTES not found"
+    cap = int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+    for name in ("single32", "gptoss128", "glm256", "widek256"):
+        s = synth.SHAPES[name]
+        need = L.mxfp4_moe_workspace_size(32, s.K, s.I, s.E, s.topk)
+        assert 0 < need <= cap, (name, need, cap)

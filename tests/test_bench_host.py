@@ -63,11 +63,10 @@ def test_traffic_record_only_for_the_measured_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h = bench.kernel_hash("decode")
     rec = {"kernel_hash": h, "dram_over_alg": {"32": 1.007}}
-    (tmp_path / "profiles" / "decode_traffic.md").write_text(
-        "# summary\n\nrecord: " + json.dumps(rec) + "\n")
+    (tmp_path / "profiles" / "decode_traffic.json").write_text(json.dumps(rec))
     assert bench.recorded_traffic("decode") == rec
     (csrc / "decode.cu").write_text("// changed\n")      # the kernel changed since
     assert bench.kernel_hash("decode") != h
     assert bench.recorded_traffic("decode") is None
-    (tmp_path / "profiles" / "decode_traffic.md").unlink()
+    (tmp_path / "profiles" / "decode_traffic.json").unlink()
     assert bench.recorded_traffic("decode") is None
