@@ -407,14 +407,18 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
     return out
 
 
+CONFIG_LAYERS = 8
+
+
 def measure_configs(dev, hbm_gbs: float, reps: int = 10):
     """The other decode workload shapes (the 32-expert single layer at T = 1,
     the 6144 x 2048 256-expert layer at T = 1, 8, 32 and the wide-K skewed
     layer at T = 1 .. 32) and the gpt-oss form of the 2880 x 2880 128-expert
     layer (interleaved gate/up rows, biases, SwiGLU-OAI; T = 1 .. 32):
     microseconds per call and GB/s of the touched experts' packed bytes, from
-    CUDA-graph replays of single calls that alternate between two layers of
-    weights (inputs larger than L2)."""
+    CUDA-graph replays of single calls that rotate over eight layers of
+    weights, so no call finds its experts in L2 from an earlier replay (at
+    T = 1 the smallest shape touches 53 MB a call, 423 MB over the ring)."""
     from mxfp4_mixture_experts_gb300 import moe
     out = {}
     stream = torch.cuda.Stream()
@@ -422,7 +426,8 @@ def measure_configs(dev, hbm_gbs: float, reps: int = 10):
         oai = name.endswith("_oai")
         sh = synth.SHAPES[name[:-4] if oai else name]
         Ts = (1, 4, 16, 32) if name in ("single32", "gptoss128_oai") else sh.tokens
-        layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev) for l in range(2)]
+        layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev)
+                  for l in range(CONFIG_LAYERS)]
         res = {}
         for T in Ts:
             ws = moe.new_workspace(T, sh.K, sh.I, sh.E, sh.topk, dev)
@@ -632,7 +637,23 @@ def time_phases(wl, steps: int, warmup: int):
                 ms = e0.elapsed_time(e1)
                 per_T[ly["T"]].append((ms, ly))
                 launches.append((wl.alg_bytes(ly), ms))
-    return per_T, launches
+    # cross-check: single cold calls, each after writing 1 GiB (8x the L2) so
+    # nothing of the call's weights or activations is left in L2
+    cold = {T: [] for T in wl.tokens}
+    scrub = torch.empty(1 << 30, dtype=torch.uint8, device=wl.dev)
+    with torch.cuda.stream(stream):
+        for r in range(3):
+            for l, ly in enumerate(wl.L):
+                scrub.fill_(r + 1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                graphs[l].replay()
+                e1.record(stream)
+                stream.synchronize()
+                cold[ly["T"]].append(e0.elapsed_time(e1))
+    del scrub
+    return per_T, launches, cold
 
 
 # Sources that make up each kernel: a profile summary under profiles/ records
@@ -655,17 +676,15 @@ def kernel_hash(kind: str) -> str:
 
 
 def recorded_traffic(kind: str):
-    """The `record:` line of profiles/<kind>_traffic.md, if its kernel hash is
-    the current one, else None."""
-    path = os.path.join(ROOT, "profiles", f"{kind}_traffic.md")
+    """The DRAM-traffic record of profiles/<kind>_traffic.json (written with
+    the ncu capture it summarises), if its kernel hash is the current one,
+    else None."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        for line in f:
-            if line.startswith("record:"):
-                rec = json.loads(line[len("record:"):])
-                return rec if rec.get("kernel_hash") == kernel_hash(kind) else None
-    return None
+        rec = json.load(f)
+    return rec if rec.get("kernel_hash") == kernel_hash(kind) else None
 
 
 def time_e2e(wl, steps: int, warmup: int):
@@ -690,38 +709,56 @@ def time_e2e(wl, steps: int, warmup: int):
     return e0.elapsed_time(e1), h2d // steps, d2h // steps
 
 
-def cpu_oracle_sample(wl, budget_s: float = 15.0):
-    """The oracle as it stands, timed on this host on single calls of the
-    workload (smallest T first) until about budget_s of CPU work."""
-    from oracle import mxfp4_moe_oracle as O
-    times, sample = [], []
-    t_start = time.perf_counter()
-    for ly in sorted(wl.L, key=lambda l: l["T"]):
-        if time.perf_counter() - t_start > budget_s and times:
-            break
-        ids = ly["ids"].cpu().numpy().astype(np.int64)
-        E = wl.shape.E
-        used = np.unique(ids[(ids >= 0) & (ids < E)])
-        idx = torch.as_tensor(used, device=ly["w13"].device)
-        host = [t.index_select(0, idx).cpu().numpy() for t in (ly["w13"], ly["s13"], ly["w2"], ly["s2"])]
-        remap = np.full(E, -1)
-        remap[used] = np.arange(len(used))
-        sub = remap[ids]
-        hb = ly["hidden"].cpu().view(torch.int16).numpy().view(np.uint16)
-        w = ly["w"].cpu().numpy()
-        t0 = time.perf_counter()
-        O.forward(hb, sub, w, *host)
-        times.append(time.perf_counter() - t0)
-        sample.append(ly["T"])
+def _oracle_inputs(ly, E):
+    """Host copies of one bench layer's call for the oracle: only the experts
+    the call touches, relabelled 0..n-1 (the oracle is pinned invariant under
+    expert relabelling)."""
+    ids = ly["ids"].cpu().numpy().astype(np.int64)
+    used = np.unique(ids[(ids >= 0) & (ids < E)])
+    idx = torch.as_tensor(used, device=ly["w13"].device)
+    host = [t.index_select(0, idx).cpu().numpy() for t in (ly["w13"], ly["s13"], ly["w2"], ly["s2"])]
+    remap = np.full(E, -1)
+    remap[used] = np.arange(len(used))
+    hb = ly["hidden"].cpu().view(torch.int16).numpy().view(np.uint16)
+    return (hb, remap[ids], ly["w"].cpu().numpy(), *host)
+
+
+def _host_cores():
     try:
         from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:
-        cores = os.cpu_count()
-    us = statistics.mean(times) * 1e6
-    return {"value": us, "unit": "us_per_moe_call", "cores": cores, "kind": "oracle",
-            "sample": f"{len(times)} single oracle calls of the same workload at T={sample} "
-                      f"(float64 numpy, {sum(times):.1f} s of CPU work)"}
+        return os.cpu_count()
+
+
+def cpu_oracle_sample(wl):
+    """The oracle as it stands, timed on this host on one call at each T of
+    the workload's mix (the first layer of each T; value = the mean over the
+    T, as the headline's). The oracle rows of those calls also give the
+    parity figures of the GPU's outputs of the same calls: rel_l2 against the
+    bf16-intermediate oracle (the pages' reference) and the unrounded one,
+    and the largest absolute error, over every row."""
+    from oracle import mxfp4_moe_oracle as O
+    times, parity = {}, {}
+    for T in wl.tokens:
+        ly = next(l for l in wl.L if l["T"] == T)
+        args = _oracle_inputs(ly, wl.shape.E)
+        t0 = time.perf_counter()
+        ya = O.forward(*args, intermediate="bf16")
+        times[T] = time.perf_counter() - t0
+        yb = O.forward(*args, intermediate="fp32")
+        got = ly["out"].float().cpu().numpy().astype(np.float64)
+        parity[str(T)] = {"rows": int(T),
+                          "rel_l2_bf16_intermediate": float(np.linalg.norm(got - ya) / np.linalg.norm(ya)),
+                          "rel_l2_fp32_intermediate": float(np.linalg.norm(got - yb) / np.linalg.norm(yb)),
+                          "max_abs_err": float(np.abs(got - ya).max()),
+                          "max_abs_ref": float(np.abs(ya).max())}
+    us = statistics.mean(times.values()) * 1e6
+    cpu = {"value": round(us, 1), "unit": "us_per_moe_call", "cores": _host_cores(),
+           "kind": "oracle",
+           "sample": f"one oracle call at each T={list(times)} of the workload (float64 numpy, "
+                     f"{sum(times.values()):.1f} s of CPU work); value = mean over the T"}
+    return cpu, parity
 
 
 # ---------------------------------------------------------------------------
@@ -736,7 +773,7 @@ def run_ours(args, dist: Dist):
     elapsed_ms = dist.max(elapsed_ms)
     calls = args.steps * wl.calls_per_step
     value = aggregate_us_per_call(elapsed_ms, calls, dist.world)
-    per_T_raw, launches = time_phases(wl, args.steps, min(args.warmup, 3))
+    per_T_raw, launches, cold = time_phases(wl, args.steps, min(args.warmup, 3))
     e2e_ms, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
     e2e_ms = dist.max(e2e_ms)
     per_T = {}
@@ -747,7 +784,8 @@ def run_ours(args, dist: Dist):
         per_T[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                          "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
-                         "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+                         "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm, 3),
+                         "cold_us": round(statistics.median(cold[T]) * 1000, 2)}
     # roofline: the T = 32 calls (the bandwidth-bound end of the decode range)
     big = max(wl.tokens)
     l32 = [(wl.alg_bytes(ly), ms) for ms, ly in per_T_raw[big]]
@@ -771,7 +809,7 @@ def run_ours(args, dist: Dist):
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "traffic_source": "profiles/decode_traffic.md" if traffic is not None else None,
+                     "traffic_source": "profiles/decode_traffic.json" if traffic is not None else None,
                      "alg_bytes_per_launch": int(tot_b / max(len(l32), 1)),
                      "avg_launch_us": round(tot_ms / max(len(l32), 1) * 1000, 2)},
         "e2e": {"value": round(aggregate_us_per_call(e2e_ms, calls, dist.world), 3),
@@ -782,7 +820,7 @@ def run_ours(args, dist: Dist):
         "wall_s_timed_region": round(t_wall, 3),
     }
     if dist.rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_oracle_sample(wl)
+        out["cpu_baseline"], out["parity"] = cpu_oracle_sample(wl)
     del wl
     torch.cuda.empty_cache()
     if not args.no_configs:
@@ -798,47 +836,53 @@ def run_ours(args, dist: Dist):
 
 
 def run_reference(args, dist: Dist):
-    """The CPU oracle as the reference arm, on the same workload."""
+    """The CPU oracle as the reference arm, on the same workload: each step is
+    one call at the next T of the mix 1, 4, 16, 32 (the routing of the GPU
+    arm's layer of that T, random packed weights for the experts it touches);
+    value = the mean over the T of the mean time per call, as the headline's."""
     if dist.rank != 0:
         return None
     from oracle import mxfp4_moe_oracle as O
     s = synth.SHAPES["gptoss128"]
-    rng = np.random.Generator(np.random.PCG64(0))
-    T = 1
-    hidden, _, ids, w = synth.draw_activations(s, T, rng)
-    ids = ids.numpy().astype(np.int64)
-    used = np.unique(ids)
-    remap = np.full(s.E, -1)
-    remap[used] = np.arange(len(used))
-    g = np.random.Generator(np.random.PCG64(1))
-    n = len(used)
-    w13 = g.integers(0, 256, (n, 2 * s.I, s.K // 2), dtype=np.uint8)
-    s13 = g.integers(118, 125, (n, 2 * s.I, s.K // 32), dtype=np.uint8)
-    w2 = g.integers(0, 256, (n, s.K, s.I // 2), dtype=np.uint8)
-    s2 = g.integers(118, 125, (n, s.K, s.I // 32), dtype=np.uint8)
-    hb = hidden.view(torch.int16).numpy().view(np.uint16)
-    args_ = (hb, remap[ids], w.numpy(), w13, s13, w2, s2)
-    for _ in range(args.warmup):
-        O.forward(*args_)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        O.forward(*args_)
-    el = time.perf_counter() - t0
-    us = el / args.steps * 1e6
-    try:
-        from threadpoolctl import threadpool_info
-        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        cores = os.cpu_count()
+    tokens = DecodeWorkload.tokens
+    calls = {}
+    for l, T in enumerate(tokens):
+        hidden, _, ids, w = synth.draw_activations(s, T, np.random.Generator(np.random.PCG64(l)))
+        ids = ids.numpy().astype(np.int64)
+        used = np.unique(ids)
+        remap = np.full(s.E, -1)
+        remap[used] = np.arange(len(used))
+        g = np.random.Generator(np.random.PCG64(100 + l))
+        n = len(used)
+        w13 = g.integers(0, 256, (n, 2 * s.I, s.K // 2), dtype=np.uint8)
+        s13 = g.integers(118, 125, (n, 2 * s.I, s.K // 32), dtype=np.uint8)
+        w2 = g.integers(0, 256, (n, s.K, s.I // 2), dtype=np.uint8)
+        s2 = g.integers(118, 125, (n, s.K, s.I // 32), dtype=np.uint8)
+        hb = hidden.view(torch.int16).numpy().view(np.uint16)
+        calls[T] = (hb, remap[ids], w.numpy(), w13, s13, w2, s2)
+    for i in range(args.warmup):
+        O.forward(*calls[tokens[i % len(tokens)]])
+    per_T = {T: [] for T in tokens}
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        T = tokens[i % len(tokens)]
+        t0 = time.perf_counter()
+        O.forward(*calls[T])
+        per_T[T].append(time.perf_counter() - t0)
+    el = time.perf_counter() - t_all
+    us = statistics.mean(statistics.mean(v) for v in per_T.values() if v) * 1e6
+    cores = _host_cores()
     return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us_per_call",
             "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": decode_config(s, DecodeWorkload.tokens, DecodeWorkload.layers),
+            "config": decode_config(s, tokens, DecodeWorkload.layers),
+            "per_T_us": {str(T): round(statistics.mean(v) * 1e6, 1) for T, v in per_T.items() if v},
             "cpu_baseline": {"value": round(us, 1), "unit": "us_per_call", "cores": cores,
                              "kind": "oracle",
-                             "sample": "each step: one T=1 call of the workload (4 touched "
-                                       "experts), float64 numpy oracle"},
+                             "sample": "each step: one call at the next T of the mix 1, 4, 16, "
+                                       "32 (float64 numpy oracle, touched experts only); value "
+                                       "= mean over the T of the mean time per call"},
             "e2e": {"value": round(us, 1), "unit": "us_per_call", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
