@@ -16,9 +16,10 @@ line carries the same measurement, shorter, under ``prefill``.
 Printed: one JSON line (rank 0). ``value`` is microseconds per MoE call
 (whole job: all calls of all ranks / time), taken from CUDA-graph replays of
 the step with events on the replay stream. ``per_T`` and ``roofline`` come
-from a second pass in which each layer's call (one cooperative decode launch:
-w13 + SwiGLU, w2, combine) is its own graph, replayed alone between CUDA
-events, against the touched experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
+from a second pass at each T: a chain of 8 calls (one cooperative decode
+launch each: w13 + SwiGLU, w2, combine) on 8 distinct layers captured in one
+graph, median replay time / 8 (the pages' protocol), against the touched
+experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
 with host buffers (pinned host -> device copies of each call's activations and
 routing, device -> host copy of its output, inside the timed region).
 ``--impl reference`` times the CPU oracle on the same workload instead.
@@ -407,18 +408,75 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
     return out
 
 
-CONFIG_LAYERS = 8
+CHAIN = 8          # calls (distinct layers) per timed chain
+
+
+def time_chain(fwd, calls, stream, reps: int = 20, warmup: int = 3, cold_reps: int = 3):
+    """The pages' timing protocol ("MXFP4 MoE decode kernels", Measured
+    results: a chain of 8 calls in a graph, median of replays): the CHAIN
+    calls, each on its own layer's weights so that no call finds its experts
+    in L2 from the call before, are captured back to back in one CUDA graph;
+    each replay is timed with CUDA events on the replay stream and the median
+    replay time / CHAIN is the time per call. The cold cross-check times a
+    graph of [1 GiB L2 scrub, one call] against a graph of the scrub alone;
+    the difference is one call that starts with nothing in L2.
+    calls: list of (args, kwargs) for fwd. Returns (us per call, cold us)."""
+    with torch.cuda.stream(stream):
+        for a, k in calls:
+            fwd(*a, **k)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for a, k in calls:
+            fwd(*a, **k)
+    times = []
+    with torch.cuda.stream(stream):
+        for r in range(warmup + reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            if r >= warmup:
+                times.append(e0.elapsed_time(e1) / len(calls))
+    scrub = torch.empty(1 << 30, dtype=torch.uint8, device=calls[0][0][0].device)
+    gs, gc = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gs, stream=stream):
+        scrub.fill_(1)
+    a, k = calls[0]
+    with torch.cuda.graph(gc, stream=stream):
+        scrub.fill_(2)
+        fwd(*a, **k)
+    ts, tc = [], []
+    with torch.cuda.stream(stream):
+        for r in range(1 + cold_reps):
+            for gr, lst in ((gs, ts), (gc, tc)):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                gr.replay()
+                e1.record(stream)
+                stream.synchronize()
+                if r >= 1:
+                    lst.append(e0.elapsed_time(e1))
+    del g, gs, gc, scrub
+    return statistics.median(times) * 1000, (statistics.median(tc) - statistics.median(ts)) * 1000
+
+
+def per_call_figures(us: float, alg_bytes: float, hbm_gbs: float):
+    gbs = alg_bytes / (us * 1e-6) / 1e9
+    return {"us": round(us, 2), "alg_bytes": int(alg_bytes), "gbs": round(gbs, 1),
+            "frac_of_8tbs": round(gbs / 8000.0, 3), "frac_of_measured": round(gbs / hbm_gbs, 3)}
 
 
 def measure_configs(dev, hbm_gbs: float, reps: int = 10):
-    """The other decode workload shapes (the 32-expert single layer at T = 1,
-    the 6144 x 2048 256-expert layer at T = 1, 8, 32 and the wide-K skewed
-    layer at T = 1 .. 32) and the gpt-oss form of the 2880 x 2880 128-expert
-    layer (interleaved gate/up rows, biases, SwiGLU-OAI; T = 1 .. 32):
-    microseconds per call and GB/s of the touched experts' packed bytes, from
-    CUDA-graph replays of single calls that rotate over eight layers of
-    weights, so no call finds its experts in L2 from an earlier replay (at
-    T = 1 the smallest shape touches 53 MB a call, 423 MB over the ring)."""
+    """The other decode workload shapes (the 32-expert single layer, the
+    6144 x 2048 256-expert layer at T = 1, 8, 32 and the wide-K skewed layer
+    at T = 1 .. 32) and the gpt-oss form of the 2880 x 2880 128-expert layer
+    (interleaved gate/up rows, biases, SwiGLU-OAI): microseconds per call and
+    GB/s of the touched experts' packed bytes, from chains of 8 calls on 8
+    distinct layers (time_chain)."""
     from mxfp4_mixture_experts_gb300 import moe
     out = {}
     stream = torch.cuda.Stream()
@@ -426,57 +484,33 @@ def measure_configs(dev, hbm_gbs: float, reps: int = 10):
         oai = name.endswith("_oai")
         sh = synth.SHAPES[name[:-4] if oai else name]
         Ts = (1, 4, 16, 32) if name in ("single32", "gptoss128_oai") else sh.tokens
-        layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev)
-                  for l in range(CONFIG_LAYERS)]
+        layers = [synth.draw_weights_cuda(sh, seed=0, layer=l, device=dev) for l in range(CHAIN)]
+        biases = ([tuple(b.to(dev) for b in synth.draw_biases(sh, seed=0, layer=l))
+                   for l in range(CHAIN)] if oai else None)
         res = {}
         for T in Ts:
             ws = moe.new_workspace(T, sh.K, sh.I, sh.E, sh.topk, dev)
-            calls = []
+            calls, D = [], []
             for l, (w13, s13, w2, s2) in enumerate(layers):
                 rng = np.random.Generator(np.random.PCG64(1000 * T + l))
                 hidden, _, ids, w = synth.draw_activations(sh, T, rng)
                 x, ids, w = hidden.to(dev), ids.to(dev), w.to(dev)
                 y = torch.empty(T, sh.K, dtype=torch.bfloat16, device=dev)
                 if oai:   # the gpt-oss form: the same bytes, interleaved rows, biases
-                    b13, b2 = (b.to(dev) for b in synth.draw_biases(sh, seed=0, layer=l))
-                    args = (x, ids, w, w13, s13, b13, w2, s2, b2)
-                    fwd = moe.forward_oai
+                    b13, b2 = biases[l]
+                    calls.append(((x, ids, w, w13, s13, b13, w2, s2, b2), dict(out=y, workspace=ws)))
                 else:
-                    args = (x, ids, w, w13, s13, w2, s2)
-                    fwd = moe.forward
-                with torch.cuda.stream(stream):
-                    fwd(*args, out=y, workspace=ws)
-                stream.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    fwd(*args, out=y, workspace=ws)
-                D = touched_experts(ids, sh.E)
-                calls.append((g, D * expert_bytes(sh.K, sh.I) + 4 * T * sh.K, D, args, y))
-            times, bytes_ = [], []
-            with torch.cuda.stream(stream):
-                for r in range(reps + 2):
-                    for g, b, D, _, _ in calls:
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
-                        g.replay()
-                        e1.record(stream)
-                        stream.synchronize()
-                        if r >= 2:
-                            times.append(e0.elapsed_time(e1))
-                            bytes_.append(b)
-            ms = statistics.median(times)
-            b = statistics.mean(bytes_)
-            res[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
-                           "touched": [c[2] for c in calls],
-                           "gbs": round(b / (ms * 1e-3) / 1e9, 1),
-                           "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
-                           "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm_gbs, 3)}
+                    calls.append(((x, ids, w, w13, s13, w2, s2), dict(out=y, workspace=ws)))
+                D.append(touched_experts(ids, sh.E))
+            us, cold = time_chain(moe.forward_oai if oai else moe.forward, calls, stream, reps=reps)
+            alg = statistics.mean(D) * expert_bytes(sh.K, sh.I) + 4 * T * sh.K
+            res[str(T)] = dict(per_call_figures(us, alg, hbm_gbs), touched=D,
+                               cold_us=round(cold, 2))
             del calls, ws
         out[name] = {"K": sh.K, "I": sh.I, "E": sh.E, "topk": sh.topk, "per_T": res}
         if oai:
             out[name]["form"] = "gpt-oss: interleaved gate/up rows, f32 biases, SwiGLU-OAI"
-        del layers
+        del layers, biases
         torch.cuda.empty_cache()
     return out
 
@@ -601,59 +635,28 @@ def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     return e0.elapsed_time(e1), ck, t_wall
 
 
-def time_phases(wl, steps: int, warmup: int):
-    """Per-call kernel time: each layer's call is captured as its own CUDA
-    graph (one cooperative decode launch) and replayed alone, with CUDA events
-    on the replay stream; the layers rotate, so no call finds its weights in
-    L2 from the previous replay."""
+def time_per_T(wl, reps: int):
+    """Per-call time at each T of the headline workload: chains of CHAIN calls
+    at one T on the workload's 8 distinct layers (time_chain), with the
+    touched experts' algorithmic bytes of each call."""
     stream = torch.cuda.Stream()
-    graphs = {}
-    with torch.cuda.stream(stream):
-        for l, ly in enumerate(wl.L):
-            wl.call(ly)
-    stream.synchronize()
-    for l, ly in enumerate(wl.L):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            wl.call(ly)
-        graphs[l] = g
-    per_T = {T: [] for T in wl.tokens}
-    launches = []          # (algorithmic bytes, ms) per launch
-    with torch.cuda.stream(stream):
-        for s in range(warmup + steps):
-            evs = []
-            for l in range(len(wl.L)):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graphs[l].replay()
-                e1.record(stream)
-                evs.append((l, e0, e1))
-            stream.synchronize()
-            if s < warmup:
-                continue
-            for l, e0, e1 in evs:
-                ly = wl.L[l]
-                ms = e0.elapsed_time(e1)
-                per_T[ly["T"]].append((ms, ly))
-                launches.append((wl.alg_bytes(ly), ms))
-    # cross-check: single cold calls, each after writing 1 GiB (8x the L2) so
-    # nothing of the call's weights or activations is left in L2
-    cold = {T: [] for T in wl.tokens}
-    scrub = torch.empty(1 << 30, dtype=torch.uint8, device=wl.dev)
-    with torch.cuda.stream(stream):
-        for r in range(3):
-            for l, ly in enumerate(wl.L):
-                scrub.fill_(r + 1)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                graphs[l].replay()
-                e1.record(stream)
-                stream.synchronize()
-                cold[ly["T"]].append(e0.elapsed_time(e1))
-    del scrub
-    return per_T, launches, cold
+    s = wl.shape
+    out = {}
+    for T in wl.tokens:
+        ws = wl.moe.new_workspace(T, s.K, s.I, s.E, s.topk, wl.dev)
+        calls, alg = [], []
+        for l, ly in enumerate(wl.L[:CHAIN]):
+            rng = np.random.Generator(np.random.PCG64(1000 * T + l))
+            hidden, _, ids, w = synth.draw_activations(s, T, rng)
+            x, ids, w = hidden.to(wl.dev), ids.to(wl.dev), w.to(wl.dev)
+            y = torch.empty(T, s.K, dtype=torch.bfloat16, device=wl.dev)
+            calls.append(((x, ids, w, ly["w13"], ly["s13"], ly["w2"], ly["s2"]),
+                          dict(out=y, workspace=ws)))
+            alg.append(touched_experts(ids, s.E) * expert_bytes(s.K, s.I) + 4 * T * s.K)
+        us, cold = time_chain(wl.moe.forward, calls, stream, reps=reps)
+        out[T] = (us, statistics.mean(alg), cold)
+        del calls, ws
+    return out
 
 
 # Sources that make up each kernel: a profile summary under profiles/ records
@@ -773,29 +776,22 @@ def run_ours(args, dist: Dist):
     elapsed_ms = dist.max(elapsed_ms)
     calls = args.steps * wl.calls_per_step
     value = aggregate_us_per_call(elapsed_ms, calls, dist.world)
-    per_T_raw, launches, cold = time_phases(wl, args.steps, min(args.warmup, 3))
+    per_T_raw = time_per_T(wl, reps=max(args.steps, 10))
     e2e_ms, h2d, d2h = time_e2e(wl, args.steps, args.warmup)
     e2e_ms = dist.max(e2e_ms)
-    per_T = {}
     hbm = peaks["hbm_gbs"]
-    for T, recs in per_T_raw.items():
-        ms = statistics.median([r[0] for r in recs])
-        b = statistics.mean([wl.alg_bytes(r[1]) for r in recs])
-        per_T[str(T)] = {"us": round(ms * 1000, 2), "alg_bytes": int(b),
-                         "gbs": round(b / (ms * 1e-3) / 1e9, 1),
-                         "frac_of_8tbs": round(b / (ms * 1e-3) / 8e12, 3),
-                         "frac_of_measured": round(b / (ms * 1e-3) / 1e9 / hbm, 3),
-                         "cold_us": round(statistics.median(cold[T]) * 1000, 2)}
-    # roofline: the T = 32 calls (the bandwidth-bound end of the decode range)
+    per_T = {str(T): dict(per_call_figures(us, b, hbm), cold_us=round(cold, 2))
+             for T, (us, b, cold) in per_T_raw.items()}
+    # roofline: the T = 32 calls (the bandwidth-bound end of the decode range);
+    # a launch's duration = the chain's time per call (kernel + the gap to the
+    # next launch of the chain)
     big = max(wl.tokens)
-    l32 = [(wl.alg_bytes(ly), ms) for ms, ly in per_T_raw[big]]
-    tot_b = sum(b for b, _ in l32)
-    tot_ms = sum(t for _, t in l32)
-    achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    us32, b32, _ = per_T_raw[big]
+    achieved = b32 / (us32 * 1e-6) / 1e9
     rec = recorded_traffic("decode")
     traffic = None
     if rec is not None:   # ncu DRAM bytes / algorithmic bytes of a launch at this T, scaled
-        traffic = int(rec["dram_over_alg"][str(big)] * tot_b / max(len(l32), 1))
+        traffic = int(rec["dram_over_alg"][str(big)] * b32)
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "us_per_call",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -810,8 +806,10 @@ def run_ours(args, dist: Dist):
                      "frac": round(achieved / hbm, 3), "peak_kind": peak_kind,
                      "traffic": traffic,
                      "traffic_source": "profiles/decode_traffic.json" if traffic is not None else None,
-                     "alg_bytes_per_launch": int(tot_b / max(len(l32), 1)),
-                     "avg_launch_us": round(tot_ms / max(len(l32), 1) * 1000, 2)},
+                     "alg_bytes_per_launch": int(b32),
+                     "avg_launch_us": round(us32, 2),
+                     "timing": f"chains of {CHAIN} calls on {CHAIN} distinct layers at T = {big}, "
+                               "median replay / calls"},
         "e2e": {"value": round(aggregate_us_per_call(e2e_ms, calls, dist.world), 3),
                 "unit": "us_per_call", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},

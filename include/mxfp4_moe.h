@@ -76,11 +76,17 @@ typedef enum {
  * 16-byte aligned; workspace 256-byte aligned. */
 
 /* Bytes of device workspace a forward call with these sizes needs (either
- * path). The first mxfp4_moe_workspace_size(...) bytes must be zero before
- * the first call that uses a workspace; every call leaves the bookkeeping part
- * zero again (also one whose bounded wait gave up), so a workspace can be
- * reused without clearing. Returns 0 for invalid sizes. */
+ * path). The bookkeeping part (the first mxfp4_moe_workspace_zero_bytes()
+ * bytes) must be zero before the first call that uses a workspace; every call
+ * leaves it zero again (also one whose bounded wait gave up), so a workspace
+ * can be reused without clearing. Returns 0 for invalid sizes. */
 size_t mxfp4_moe_workspace_size(int T, int K, int I, int E, int topk);
+
+/* Bytes at the start of every workspace that hold the bookkeeping: they must
+ * be zero before the first call (clearing only them is enough) and every call
+ * leaves them zero. The same for all sizes (a few KB), so a workspace
+ * sized for the largest call serves calls of any smaller size. */
+size_t mxfp4_moe_workspace_zero_bytes(void);
 
 /* Routing / permute ("MXFP4 MoE decode kernels", Design, "Routing inside the
  * kernel": a counting sort of the routes by expert; absent experts skipped).

@@ -79,7 +79,7 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // Workspace layout. The bookkeeping that must be zero between calls comes
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
-  size_t gbar;                                             // zero-kept
+  size_t gbar;                                             // zero-kept, fixed size
   size_t h, P, rcount, roffset, rlist, rinv, xp;           // scratch
   size_t total;
 };
@@ -97,7 +97,9 @@ Layout layout(int T, int K, int I, int E, int topk) {
   const size_t R = (size_t)T * topk;
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
-  L.gbar = take(2 * sizeof(int));
+  // the zero-kept prefix has the same size for every call, so workspaces
+  // sized for one T serve calls of any smaller T
+  L.gbar = take(4 * sizeof(int));
   L.h = take(R * I * 2);
   L.P = take(R * K * sizeof(float));
   L.rcount = take((size_t)E * sizeof(int));
@@ -120,7 +122,7 @@ void record_phase(int i, cudaStream_t s) {
 
 namespace mxmoe {
 // Bytes at the start of every workspace that must be zero when a call starts
-// (the decode launch's grid counters; the same for all sizes).
+// (the decode launch's counters; the same for all sizes).
 size_t workspace_zero_kept_bytes() { return layout(1, 64, 64, 1, 1).h; }
 
 bool encode_tiled_2d(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64_t dim0,
@@ -277,6 +279,8 @@ size_t mxfp4_moe_workspace_size(int T, int K, int I, int E, int topk) {
   if (!shape_ok(T, K, I, E, topk)) return 0;
   return layout(T, K, I, E, topk).total;
 }
+
+size_t mxfp4_moe_workspace_zero_bytes(void) { return mxmoe::workspace_zero_kept_bytes(); }
 
 int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E, int32_t* expert_count,
                     int32_t* expert_offset, int32_t* route_list, int32_t* status, void* stream) {

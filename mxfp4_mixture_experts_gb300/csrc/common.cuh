@@ -48,6 +48,12 @@ __device__ __forceinline__ uint4 ldcg16(const void* p) {
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+// Programmatic dependent launch: allow the next kernel of the stream to be
+// scheduled (it still waits for this grid in its grid_dependency_wait).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 
 // Exact bf16x2 product (inputs and results may be subnormal).
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
@@ -136,6 +142,20 @@ __device__ __forceinline__ void dequant32_bf16(const uint32_t (&wd)[4], const Sc
     o[4 * c + 2] = prmt(p0, p1, 0x7632u);   // (n4, n5)
     o[4 * c + 3] = prmt(p2, p3, 0x7632u);   // (n6, n7)
   }
+}
+
+// silu(z) = z * sigmoid(z) with the fast exponential and division (a few ulp
+// of fp32; the product is rounded to bf16 afterwards).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// SwiGLU-OAI ("MXFP4 MoE decode kernels", Design, Fused epilogues) with the
+// same fast exponential and division: gate capped at 7 (no lower cap), up
+// clamped to [-7, 7], gate * sigmoid(1.702 gate) * (up + 1); comparisons keep
+// a NaN input NaN.
+__device__ __forceinline__ float swiglu_oai_fast(float gate, float up) {
+  gate = gate > 7.0f ? 7.0f : gate;
+  up = up > 7.0f ? 7.0f : (up < -7.0f ? -7.0f : up);
+  return __fdividef(gate, 1.0f + __expf(-1.702f * gate)) * (up + 1.0f);
 }
 
 // fp32 -> bf16 bits, round to nearest even (NaN kept quiet).

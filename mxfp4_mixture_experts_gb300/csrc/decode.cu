@@ -40,8 +40,9 @@
 //    exact power-of-two prescale per row (max |x| lands in [2^14, 2^15)); the
 //    epilogue multiplies it back. Rows that do not fit are converted once, with
 //    the same prescale, into an f16 scratch in global memory and read from
-//    there (generic loads that bypass L1). Thread 0 also waits for the grid
-//    between the phases.
+//    there (generic loads that bypass L1). When a phase needs fewer rows than
+//    the CTA has warps, several warps share each row's conversion. Thread 0
+//    also waits for the grid between the phases.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -124,6 +125,18 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v, float mul) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Largest biased exponent of 8 bf16 values (one uint4).
+__device__ __forceinline__ uint32_t bf16x8_max_exponent(uint4 q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t e = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    e = max(e, (w[i] >> 7) & 0xFFu);
+    e = max(e, (w[i] >> 23) & 0xFFu);
+  }
+  return e;
+}
+
 // An item's routes: expert e, route-list positions q0 .. q0 + cnt - 1 (a batch
 // of at most kBatch of the expert's routes; more than one batch per expert
 // only when a token names the same expert in several slots).
@@ -196,6 +209,29 @@ __device__ __forceinline__ RowPlan row_plan(const PhaseView& v, int xs_rows_cap)
   r.xs_rows = min(min(v.n_need, xs_rows_cap), r.rows_per_bar * kRowBars);
   r.nbars = (r.xs_rows + r.rows_per_bar - 1) / r.rows_per_bar;
   return r;
+}
+
+// Converts part of staged activation row r (16-byte chunks c0, c0 + step, ..)
+// to f16 after the exact power-of-two prescale that puts the row's largest
+// exponent emax at 2^14 (the epilogue multiplies it back): in place when the
+// row is staged in shared memory, else into the f16 scratch in global memory.
+__device__ __forceinline__ void convert_row_part(const DecodeArgs& a, const PhaseView& v,
+                                                 uint8_t* xs, int xs_stride, int* row_sh,
+                                                 const RowPlan& rp, const RouteTables& tb,
+                                                 int phase, int r, uint32_t emax, int c0, int step,
+                                                 bool write_sh) {
+  const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
+  if (write_sh) row_sh[r] = sh;
+  const float mul = pow2f(-sh);
+  if (r < rp.xs_rows) {
+    uint4* row = reinterpret_cast<uint4*>(xs + (size_t)r * xs_stride);
+    for (int c16 = c0; c16 < v.kred / 8; c16 += step) row[c16] = bf16x8_to_f16x8(row[c16], mul);
+  } else {   // rows with no room here: converted once into the f16 scratch
+    const size_t xf_stride = (size_t)(a.K > a.I ? a.K : a.I);
+    const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
+    uint4* dst = reinterpret_cast<uint4*>(a.xf + (size_t)(v.p_lo + r) * xf_stride);
+    for (int c16 = c0; c16 < v.kred / 8; c16 += step) dst[c16] = bf16x8_to_f16x8(ldcg16(src + c16), mul);
+  }
 }
 
 // B operand of one token group for this lane (token column g), at block 0:
@@ -605,6 +641,10 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   tb.touched = tb.run + E;
   tb.lst = tb.touched + E;
   tb.misc = tb.lst + R;
+  // flags[0..2]: grid waits passed, expert-batch count; flags[4..15]: the
+  // exponent maxima of rows whose conversion several warps share (fewer rows
+  // than warps, at most 11)
+  int* rmax = flags + 4;
   int* row_sh = reinterpret_cast<int*>(smem + M.row_sh);          // [R]
   int* eb = reinterpret_cast<int*>(smem + M.eb);                  // [nEB] (expert << 8) | batch
   uint8_t* xs = smem + M.xs;
@@ -614,6 +654,10 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nCta = gridDim.x;
+  // programmatic dependent launch (10- to 12-warp forms): the next call may
+  // be scheduled now; its CTAs start as these exit and wait before touching
+  // global memory
+  if constexpr (CW >= 10) grid_launch_dependents();
 
   if (tid < 16) flags[tid] = 0;
   if (tid == 0) {
@@ -626,6 +670,9 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     prefetch_tensormap(&P.tmap1);
     prefetch_tensormap(&P.tmap2);
   }
+  // everything the previous kernel of the stream wrote (inputs, the
+  // workspace) is visible after this wait
+  if constexpr (CW >= 10) grid_dependency_wait();
   cta_route_small(a.ids, R, E, a.ebase, a.window, tb);   // ends with __syncthreads
   const int nD = tb.misc[0];
   if (warp == 0) {   // expert-batch table: each touched expert's routes in batches of kBatch
@@ -702,6 +749,8 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     const PhaseView& v = phase == 1 ? v1 : v2;
     const RowPlan& rp = phase == 1 ? rp1 : rp2;
     if (phase == 2) {   // h of every CTA is complete (also for rows read from global)
+      if constexpr (CW >= 10)
+        if (ctid >= 32 && ctid < 44) rmax[ctid - 32] = 0;
       if (ctid == 0) {
         flags[1] = grid_wait(gbar, (uint32_t)nCta) ? 1 : 0;
         if (flags[1] != 0) {
@@ -722,31 +771,54 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       if (!ok) fail |= 4;
     }
     if (phase == 1) rows_used = (1u << rp.nbars) - 1u;
-    for (int r = cw; r < v.n_need && ok; r += CW) {
-      const bool staged = r < rp.xs_rows;
-      uint4* row = reinterpret_cast<uint4*>(xs + (size_t)r * xs_stride);
-      const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
-      uint32_t emax = 0;
-      for (int c16 = lane; c16 < v.kred / 8; c16 += 32) {
-        const uint4 q = staged ? row[c16] : ldcg16(src + c16);
-        const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
+    bool shared_rows = false;   // fewer rows than warps: G warps share each row
+    if constexpr (CW >= 10) shared_rows = v.n_need > 0 && v.n_need < CW;
+    if (!shared_rows) {   // one warp per row
+      for (int r = cw; r < v.n_need && ok; r += CW) {
+        const bool staged = r < rp.xs_rows;
+        uint4* row = reinterpret_cast<uint4*>(xs + (size_t)r * xs_stride);
+        const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
+        uint32_t emax = 0;
+        for (int c16 = lane; c16 < v.kred / 8; c16 += 32) {
+          const uint4 q = staged ? row[c16] : ldcg16(src + c16);
+          const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          emax = max(emax, (wq[i] >> 7) & 0xFFu);
-          emax = max(emax, (wq[i] >> 23) & 0xFFu);
+          for (int i = 0; i < 4; ++i) {
+            emax = max(emax, (wq[i] >> 7) & 0xFFu);
+            emax = max(emax, (wq[i] >> 23) & 0xFFu);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
+        if (lane == 0) row_sh[r] = sh;
+        const float mul = pow2f(-sh);
+        if (staged) {
+          for (int c16 = lane; c16 < v.kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
+        } else {   // rows with no room here: converted once into the f16 scratch
+          uint4* dst = reinterpret_cast<uint4*>(a.xf + (size_t)(v.p_lo + r) * xf_stride);
+          for (int c16 = lane; c16 < v.kred / 8; c16 += 32) dst[c16] = bf16x8_to_f16x8(ldcg16(src + c16), mul);
         }
       }
+    } else {
+      const int G = CW / v.n_need;
+      const int r = cw / G, part = cw - r * G;
+      const bool mine = r < v.n_need && ok;
+      if (mine) {
+        const bool staged = r < rp.xs_rows;
+        const uint4* row = reinterpret_cast<const uint4*>(xs + (size_t)r * xs_stride);
+        const uint4* src = reinterpret_cast<const uint4*>(act_row(phase, a, tb, v.p_lo + r));
+        uint32_t emax = 0;
+        for (int c16 = part * 32 + lane; c16 < v.kred / 8; c16 += G * 32)
+          emax = max(emax, bf16x8_max_exponent(staged ? row[c16] : ldcg16(src + c16)));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-      const int sh = max(-100, min(100, emax == 0 ? 0 : (int)emax - 127 - 14));
-      if (lane == 0) row_sh[r] = sh;
-      const float mul = pow2f(-sh);
-      if (staged) {
-        for (int c16 = lane; c16 < v.kred / 8; c16 += 32) row[c16] = bf16x8_to_f16x8(row[c16], mul);
-      } else {   // rows with no room here: converted once into the f16 scratch
-        uint4* dst = reinterpret_cast<uint4*>(a.xf + (size_t)(v.p_lo + r) * xf_stride);
-        for (int c16 = lane; c16 < v.kred / 8; c16 += 32) dst[c16] = bf16x8_to_f16x8(ldcg16(src + c16), mul);
+        for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        if (lane == 0) atomicMax(&rmax[r], (int)emax);
       }
+      named_barrier(kBarConsumers, kThreadsCW);
+      if (mine)
+        convert_row_part(a, v, xs, xs_stride, row_sh, rp, tb, phase, r, (uint32_t)rmax[r],
+                         part * 32 + lane, G * 32, part == 0 && lane == 0);
     }
     named_barrier(kBarConsumers, kThreadsCW);
 
@@ -986,11 +1058,15 @@ static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cu
   cfg.blockDim = dim3(CW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  // the 10- to 12-warp forms may overlap the tail of the previous kernel in
+  // the stream (the kernel waits for it before reading anything)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CW >= 10 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel<CW>, p);
 }
 

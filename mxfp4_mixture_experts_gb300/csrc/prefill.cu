@@ -132,19 +132,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
-// silu(z) = z * sigmoid(z) with the fast exponential and division (a few ulp
-// of fp32; the product is rounded to bf16 afterwards).
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
-
-// SwiGLU-OAI ("MXFP4 MoE decode kernels", Design, Fused epilogues) with the
-// same fast exponential and division: gate capped at 7, up clamped to
-// [-7, 7], gate * sigmoid(1.702 gate) * (up + 1); comparisons keep NaN.
-__device__ __forceinline__ float swiglu_oai_fast(float gate, float up) {
-  gate = gate > 7.0f ? 7.0f : gate;
-  up = up > 7.0f ? 7.0f : (up < -7.0f ? -7.0f : up);
-  return __fdividef(gate, 1.0f + __expf(-1.702f * gate)) * (up + 1.0f);
-}
-
 template <int PHASE, bool OAI>
 __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];

@@ -39,6 +39,8 @@ def lib() -> ctypes.CDLL:
     vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     L.mxfp4_moe_workspace_size.argtypes = [i32] * 5
     L.mxfp4_moe_workspace_size.restype = sz
+    L.mxfp4_moe_workspace_zero_bytes.argtypes = []
+    L.mxfp4_moe_workspace_zero_bytes.restype = sz
     L.mxfp4_moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.mxfp4_moe_route.restype = i32
     L.mxfp4_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
@@ -105,6 +107,12 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
 
 def workspace_size(T: int, K: int, I: int, E: int, topk: int) -> int:
     return int(lib().mxfp4_moe_workspace_size(T, K, I, E, topk))
+
+
+def workspace_zero_bytes() -> int:
+    """Bytes at the start of a workspace that must be zero before first use
+    (every call leaves them zero)."""
+    return int(lib().mxfp4_moe_workspace_zero_bytes())
 
 
 def new_workspace(T: int, K: int, I: int, E: int, topk: int, device="cuda") -> torch.Tensor:

@@ -264,3 +264,11 @@ def test_noalloc_array_holds_the_decode_workspace_of_every_workload_shape(L):
         s = synth.SHAPES[name]
         need = L.mxfp4_moe_workspace_size(32, s.K, s.I, s.E, s.topk)
         assert 0 < need <= cap, (name, need, cap)
+
+
+def test_workspace_zero_prefix_is_fixed_and_inside_every_workspace(L):
+    from mxfp4_mixture_experts_gb300 import moe
+    z = moe.workspace_zero_bytes()
+    assert 0 < z <= 16 * 1024 and z % 256 == 0
+    for T in (1, 7, 32, 33, 8192):
+        assert L.mxfp4_moe_workspace_size(T, 2880, 2880, 128, 4) > z

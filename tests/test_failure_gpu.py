@@ -53,7 +53,7 @@ def test_missing_arrival_is_reported_and_the_workspace_stays_usable(moe, cta):
     assert s2 & GRID_WAIT_COMBINE, hex(s2)
     assert 1 <= int(status[3]) <= nsm
     # the kernel's last CTA reset the grid counters on its way out
-    assert torch.count_nonzero(ws[:256]).item() == 0
+    assert torch.count_nonzero(ws[:moe.workspace_zero_bytes()]).item() == 0
     # the same workspace, not cleared by the caller, serves the next call
     status.zero_()
     y = moe.forward(g.hidden, g.topk_ids, g.topk_weights, g.w13, g.s13, g.w2, g.s2,

@@ -53,7 +53,8 @@ def test_writes_stay_inside_out_and_workspace(moe, name, T, path):
     assert int(status[2]) == 0
     assert guards_intact(out_buf), "a write landed next to the output"
     assert guards_intact(ws_buf), "a write landed next to the workspace"
-    assert torch.count_nonzero(ws[:256]).item() == 0, "bookkeeping bytes not left at zero"
+    assert torch.count_nonzero(ws[:moe.workspace_zero_bytes()]).item() == 0, \
+        "bookkeeping bytes not left at zero"
     assert torch.isfinite(out.float()).all()
     for a, b in zip(keep, (x, ids, w, s13, s2)):
         assert torch.equal(a, b), "an input was modified"
