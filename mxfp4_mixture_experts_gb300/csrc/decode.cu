@@ -16,7 +16,8 @@
 //
 // One CTA per SM; every warp is a consumer: 10 to 12 warps with 3-deep rings
 // when the activation rows a CTA is expected to need fit in shared memory
-// next to the rings, else 8 warps with 4-deep rings (decode_warps).
+// next to the rings, else 8 warps, which leave the most room for rows
+// (decode_warps).
 //  * Work item = 16 weight rows of one touched expert over the whole
 //    reduction (phase 1: gate rows i0..i0+7 and the matching up rows; phase 2:
 //    16 w2 rows) times up to 32 of the expert's routes. A phase's items are
@@ -52,8 +53,9 @@
 
 namespace mxmoe {
 
-// stages in each warp's ring: 4 with 8 warps, 3 with 10 to 12 (shared memory)
-__host__ __device__ constexpr int ring_depth(int cw) { return cw >= 10 ? 3 : 4; }
+// stages in each warp's ring: 3 (a 4-deep ring in the 8-warp form took the
+// shared memory that activation rows need: measured slower on every shape)
+__host__ __device__ constexpr int ring_depth(int) { return 3; }
 constexpr int kRows = 16;                    // weight rows per item (one m16 tile)
 constexpr int kChunk = 256;                  // packed bytes per row per stage
 constexpr int kChunkBlocks = kChunk / 16;    // 16 scale blocks per stage
@@ -1002,19 +1004,20 @@ static int routes_per_expert_p99(int T, int topk, int E) {
   return T;
 }
 
-// Warps per CTA: the most of 12, 11 or 10 (3-deep rings; more warps hide more
-// of the latency of the conversion and MMA chain) whose rings, scale slots and
-// the activation rows a CTA is expected to need all fit. A CTA's items span
-// one or two expert batches, so it needs the rows of those experts' routes:
-// at most 2 m99 (m99 from routes_per_expert_p99), and 3 rho + 3 covered the
+// Warps per CTA: the most of 12, 11 or 10 (more warps hide more of the
+// latency of the conversion and MMA chain) whose rings, scale slots and the
+// activation rows a CTA is expected to need all fit. A CTA's items span one
+// or two expert batches, so it needs the rows of those experts' routes: at
+// most 2 m99 (m99 from routes_per_expert_p99), and 3 rho + 3 covered the
 // largest need of every CTA on the workload shapes (rho = R / (E (1 - (1 -
 // 1/E)^R)), the expected routes per touched expert). When those rows do not
-// fit next to any of them: 10 warps anyway (its batched reads of the f16
-// scratch) if experts with more than 8 routes are unlikely (m99 <= 5; their
-// items would take the per-block path of that form), else 8 warps (4-deep rings, batched paths for rows read from
-// the f16 scratch and for items with several token groups). 0 when even 8
-// warps do not fit. Rows beyond the staged ones are read from the f16 scratch
-// in global memory (correct for any routing, only slower).
+// fit next to any of them: 8 warps, the form with the most room for rows
+// (and batched paths for rows read from the f16 scratch and for items with
+// several token groups) -- an item whose rows are not all staged reads them
+// through L2 on every block and runs about 1.5x longer, which decides the
+// call's time through the slowest CTA. 0 when even 8 warps do not fit. Rows
+// beyond the staged ones are read from the f16 scratch in global memory
+// (correct for any routing, only slower).
 int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
   const int R = T * topk;
   const int stride = decode_row_stride(K, I);
@@ -1025,7 +1028,6 @@ int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
   if (want > R) want = R;
   for (int cw = 12; cw >= 10; --cw)
     if (decode_smem_bytes(cw, K, I, E, R, want, stride) <= (size_t)max_smem) return cw;
-  if (m99 <= 5 && decode_smem_bytes(10, K, I, E, R, 1, stride) <= (size_t)max_smem) return 10;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
 }
