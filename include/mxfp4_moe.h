@@ -102,6 +102,20 @@ int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E,
                     int32_t* expert_count, int32_t* expert_offset, int32_t* route_list,
                     int32_t* status, void* stream);
 
+/* The same routing with device scratch for many routes: identical outputs
+ * (bit for bit) to mxfp4_moe_route. From 8192 routes on it sorts over many
+ * CTAs -- per-chunk expert counts, one prefix pass, an in-order placement per
+ * chunk -- which is the form the prefill path runs; fewer routes take the
+ * one-CTA sort. workspace: device memory of at least
+ * mxfp4_moe_route_workspace_size(T, topk, E) bytes, 16-byte aligned
+ * (MXFP4_MOE_ERR_WORKSPACE / MXFP4_MOE_ERR_ALIGN), no initial contents
+ * required, not shared by calls that may run concurrently. Other arguments,
+ * limits and errors as mxfp4_moe_route. */
+size_t mxfp4_moe_route_workspace_size(int T, int topk, int E);
+int mxfp4_moe_route_ws(const int32_t* topk_ids, int T, int topk, int E,
+                       int32_t* expert_count, int32_t* expert_offset, int32_t* route_list,
+                       int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Router: the step before routing ("MXFP4 MoE decode kernels", Design, "Routing
  * inside the kernel" takes its top-k ids; the workload shapes fix the
  * scoring). Per token t:

@@ -80,7 +80,7 @@ size_t up256(size_t n) { return (n + 255) & ~size_t(255); }
 // first; the scratch regions after it are overwritten by every call.
 struct Layout {
   size_t gbar;                                             // zero-kept, fixed size
-  size_t h, P, rcount, roffset, rlist, rinv, xp;           // scratch
+  size_t h, P, rcount, roffset, rlist, rinv, rpart, xp;    // scratch
   size_t total;
 };
 
@@ -106,6 +106,7 @@ Layout layout(int T, int K, int I, int E, int topk) {
   L.roffset = take((size_t)(E + 1) * sizeof(int));
   L.rlist = take(R * sizeof(int));
   L.rinv = take(R * sizeof(int));
+  L.rpart = take(route_part_ints(E) * sizeof(int));
   L.xp = take(R * (size_t)(K > I ? K : I) * 2);   // (decode: the f16 row scratch)
   L.total = o;
   return L;
@@ -261,6 +262,7 @@ int run_prefill(const void* hidden, const int32_t* topk_ids, const float* topk_w
   p.hp = reinterpret_cast<uint16_t*>(ws + L.h);   // SwiGLU output, expert order
   p.P = reinterpret_cast<float*>(ws + L.P);
   p.inv = reinterpret_cast<int32_t*>(ws + L.rinv);
+  p.rpart = reinterpret_cast<int32_t*>(ws + L.rpart);
   p.num_sms = d->num_sms;
   p.b13 = b13;
   p.b2 = b2;
@@ -292,6 +294,28 @@ int mxfp4_moe_route(const int32_t* topk_ids, int T, int topk, int E, int32_t* ex
   if (int rc = current_device(&d)) return rc;
   return cuda_status(launch_route(topk_ids, T * topk, E, 0, 0, expert_count, expert_offset, route_list,
                                   status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxfp4_moe_route_workspace_size(int T, int topk, int E) {
+  if (T < 0 || topk < 1 || topk > 32 || E < 1 || E > kMaxExperts) return 0;
+  return route_part_ints(E) * sizeof(int);
+}
+
+int mxfp4_moe_route_ws(const int32_t* topk_ids, int T, int topk, int E, int32_t* expert_count,
+                       int32_t* expert_offset, int32_t* route_list, int32_t* status,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || topk < 1 || topk > 32 || E < 1 || E > kMaxExperts) return MXFP4_MOE_ERR_SHAPE;
+  if (expert_count == nullptr || expert_offset == nullptr) return MXFP4_MOE_ERR_ARG;
+  if (T > 0 && (topk_ids == nullptr || route_list == nullptr)) return MXFP4_MOE_ERR_ARG;
+  if ((int64_t)T * topk >= ((int64_t)1 << 30)) return MXFP4_MOE_ERR_SHAPE;
+  if (workspace == nullptr || workspace_bytes < route_part_ints(E) * sizeof(int))
+    return MXFP4_MOE_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return MXFP4_MOE_ERR_ALIGN;
+  DeviceInfo* d = nullptr;
+  if (int rc = current_device(&d)) return rc;
+  return cuda_status(launch_route_parts(topk_ids, T * topk, E, 0, 0, expert_count, expert_offset,
+                                        route_list, status, static_cast<int32_t*>(workspace),
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 int mxfp4_moe_forward(const void* hidden, const int32_t* topk_ids, const float* topk_weights,

@@ -84,6 +84,15 @@ bool encode_tiled_u8(CUtensorMap* m, const void* base, int rank, const uint64_t*
 cudaError_t launch_route(const int32_t* ids, int R, int E, int ebase, int window, int32_t* count,
                          int32_t* offset, int32_t* list, int32_t* status, cudaStream_t stream);
 
+// The same sort over many CTAs for many routes (R >= kRoutePartMin; fewer go
+// to launch_route): part is device scratch of route_part_ints(E) ints.
+constexpr int kRoutePartCtas = 128;
+constexpr int kRoutePartMin = 8192;
+size_t route_part_ints(int E);
+cudaError_t launch_route_parts(const int32_t* ids, int R, int E, int ebase, int window,
+                               int32_t* count, int32_t* offset, int32_t* list, int32_t* status,
+                               int32_t* part, cudaStream_t stream);
+
 // MXFP4 encoder: bf16 [rows, cols] (cols % 32 == 0) -> packed [rows, cols/2]
 // and E8M0 scales [rows, cols/32]; quark != 0 takes the Quark exponent rule
 // (encode.cu).

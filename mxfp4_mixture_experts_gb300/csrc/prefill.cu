@@ -547,8 +547,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream, void* cons
   };
   const int R = a.T * a.topk;
   rec(0);
-  cudaError_t e = launch_route(a.ids, R, a.E, a.ebase, a.window, a.count, a.offset, a.list,
-                               a.status, stream);
+  cudaError_t e = launch_route_parts(a.ids, R, a.E, a.ebase, a.window, a.count, a.offset, a.list,
+                                     a.status, a.rpart, stream);
   if (e != cudaSuccess) return e;
   int gblocks = a.num_sms * 8;
   gather_kernel<<<gblocks, 256, 0, stream>>>(a.hidden, a.list, a.offset + a.E, a.K, a.topk, a.xp,

@@ -24,6 +24,7 @@ struct PrefillArgs {
   uint16_t* hp;             // bf16 [R, I], rows in expert order
   float* P;                 // fp32 [R, K], rows in expert order, unweighted
   int32_t* inv;             // [R] route -> row of P
+  int32_t* rpart;           // route_part_ints(E): scratch of the many-CTA route sort
   int num_sms;
   // gpt-oss form (oai != 0): w13 rows interleaved (row 2i gate i, row 2i + 1
   // up i), f32 biases b13 [E, 2I] (same row order) and b2 [E, K], SwiGLU-OAI

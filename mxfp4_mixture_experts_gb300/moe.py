@@ -43,6 +43,10 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_workspace_zero_bytes.restype = sz
     L.mxfp4_moe_route.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.mxfp4_moe_route.restype = i32
+    L.mxfp4_moe_route_workspace_size.argtypes = [i32, i32, i32]
+    L.mxfp4_moe_route_workspace_size.restype = sz
+    L.mxfp4_moe_route_ws.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+    L.mxfp4_moe_route_ws.restype = i32
     L.mxfp4_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                     vp, vp, vp, sz, i32, vp]
     L.mxfp4_moe_forward.restype = i32
@@ -123,9 +127,11 @@ def new_workspace(T: int, K: int, I: int, E: int, topk: int, device="cuda") -> t
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def route(topk_ids: torch.Tensor, E: int, stream=None):
+def route(topk_ids: torch.Tensor, E: int, stream=None, many_ctas: bool = False):
     """Stable counting sort of routes by expert -> (count[E], offset[E+1],
-    route_list[T*k], status[4]), all int32 CUDA tensors."""
+    route_list[T*k], status[4]), all int32 CUDA tensors. many_ctas takes
+    mxfp4_moe_route_ws (the prefill path's sort, over many CTAs from 8192
+    routes on) with scratch allocated here."""
     _need(topk_ids, "topk_ids", torch.int32, 2)
     T, k = topk_ids.shape
     dev = topk_ids.device
@@ -133,10 +139,18 @@ def route(topk_ids: torch.Tensor, E: int, stream=None):
     offset = torch.empty(E + 1, dtype=torch.int32, device=dev)
     lst = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
-    rc = lib().mxfp4_moe_route(_ptr(topk_ids), T, k, E, _ptr(count), _ptr(offset), _ptr(lst),
-                               _ptr(status), _stream(stream))
-    if rc:
-        raise MoEError(rc, "mxfp4_moe_route")
+    if many_ctas:
+        n = int(lib().mxfp4_moe_route_workspace_size(T, k, E))
+        ws = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+        rc = lib().mxfp4_moe_route_ws(_ptr(topk_ids), T, k, E, _ptr(count), _ptr(offset),
+                                      _ptr(lst), _ptr(status), _ptr(ws), n, _stream(stream))
+        if rc:
+            raise MoEError(rc, "mxfp4_moe_route_ws")
+    else:
+        rc = lib().mxfp4_moe_route(_ptr(topk_ids), T, k, E, _ptr(count), _ptr(offset),
+                                   _ptr(lst), _ptr(status), _stream(stream))
+        if rc:
+            raise MoEError(rc, "mxfp4_moe_route")
     return count, offset, lst[:T * k], status
 
 

@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("mxfp4_moe_route", "mxfp4_moe_router", "mxfp4_moe_router_grouped",
+    for n in ("mxfp4_moe_route", "mxfp4_moe_route_ws", "mxfp4_moe_router", "mxfp4_moe_router_grouped",
               "mxfp4_moe_forward", "mxfp4_moe_forward_oai",
               "mxfp4_moe_forward_window",
               "mxfp4_moe_dequant", "mxfp4_moe_dequant_form", "mxfp4_moe_encode",
@@ -272,3 +272,16 @@ def test_workspace_zero_prefix_is_fixed_and_inside_every_workspace(L):
     assert 0 < z <= 16 * 1024 and z % 256 == 0
     for T in (1, 7, 32, 33, 8192):
         assert L.mxfp4_moe_workspace_size(T, 2880, 2880, 128, 4) > z
+
+
+def test_route_ws_rejects_bad_arguments(L):
+    from mxfp4_mixture_experts_gb300 import moe as m
+    n = L.mxfp4_moe_route_workspace_size(8192, 8, 256)
+    assert n > 0 and L.mxfp4_moe_route_workspace_size(1, 0, 8) == 0
+    f = L.mxfp4_moe_route_ws
+    assert f(VP(0x1000), 4, 2, 8, VP(0x2000), VP(0x3000), VP(0x4000), None, None, 0, None) == \
+        m.ERR_WORKSPACE
+    assert f(VP(0x1000), 4, 2, 8, VP(0x2000), VP(0x3000), VP(0x4000), None, VP(0x5008), n,
+             None) == m.ERR_ALIGN
+    assert f(VP(0x1000), 4, 0, 8, VP(0x2000), VP(0x3000), VP(0x4000), None, VP(0x5000), n,
+             None) == m.ERR_SHAPE

@@ -17,9 +17,9 @@ def moe():
     return moe
 
 
-def check(moe, ids_np, E):
+def check(moe, ids_np, E, many_ctas=False):
     ids = torch.as_tensor(ids_np, dtype=torch.int32, device="cuda")
-    cnt, off, lst, status = moe.route(ids, E)
+    cnt, off, lst, status = moe.route(ids, E, many_ctas=many_ctas)
     torch.cuda.synchronize()
     rt = O.route(ids_np, E)
     assert np.array_equal(cnt.cpu().numpy(), rt["count"])
@@ -59,3 +59,27 @@ def test_route_skewed_prefill(moe):
     p = rng.dirichlet(np.full(256, 0.3))
     ids = rng.choice(256, size=(8192, 8), p=p).astype(np.int32)
     check(moe, ids, 256)
+
+
+# the prefill path's sort over many CTAs (mxfp4_moe_route_ws): from 8192
+# routes on, chunks of routes per CTA; below, the one-CTA sort
+@pytest.mark.parametrize("T,k,E", [(1000, 8, 256), (1024, 8, 256), (8192, 8, 256), (8191, 3, 1024),
+                                   (16384, 4, 128), (65536, 8, 32), (3000, 3, 7)])
+def test_route_many_ctas_random(moe, T, k, E):
+    rng = np.random.default_rng(T * 7 + k)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    check(moe, ids, E, many_ctas=True)
+
+
+def test_route_many_ctas_padding_invalid_skew(moe):
+    rng = np.random.default_rng(5)
+    p = rng.dirichlet(np.full(256, 0.2))
+    ids = rng.choice(256, size=(8192, 8), p=p).astype(np.int32)
+    ids[rng.random(ids.shape) < 0.05] = -1      # padding
+    ids[rng.random(ids.shape) < 0.02] = 300     # invalid
+    check(moe, ids, 256, many_ctas=True)
+
+
+def test_route_many_ctas_all_to_one_expert(moe):
+    check(moe, np.full((4096, 4), 3, dtype=np.int32), 16, many_ctas=True)
+    check(moe, np.full((4096, 4), -1, dtype=np.int32), 16, many_ctas=True)
