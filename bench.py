@@ -15,7 +15,8 @@ line carries the same measurement, shorter, under ``prefill``.
 
 Printed: one JSON line (rank 0). ``value`` is microseconds per MoE call
 (whole job: all calls of all ranks / time), taken from CUDA-graph replays of
-the step with events on the replay stream. ``per_T`` and ``roofline`` come
+two steps at a time (the 8 calls on the 8 layers, the pages' chain of 8
+calls) with events on the replay stream. ``per_T`` and ``roofline`` come
 from a second pass at each T: a chain of 8 calls (one cooperative decode
 launch each: w13 + SwiGLU, w2, combine) on 8 distinct layers captured in one
 graph, median replay time / 8 (the pages' protocol), against the touched
@@ -595,25 +596,29 @@ def measure_encode(dev, hbm_gbs: float, reps: int = 10):
 
 # ---------------------------------------------------------------------------
 def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
-    """Headline timing: each step is captured once as a CUDA graph (two graphs
-    alternate over the layer ring) and replayed."""
+    """Headline timing, the pages' protocol ("MXFP4 MoE decode kernels",
+    Measured results: a chain of 8 calls in a graph): two steps -- the 8
+    calls on the 8 distinct layers, T = 1, 4, 16, 32 twice -- are captured in
+    one CUDA graph and replayed; an odd step count ends with a graph of one
+    step. CUDA events on the replay stream bracket all `steps` steps."""
     stream = torch.cuda.Stream()
-    n_graphs = wl.layers // wl.calls_per_step
-    graphs = []
-    with torch.cuda.stream(stream):
-        for gi in range(n_graphs):          # eager warm-up of every layer first
+    per_graph = wl.layers // wl.calls_per_step          # 2 steps: every layer once
+    with torch.cuda.stream(stream):                      # eager warm-up of every layer first
+        for gi in range(per_graph):
             for ly in wl.step_layers(gi):
                 wl.call(ly)
     stream.synchronize()
-    for gi in range(n_graphs):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
+    g_chain, g_one = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_chain, stream=stream):
+        for gi in range(per_graph):
             for ly in wl.step_layers(gi):
                 wl.call(ly)
-        graphs.append(g)
+    with torch.cuda.graph(g_one, stream=stream):
+        for ly in wl.step_layers(0):
+            wl.call(ly)
     with torch.cuda.stream(stream):
         for s in range(warmup):
-            graphs[s % n_graphs].replay()
+            g_chain.replay()
     stream.synchronize()
     dist.barrier()
     torch.cuda.synchronize()
@@ -624,8 +629,10 @@ def time_graph_loop(wl, steps: int, warmup: int, dist: Dist):
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for s in range(steps):
-            graphs[s % n_graphs].replay()
+        for s in range(steps // per_graph):
+            g_chain.replay()
+        for s in range(steps % per_graph):
+            g_one.replay()
         e1.record(stream)
     stream.synchronize()
     t_wall = time.perf_counter() - t_wall

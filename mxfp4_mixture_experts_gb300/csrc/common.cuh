@@ -48,11 +48,7 @@ __device__ __forceinline__ uint4 ldcg16(const void* p) {
 __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
-// Programmatic dependent launch: allow the next kernel of the stream to be
-// scheduled (it still waits for this grid in its grid_dependency_wait).
-__device__ __forceinline__ void grid_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
+
 
 
 // Exact bf16x2 product (inputs and results may be subnormal).

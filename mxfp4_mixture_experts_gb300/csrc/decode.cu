@@ -656,10 +656,6 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int nCta = gridDim.x;
-  // programmatic dependent launch (10- to 12-warp forms): the next call may
-  // be scheduled now; its CTAs start as these exit and wait before touching
-  // global memory
-  if constexpr (CW >= 10) grid_launch_dependents();
 
   if (tid < 16) flags[tid] = 0;
   if (tid == 0) {
@@ -672,9 +668,6 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
     prefetch_tensormap(&P.tmap1);
     prefetch_tensormap(&P.tmap2);
   }
-  // everything the previous kernel of the stream wrote (inputs, the
-  // workspace) is visible after this wait
-  if constexpr (CW >= 10) grid_dependency_wait();
   cta_route_small(a.ids, R, E, a.ebase, a.window, tb);   // ends with __syncthreads
   const int nD = tb.misc[0];
   if (warp == 0) {   // expert-batch table: each touched expert's routes in batches of kBatch
@@ -1060,15 +1053,11 @@ static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cu
   cfg.blockDim = dim3(CW * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  // the 10- to 12-warp forms may overlap the tail of the previous kernel in
-  // the stream (the kernel waits for it before reading anything)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CW >= 10 ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel<CW>, p);
 }
 

@@ -42,13 +42,13 @@ constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 64;                   // K values per stage (128 bytes of bf16)
 constexpr int kMaxTok = 320;              // tokens per tile (accumulator columns)
 constexpr int kXBox = 64;                 // token rows per TMA copy (<= 5 a stage)
-constexpr int kSX = 4, kSP = 12, kSW = 4; // rings: tokens (smem), packed (smem), bf16 weights (TMEM)
+constexpr int kSX = 4, kSP = 12, kSW = 6; // rings: tokens (smem), packed (smem), bf16 weights (TMEM)
 constexpr int kXStage = kMaxTok * kBK * 2;   // 40 KB
 constexpr int kXBoxBytes = kXBox * kBK * 2;  // 8 KB
 constexpr int kPStage = kBM * kBK / 2;       // 4 KB of packed bytes
 constexpr int kPBoxRows = 64;
 constexpr int kTmemCols = 512;
-constexpr int kWCol0 = kMaxTok;           // operand-A ring: columns 320..447
+constexpr int kWCol0 = kMaxTok;           // operand-A ring: columns 320..511
 constexpr int kWCols = kBK / 2;           // 32 columns (bf16 pairs) a stage
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpTmaW = 2, kWarpEpi = 4, kWarpDeq = 8;
 constexpr int kWarpEpi2 = 16;            // second epilogue group: the upper half of the tokens
@@ -414,24 +414,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   }
 }
 
-// xp[pos] = hidden[list[pos] / topk] for the valid (expert-sorted) routes.
-// Also inv[route] = pos, the row of the route's output in P.
+// xp[pos] = hidden[list[pos] / topk] for the valid (expert-sorted) routes,
+// one warp per row (16-byte loads and stores, the row read from L2 after its
+// first use). Also inv[route] = pos, the row of the route's output in P.
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ hidden,
                                                      const int32_t* __restrict__ list,
                                                      const int32_t* __restrict__ n_valid, int K,
                                                      int topk, uint16_t* __restrict__ xp,
                                                      int32_t* __restrict__ inv) {
   const int n = *n_valid;
-  for (int pos = blockIdx.x * blockDim.x + threadIdx.x; pos < n; pos += gridDim.x * blockDim.x)
-    inv[list[pos]] = pos;
-  const int per_row = K / 8;
-  const int64_t total = (int64_t)n * per_row;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int pos = (int)(i / per_row), c = (int)(i - (int64_t)pos * per_row);
-    const int tok = list[pos] / topk;
-    reinterpret_cast<uint4*>(xp + (size_t)pos * K)[c] =
-        reinterpret_cast<const uint4*>(hidden + (size_t)tok * K)[c];
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int per_row = K / 8;   // 16-byte chunks
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < n; pos += warps) {
+    const int r = list[pos];
+    if (lane == 0) inv[r] = pos;
+    const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(r / topk) * K);
+    uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * K);
+    for (int c = lane; c < per_row; c += 32) dst[c] = src[c];
   }
 }
 
