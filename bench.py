@@ -381,6 +381,13 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
     peak = peaks["bf16_tflops"]
     g1 = f1 / (med[1] * 1e-3) / 1e12
     g2 = f2 / (med[2] * 1e-3) / 1e12
+    # GEMM1's algorithmic bytes: the w13 packed bytes and scales of the touched
+    # experts, the routed token rows, h written; DRAM traffic from the
+    # recorded ratio while the prefill sources hash the same
+    s = wl.shape
+    b1 = wl.D * w13_bytes(s.K, s.I) + wl.routes * s.K * 2 + wl.routes * s.I * 2
+    rec = recorded_traffic("prefill")
+    traffic1 = int(rec["gemm1_dram_over_alg"] * b1) if rec is not None else None
     out = {
         "metric": METRIC, "value": round(tflops, 1), "unit": "TFLOP/s",
         "n_gpus": dist.world, "steps": steps, "warmup": warmup,
@@ -393,7 +400,9 @@ def run_prefill(args, dist: Dist, steps: int, warmup: int, cpu: bool):
         "roofline": {"kernel": "gemm_kernel<1> (w13 grouped GEMM + SwiGLU)", "bound": "tensor",
                      "achieved": round(g1, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(g1 / peak, 3), "peak_kind": peak_kind + " bf16 burst",
-                     "traffic": None, "alg_flops_per_launch": f1,
+                     "traffic": traffic1,
+                     "traffic_source": "profiles/prefill_traffic.json" if traffic1 else None,
+                     "alg_bytes_per_launch": int(b1), "alg_flops_per_launch": f1,
                      "avg_launch_us": round(med[1] * 1000, 1)},
         "e2e": {"value": round((f1 + f2) * dist.world * steps / (e2e_ms * 1e-3) / 1e12, 1),
                 "unit": "TFLOP/s", "h2d_bytes_per_step": wl.e2e_bytes()[0],
