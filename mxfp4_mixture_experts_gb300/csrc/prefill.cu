@@ -17,6 +17,10 @@
 // tensor memory and the tokens as operand B in shared memory (N = tokens
 // rounded up to 16, so an expert's tokens cost no padding beyond that).
 // Warp roles:
+// The token tile and the dequantised weights of a k-stage share one ring
+// slot and one pair of barriers (full: the token bytes and the 8 dequant
+// warps; empty: the MMAs that read the slot), so the MMA issuer waits and
+// commits once per stage.
 //   warp 0      TMA producer of token tiles (128 rows x 64 bf16, 128-byte swizzle)
 //   warp 1      MMA issuer: tcgen05.mma M128 N<=256 K16, A from tensor memory
 //   warp 2      TMA producer of packed weight bytes (2 x 64 rows x 32 bytes a stage)
@@ -42,7 +46,7 @@ constexpr int kBM = 128;                  // weight rows per tile (MMA M)
 constexpr int kBK = 64;                   // K values per stage (128 bytes of bf16)
 constexpr int kMaxTok = 320;              // tokens per tile (accumulator columns)
 constexpr int kXBox = 64;                 // token rows per TMA copy (<= 5 a stage)
-constexpr int kSX = 4, kSP = 12, kSW = 6; // rings: tokens (smem), packed (smem), bf16 weights (TMEM)
+constexpr int kS = 4, kSP = 12;          // rings: operand stages (tokens in smem + bf16 weights in TMEM), packed bytes (smem)
 constexpr int kXStage = kMaxTok * kBK * 2;   // 40 KB
 constexpr int kXBoxBytes = kXBox * kBK * 2;  // 8 KB
 constexpr int kPStage = kBM * kBK / 2;       // 4 KB of packed bytes
@@ -55,7 +59,7 @@ constexpr int kWarpEpi2 = 16;            // second epilogue group: the upper hal
 constexpr int kEpiWarps = 8;
 constexpr int kDeqWarps = 8;
 constexpr int kScaleAhead = 8;            // k-stages of scale bytes held in registers
-static_assert(kWCol0 + kSW * kWCols <= kTmemCols, "tensor memory budget");
+static_assert(kWCol0 + kS * kWCols <= kTmemCols, "tensor memory budget");
 static_assert(kMaxTok % kXBox == 0 && kMaxTok % 16 == 0, "token boxes fill a stage exactly");
 
 struct GemmParams {
@@ -137,25 +141,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sX = smem;
-  uint8_t* sP = sX + kSX * kXStage;
-  uint64_t* x_full = reinterpret_cast<uint64_t*>(sP + kSP * kPStage);
-  uint64_t* x_empty = x_full + kSX;
-  uint64_t* p_full = x_empty + kSX;
+  uint8_t* sP = sX + kS * kXStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sP + kSP * kPStage);   // [kS]
+  uint64_t* empty = full + kS;                                        // [kS]
+  uint64_t* p_full = empty + kS;
   uint64_t* p_empty = p_full + kSP;
-  uint64_t* w_full = p_empty + kSP;
-  uint64_t* w_empty = w_full + kSW;
-  uint64_t* d_full = w_empty + kSW;
+  uint64_t* d_full = p_empty + kSP;
   uint64_t* d_empty = d_full + 1;
   uint64_t* drain = d_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* tile_base = reinterpret_cast<int*>(tmem_slot + 4);   // [E+1]
+  // the experts' route counts and list offsets, read at every tile change by
+  // every role: shared copies keep global round trips out of the tile switch
+  int* s_cnt = tile_base + p.E + 1;                          // [E]
+  int* s_off = s_cnt + p.E;                                  // [E]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
+  for (int i = threadIdx.x; i < E; i += kPfThreads) {
+    s_cnt[i] = p.count[i];
+    s_off[i] = p.offset[i];
+  }
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSX; ++i) { mbar_init(&x_full[i], 1); mbar_init(&x_empty[i], 1); }
+    for (int i = 0; i < kS; ++i) { mbar_init(&full[i], 1 + kDeqWarps); mbar_init(&empty[i], 1); }
     for (int i = 0; i < kSP; ++i) { mbar_init(&p_full[i], 1); mbar_init(&p_empty[i], kDeqWarps); }
-    for (int i = 0; i < kSW; ++i) { mbar_init(&w_full[i], kDeqWarps); mbar_init(&w_empty[i], 1); }
     mbar_init(d_full, 1);
     mbar_init(d_empty, kEpiWarps);
     mbar_init(drain, 1);
@@ -195,28 +204,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     int sx = 0, kx = 0;
     uint32_t px = 0, xpar = 0;   // parity of each stage's last fill
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
-      const TileId id = decode_tile(t, tile_base, p.count, E);
-      const int row0 = p.offset[id.e] + id.t0;
+      const TileId id = decode_tile(t, tile_base, s_cnt, E);
+      const int row0 = s_off[id.e] + id.t0;
       const int nbox = (id.n + kXBox - 1) / kXBox;
       for (int kc = 0; kc < nK; ++kc) {
-        if (kx >= kSX && !mbar_wait(&x_empty[sx], px ^ 1u)) { fail = 1; break; }
+        if (kx >= kS && !mbar_wait(&empty[sx], px ^ 1u)) { fail = 1; break; }
         xpar = (xpar & ~(1u << sx)) | (px << sx);
-        mbar_arrive_expect_tx(&x_full[sx], nbox * kXBoxBytes);
+        mbar_arrive_expect_tx(&full[sx], nbox * kXBoxBytes);
         for (int b = 0; b < nbox; ++b)
           tma_load_2d(sX + sx * kXStage + b * kXBoxBytes, &p.tmapX, kc * kBK, row0 + b * kXBox,
-                      &x_full[sx]);
-        if (++sx == kSX) { sx = 0; px ^= 1u; }
+                      &full[sx]);
+        if (++sx == kS) { sx = 0; px ^= 1u; }
         ++kx;
       }
     }
     // no copy may still be landing in shared memory when the CTA exits
-    for (int i = 0; i < kSX && i < kx; ++i) mbar_wait(&x_full[i], (xpar >> i) & 1u);
+    for (int i = 0; i < kS && i < kx; ++i) mbar_wait(&full[i], (xpar >> i) & 1u);
   } else if (warp == kWarpTmaW && lane == 0) {
     // ------------------------------------------------------------ packed-weight producer
     int sp = 0, kp = 0;
     uint32_t pp = 0, ppar = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
-      const TileId id = decode_tile(t, tile_base, p.count, E);
+      const TileId id = decode_tile(t, tile_base, s_cnt, E);
       // GEMM1: 64 gate rows then the 64 matching up rows (one copy: row group
       // e 2I + i of [gate; up], or pair e I + i of the interleaved rows);
       // GEMM2: 128 rows (past the matrix: other experts' rows or zeros, never
@@ -241,10 +250,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     for (int i = 0; i < kSP && i < kp; ++i) mbar_wait(&p_full[i], (ppar >> i) & 1u);
   } else if (warp == kWarpMma && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    int sx = 0, sw = 0, tiles = 0;
-    uint32_t px = 0, pw = 0;
+    // The issuing thread is the pipe's bottleneck (each tcgen05 instruction,
+    // barrier test and commit costs it tens of cycles), so a stage is one
+    // barrier test, four MMAs on precomputed descriptors and one commit; the
+    // next stage's barrier is tested while the current stage's last MMA is
+    // queued, and a blocking wait is only taken when that test failed.
+    const uint64_t desc0 = umma_desc_sw128(smem_u32(sX));
+    int s = 0, tiles = 0;
+    uint32_t ph = 0;
+    bool ready = false;   // operands of stage s known to have landed
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++tiles) {
-      const TileId id = decode_tile(t, tile_base, p.count, E);
+      const TileId id = decode_tile(t, tile_base, s_cnt, E);
       const int n16 = (id.n + 15) & ~15;
       const int n_a = min(n16, 256), n_b = n16 - n_a;   // MMA N of the two column groups
       const uint32_t idesc_a = umma_idesc_bf16(kBM, n_a);
@@ -254,22 +270,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         tc_fence_after();
       }
       for (int kc = 0; kc < nK; ++kc) {
-        if (!mbar_wait(&w_full[sw], pw) || !mbar_wait(&x_full[sx], px)) { fail = 8; break; }
+        if (!ready && !mbar_wait(&full[s], ph)) { fail = 8; break; }
         tc_fence_after();
-        const uint32_t x_addr = smem_u32(sX + sx * kXStage);
-        const uint32_t a_col = tmem + kWCol0 + sw * kWCols;
+        const uint32_t a_col = tmem + kWCol0 + s * kWCols;
+        // start-address field (bytes / 16): stage s, k16 step 32 bytes, token 256 at 32 KB
+        const uint64_t dsc = desc0 + (uint64_t)(s * (kXStage >> 4));
+        const int s1 = s + 1 == kS ? 0 : s + 1;
+        const uint32_t ph1 = s + 1 == kS ? ph ^ 1u : ph;
 #pragma unroll
         for (int k16 = 0; k16 < kBK / 16; ++k16) {
+          if (k16 == kBK / 16 - 1) ready = mbar_test(&full[s1], ph1);
           const bool acc = kc > 0 || k16 > 0;
-          umma_bf16_ts(tmem, a_col + k16 * 8, umma_desc_sw128(x_addr + k16 * 32), idesc_a, acc);
+          umma_bf16_ts(tmem, a_col + k16 * 8, dsc + 2 * k16, idesc_a, acc);
           if (n_b > 0)
-            umma_bf16_ts(tmem + 256, a_col + k16 * 8,
-                         umma_desc_sw128(x_addr + 256 * 128 + k16 * 32), idesc_b, acc);
+            umma_bf16_ts(tmem + 256, a_col + k16 * 8, dsc + ((256 * 128) >> 4) + 2 * k16, idesc_b,
+                         acc);
         }
-        umma_commit(&w_empty[sw]);
-        umma_commit(&x_empty[sx]);
-        if (++sw == kSW) { sw = 0; pw ^= 1u; }
-        if (++sx == kSX) { sx = 0; px ^= 1u; }
+        umma_commit(&empty[s]);
+        s = s1;
+        ph = ph1;
       }
       if (fail) break;
       umma_commit(d_full);
@@ -284,21 +303,33 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     const int m = q * 32 + lane;               // operand-A row (TMEM lane)
     const int prow = packed_row<PHASE>(m);
     const uint32_t wlane = tmem + ((uint32_t)(q * 32) << 16) + kWCol0 + h * 16;
-    int sp = 0, sw = 0, kw = 0;
+    int sp = 0, sw = 0, kw = 0;   // packed-ring slot, operand-ring slot, stages done
     uint32_t pp = 0, pw = 0;
-    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
-      const TileId id = decode_tile(t, tile_base, p.count, E);
-      const uint8_t* srow =
-          p.wsc + (size_t)weight_row<PHASE>(id.e, id.nt, p, m) * (p.kred / kScaleBlock) + h;
-      // the scale byte of each of the next kScaleAhead stages, loaded one window early
-      uint32_t sc[kScaleAhead];
+    // scale row of this thread's weight row in tile t (its half's bytes)
+    auto scale_row = [&](int t) {
+      const TileId id = decode_tile(t, tile_base, s_cnt, E);
+      return p.wsc + (size_t)weight_row<PHASE>(id.e, id.nt, p, m) * (p.kred / kScaleBlock) + h;
+    };
+    // the scale byte of each of the next kScaleAhead stages, loaded one window
+    // early (the next tile's first window during the current tile's last one)
+    uint32_t sc[kScaleAhead];
+    const uint8_t* srow = blockIdx.x < ntiles ? scale_row(blockIdx.x) : nullptr;
 #pragma unroll
-      for (int i = 0; i < kScaleAhead; ++i) sc[i] = i < nK ? ldg_u8(srow + 2 * i) : 0u;
+    for (int i = 0; i < kScaleAhead; ++i) sc[i] = (srow != nullptr && i < nK) ? ldg_u8(srow + 2 * i) : 0u;
+    for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x) {
+      const int tn = t + gridDim.x;
+      const uint8_t* srow_n = tn < ntiles ? scale_row(tn) : nullptr;
       for (int k0 = 0; k0 < nK && !fail; k0 += kScaleAhead) {
         uint32_t nx[kScaleAhead];
+        if (k0 + kScaleAhead < nK) {
 #pragma unroll
-        for (int i = 0; i < kScaleAhead; ++i)
-          nx[i] = k0 + kScaleAhead + i < nK ? ldg_u8(srow + 2 * (k0 + kScaleAhead + i)) : 0u;
+          for (int i = 0; i < kScaleAhead; ++i)
+            nx[i] = k0 + kScaleAhead + i < nK ? ldg_u8(srow + 2 * (k0 + kScaleAhead + i)) : 0u;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kScaleAhead; ++i)
+            nx[i] = (srow_n != nullptr && i < nK) ? ldg_u8(srow_n + 2 * i) : 0u;
+        }
 #pragma unroll
         for (int i = 0; i < kScaleAhead; ++i) {
           if (k0 + i >= nK || fail) break;
@@ -313,20 +344,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
           uint32_t o[16];   // this thread's 32 values, in row order (bf16 pairs)
           dequant32_bf16(wd, scale_mul(sc[i]), o);
-          if (kw >= kSW) {   // the MMAs that read this ring slot have completed
-            if (!warp_wait(&w_empty[sw], pw ^ 1u)) { fail = 32; break; }
+          if (kw >= kS) {   // the MMAs that read this ring slot have completed
+            if (!warp_wait(&empty[sw], pw ^ 1u)) { fail = 32; break; }
             tc_fence_after();
           }
           tmem_st16(wlane + sw * kWCols, o);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&w_full[sw]);
-          if (++sw == kSW) { sw = 0; pw ^= 1u; }
+          if (lane == 0) mbar_arrive(&full[sw]);
+          if (++sw == kS) { sw = 0; pw ^= 1u; }
           ++kw;
         }
 #pragma unroll
         for (int i = 0; i < kScaleAhead; ++i) sc[i] = nx[i];
       }
+      srow = srow_n;
     }
   } else if ((warp >= kWarpEpi && warp < kWarpEpi + 4) || warp >= kWarpEpi2) {
     // ------------------------------------------------------------ epilogue
@@ -334,10 +366,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
     const int half = warp >= kWarpEpi2;   // which half of the tile's tokens (32-column blocks)
     int tiles = 0;
     for (int t = blockIdx.x; t < ntiles && !fail; t += gridDim.x, ++tiles) {
-      const TileId id = decode_tile(t, tile_base, p.count, E);
+      const TileId id = decode_tile(t, tile_base, s_cnt, E);
       if (!warp_wait(d_full, tiles & 1)) { fail = 64; break; }
       tc_fence_after();
-      const int pos0 = p.offset[id.e] + id.t0;
+      const int pos0 = s_off[id.e] + id.t0;
       if (PHASE == 1) {
         // lane groups g = 2q, 2q + 1: this thread's SwiGLU pairs are
         // i = 64 nt + 8g + lane/4, tokens 8b + 2(lane%4) + {0, 1}
@@ -500,8 +532,8 @@ __global__ void __launch_bounds__(256) route_rows_kernel(const float* __restrict
 }
 
 static size_t gemm_smem_bytes(int E) {
-  return 1024 + (size_t)kSX * kXStage + (size_t)kSP * kPStage +
-         (size_t)(2 * kSX + 2 * kSP + 2 * kSW + 3) * 8 + 16 + (size_t)(E + 1) * 4;
+  return 1024 + (size_t)kS * kXStage + (size_t)kSP * kPStage +
+         (size_t)(2 * kS + 2 * kSP + 3) * 8 + 16 + (size_t)(3 * E + 1) * 4;
 }
 
 template <int PHASE, bool OAI>
