@@ -447,13 +447,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
 }
 
 // xp[pos] = hidden[list[pos] / topk] for the valid (expert-sorted) routes,
-// one warp per row (16-byte loads and stores, the row read from L2 after its
-// first use). Also inv[route] = pos, the row of the route's output in P.
+// one warp per row, 16-byte chunks in batches of 8 per lane (all loads of a
+// batch in flight before its stores); the rows of xp are written with an
+// evict-first hint, so the hidden rows (each read topk times) stay in L2.
+// Also inv[route] = pos, the row of the route's output in P.
+__device__ __forceinline__ void st_cs16(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ hidden,
                                                      const int32_t* __restrict__ list,
                                                      const int32_t* __restrict__ n_valid, int K,
                                                      int topk, uint16_t* __restrict__ xp,
                                                      int32_t* __restrict__ inv) {
+  constexpr int kB = 8;
   const int n = *n_valid;
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
@@ -463,7 +471,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
     if (lane == 0) inv[r] = pos;
     const uint4* src = reinterpret_cast<const uint4*>(hidden + (size_t)(r / topk) * K);
     uint4* dst = reinterpret_cast<uint4*>(xp + (size_t)pos * K);
-    for (int c = lane; c < per_row; c += 32) dst[c] = src[c];
+    for (int c0 = lane; c0 < per_row; c0 += 32 * kB) {
+      uint4 v[kB];
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if (c0 + 32 * j < per_row) v[j] = src[c0 + 32 * j];
+#pragma unroll
+      for (int j = 0; j < kB; ++j)
+        if (c0 + 32 * j < per_row) st_cs16(dst + c0 + 32 * j, v[j]);
+    }
   }
 }
 
