@@ -123,22 +123,37 @@ __device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm
 // One 32-value scale block as exact bf16 by integer bit placement and bf16
 // multiplies (the prefill GEMM's operand A): wd holds the 16 packed bytes
 // (value 2i in the low nibble of byte i), sm the block's scale multipliers.
-// o[4c .. 4c+3] = values 8c .. 8c+7 as bf16 pairs (low half first), i.e. the
-// 32 values in row order.
-__device__ __forceinline__ void dequant32_bf16(const uint32_t (&wd)[4], const ScaleMul& sm,
-                                               uint32_t (&o)[16]) {
+// Pair order, the order in which the bit placement produces them:
+// o[4c + P] = values (8c + P, 8c + P + 4) as a bf16 pair (low half first), so
+// each group of 8 values is held in the order 0 4 1 5 2 6 3 7. The GEMM's
+// token rows carry the same order inside each group of 8 (the dot products
+// are unchanged), which saves the byte permutes of row order.
+__device__ __forceinline__ void dequant32_bf16_pairs(const uint32_t (&wd)[4], const ScaleMul& sm,
+                                                     uint32_t (&o)[16]) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {   // values 8c .. 8c+7
-    const uint32_t p0 = apply_scale(e2m1_pair_raw<0>(wd[c]), sm);   // (n0, n4)
-    const uint32_t p1 = apply_scale(e2m1_pair_raw<1>(wd[c]), sm);   // (n1, n5)
-    const uint32_t p2 = apply_scale(e2m1_pair_raw<2>(wd[c]), sm);   // (n2, n6)
-    const uint32_t p3 = apply_scale(e2m1_pair_raw<3>(wd[c]), sm);   // (n3, n7)
-    o[4 * c + 0] = prmt(p0, p1, 0x5410u);   // (n0, n1)
-    o[4 * c + 1] = prmt(p2, p3, 0x5410u);   // (n2, n3)
-    o[4 * c + 2] = prmt(p0, p1, 0x7632u);   // (n4, n5)
-    o[4 * c + 3] = prmt(p2, p3, 0x7632u);   // (n6, n7)
+    o[4 * c + 0] = apply_scale(e2m1_pair_raw<0>(wd[c]), sm);   // (n0, n4)
+    o[4 * c + 1] = apply_scale(e2m1_pair_raw<1>(wd[c]), sm);   // (n1, n5)
+    o[4 * c + 2] = apply_scale(e2m1_pair_raw<2>(wd[c]), sm);   // (n2, n6)
+    o[4 * c + 3] = apply_scale(e2m1_pair_raw<3>(wd[c]), sm);   // (n3, n7)
   }
 }
+// The same block in row order: o[4c .. 4c+3] = values 8c .. 8c+7 as bf16
+// pairs (low half first).
+__device__ __forceinline__ void dequant32_bf16(const uint32_t (&wd)[4], const ScaleMul& sm,
+                                               uint32_t (&o)[16]) {
+  uint32_t q[16];
+  dequant32_bf16_pairs(wd, sm, q);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    o[4 * c + 0] = prmt(q[4 * c + 0], q[4 * c + 1], 0x5410u);   // (n0, n1)
+    o[4 * c + 1] = prmt(q[4 * c + 2], q[4 * c + 3], 0x5410u);   // (n2, n3)
+    o[4 * c + 2] = prmt(q[4 * c + 0], q[4 * c + 1], 0x7632u);   // (n4, n5)
+    o[4 * c + 3] = prmt(q[4 * c + 2], q[4 * c + 3], 0x7632u);   // (n6, n7)
+  }
+}
+// Position of value k of a group of 8 in pair order (0 4 1 5 2 6 3 7).
+__host__ __device__ __forceinline__ int pair_order_pos(int k) { return 2 * (k & 3) + (k >> 2); }
 
 // silu(z) = z * sigmoid(z) with the fast exponential and division (a few ulp
 // of fp32; the product is rounded to bf16 afterwards).

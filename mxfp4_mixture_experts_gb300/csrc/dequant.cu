@@ -6,9 +6,10 @@
 //          then an exact fp32 multiply by 2^(s-127) (e8m0_to_f32). Every
 //          product is representable in fp32 (E2M1 has two significant bits),
 //          so the only rounding is the final fp32 -> bf16 one.
-//  form 2  the prefill GEMM's operand A (dequant32_bf16, the same device
-//          function the GEMM's dequant warps call): the E2M1 fields placed in
-//          a bf16 bit pattern, then one or two exact bf16 multiplies.
+//  form 2  the prefill GEMM's operand A (dequant32_bf16_pairs, the device
+//          function the GEMM's dequant warps call, then put in row order): the
+//          E2M1 fields placed in a bf16 bit pattern, then one or two exact
+//          bf16 multiplies.
 // Both are exact except where the product leaves the bf16 range.
 #include "common.cuh"
 #include "kernels.h"

@@ -5,8 +5,10 @@
 // into the GEMM's shared-memory tiles instead).
 //
 //   route   stable counting sort of the routes by expert (route.cu)
-//   gather  xp[pos] = hidden[token of route list[pos]]: rows in expert order
+//   gather  xp[pos] = hidden[token of route list[pos]]: rows in expert order,
+//           each group of 8 values in pair order (0 4 1 5 2 6 3 7)
 //   GEMM1   per expert: [M_e x K] x [K x 2I]^T -> SwiGLU -> hp [M_e x I] bf16
+//           (pair order inside each group of 8 intermediate values)
 //   GEMM2   per expert: [M_e x I] x [I x K]^T -> P[pos] fp32 (expert order)
 //   combine y[t] = bf16(sum over the token's slots of w * P[pos of the route]),
 //           slot order
@@ -25,6 +27,9 @@
 //   warp 1      MMA issuer: tcgen05.mma M128 N<=256 K16, A from tensor memory
 //   warp 2      TMA producer of packed weight bytes (2 x 64 rows x 32 bytes a stage)
 //   warps 4..7  epilogue: tcgen05.ld of D -> SwiGLU / routing weight -> global
+// Both GEMMs take the reduction dimension in pair order inside each group of
+// 8 values, on the weights (as dequant32_bf16_pairs makes them) and on the
+// token rows alike, so the dot products are those of row order.
 //   warps 8..15 dequant: packed E2M1 + E8M0 -> exact bf16, tcgen05.st into the
 //               tensor-memory ring of operand A (two warps per lane quarter,
 //               32 of the stage's 64 K values each)
@@ -343,7 +348,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
           if (++sp == kSP) { sp = 0; pp ^= 1u; }
           const uint32_t wd[4] = {qv.x, qv.y, qv.z, qv.w};
           uint32_t o[16];   // this thread's 32 values, in row order (bf16 pairs)
-          dequant32_bf16(wd, scale_mul(sc[i]), o);
+          dequant32_bf16_pairs(wd, scale_mul(sc[i]), o);
           if (kw >= kS) {   // the MMAs that read this ring slot have completed
             if (!warp_wait(&empty[sw], pw ^ 1u)) { fail = 32; break; }
             tc_fence_after();
@@ -377,6 +382,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
         for (int s = 0; s < 2; ++s) {
           const int g = 2 * q + s;
           const int i = id.nt * 64 + 8 * g + (lane >> 2);
+          const int ip = (i & ~7) | pair_order_pos(i & 7);   // its column of hp
           const uint32_t taddr = tmem + ((uint32_t)(16 * g) << 16);
           float bg = 0.f, bu = 0.f;   // gpt-oss biases of pair i (interleaved order)
           if (OAI) {
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
                 } else {
                   hv = silu_fast(gt) * up;
                 }
-                if (n < id.n) p.hp[(size_t)(pos0 + n) * p.I + i] = f32_to_bf16_rne(hv);
+                if (n < id.n) p.hp[(size_t)(pos0 + n) * p.I + ip] = f32_to_bf16_rne(hv);
               }
             }
           }
@@ -447,7 +453,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) gemm_kernel(const __grid_consta
 }
 
 // xp[pos] = hidden[list[pos] / topk] for the valid (expert-sorted) routes,
-// one warp per row, 16-byte chunks in batches of 8 per lane (all loads of a
+// each group of 8 values in pair order (0 4 1 5 2 6 3 7); one warp per row,
+// 16-byte chunks (one group each) in batches of 8 per lane (all loads of a
 // batch in flight before its stores); the rows of xp are written with an
 // evict-first hint, so the hidden rows (each read topk times) stay in L2.
 // Also inv[route] = pos, the row of the route's output in P.
@@ -478,7 +485,11 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
         if (c0 + 32 * j < per_row) v[j] = src[c0 + 32 * j];
 #pragma unroll
       for (int j = 0; j < kB; ++j)
-        if (c0 + 32 * j < per_row) st_cs16(dst + c0 + 32 * j, v[j]);
+        if (c0 + 32 * j < per_row) {
+          const uint4 u = v[j];   // words (0 1) (2 3) (4 5) (6 7) -> (0 4) (1 5) (2 6) (3 7)
+          st_cs16(dst + c0 + 32 * j, make_uint4(prmt(u.x, u.z, 0x5410u), prmt(u.x, u.z, 0x7632u),
+                                                prmt(u.y, u.w, 0x5410u), prmt(u.y, u.w, 0x7632u)));
+        }
     }
   }
 }
