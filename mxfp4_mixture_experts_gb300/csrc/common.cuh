@@ -75,18 +75,26 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // and the sign goes to bit 15. One exact bf16 multiply by 2^126 * 2^(s-127)
 // then gives E2M1 * 2^(s-127).
 //
-// e2m1_pair_raw<P>(w) takes nibbles P and P+4 of the 32-bit word w (bits
+// e2m1_word_raw(w, r) places nibbles P and P+4 of the 32-bit word w (bits
 // 4P..4P+3 and 4P+16..4P+19, which sit 16 bits apart) into the low and high
-// bf16 of the result.
+// bf16 of r[P]. A code c isolated at bits 0..3 of a half, times 0x1040, is
+// c << 6 + c << 12 with no carries (bits 6..9 and 12..15): the magnitude lands
+// on bits 6..8 and the sign on bit 15, the mask clears the two copies' other
+// bits. Odd nibbles sit 4 bits higher and take 0x104 instead. One integer
+// multiply does the work of two shifts and a merge.
 // ---------------------------------------------------------------------------
-template <int P>
-__device__ __forceinline__ uint32_t e2m1_pair_raw(uint32_t w) {
-  static_assert(P >= 0 && P < 4, "pair index");
-  constexpr int kMagShift = 6 - 4 * P;     // bits 4P..4P+2 -> 6..8
-  constexpr int kSignShift = 12 - 4 * P;   // bit 4P+3 -> 15
-  const uint32_t mag = kMagShift >= 0 ? (w << kMagShift) : (w >> (-kMagShift));
-  const uint32_t sgn = w << kSignShift;
-  return (mag & 0x01C001C0u) | (sgn & 0x80008000u);
+__device__ __forceinline__ uint32_t mul_lo(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void e2m1_word_raw(uint32_t w, uint32_t (&r)[4]) {
+  constexpr uint32_t kKeep = 0x81C081C0u;   // bits 6..8 and 15 of each half
+  const uint32_t w8 = w >> 8;
+  r[0] = mul_lo(w & 0x000F000Fu, 0x1040u) & kKeep;    // nibbles 0, 4
+  r[1] = mul_lo(w & 0x00F000F0u, 0x0104u) & kKeep;    // nibbles 1, 5
+  r[2] = mul_lo(w8 & 0x000F000Fu, 0x1040u) & kKeep;   // nibbles 2, 6
+  r[3] = mul_lo(w8 & 0x00F000F0u, 0x0104u) & kKeep;   // nibbles 3, 7
 }
 
 // Multiplier pair for one E8M0 scale byte s. For s <= 128 a single exact
@@ -114,11 +122,6 @@ __device__ __forceinline__ ScaleMul scale_mul(uint32_t s) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm) {
-  uint32_t v = bf16x2_mul(raw, sm.m1);
-  if (__builtin_expect(sm.two, 0)) v = bf16x2_mul(v, sm.m2);
-  return v;
-}
 
 // One 32-value scale block as exact bf16 by integer bit placement and bf16
 // multiplies (the prefill GEMM's operand A): wd holds the 16 packed bytes
@@ -130,12 +133,16 @@ __device__ __forceinline__ uint32_t apply_scale(uint32_t raw, const ScaleMul& sm
 // are unchanged), which saves the byte permutes of row order.
 __device__ __forceinline__ void dequant32_bf16_pairs(const uint32_t (&wd)[4], const ScaleMul& sm,
                                                      uint32_t (&o)[16]) {
+  uint32_t r[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {   // values 8c .. 8c+7
-    o[4 * c + 0] = apply_scale(e2m1_pair_raw<0>(wd[c]), sm);   // (n0, n4)
-    o[4 * c + 1] = apply_scale(e2m1_pair_raw<1>(wd[c]), sm);   // (n1, n5)
-    o[4 * c + 2] = apply_scale(e2m1_pair_raw<2>(wd[c]), sm);   // (n2, n6)
-    o[4 * c + 3] = apply_scale(e2m1_pair_raw<3>(wd[c]), sm);   // (n3, n7)
+  for (int c = 0; c < 4; ++c) {   // values 8c .. 8c+7: o[4c + P] = (n_P, n_P+4)
+    e2m1_word_raw(wd[c], r);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[4 * c + q] = bf16x2_mul(r[q], sm.m1);
+  }
+  if (__builtin_expect(sm.two, 0)) {   // scale bytes above 128: the second exact step
+#pragma unroll
+    for (int q = 0; q < 16; ++q) o[q] = bf16x2_mul(o[q], sm.m2);
   }
 }
 // The same block in row order: o[4c .. 4c+3] = values 8c .. 8c+7 as bf16
