@@ -1011,7 +1011,7 @@ static int routes_per_expert_p99(int T, int topk, int E) {
 // call's time through the slowest CTA. 0 when even 8 warps do not fit. Rows
 // beyond the staged ones are read from the f16 scratch in global memory
 // (correct for any routing, only slower).
-int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
+static int decode_warps_at(int K, int I, int E, int T, int topk, int max_smem) {
   const int R = T * topk;
   const int stride = decode_row_stride(K, I);
   const double rho = (double)R / ((double)E * (1.0 - pow(1.0 - 1.0 / E, (double)R)));
@@ -1023,6 +1023,22 @@ int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
     if (decode_smem_bytes(cw, K, I, E, R, want, stride) <= (size_t)max_smem) return cw;
   if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
   return 0;
+}
+
+// The form of a call: the one its own T needs, except that when the largest
+// decode T of the layer shape runs one of the 10- to 12-warp forms, every T of
+// the shape runs that form. Each form is its own code, and a sequence of
+// calls whose T move between forms pays for the switch at every change (about
+// 8 us a switch on gptoss128, in a step of T = 1, 4, 16, 32); one form for the
+// shape costs the small calls a little (T = 4 / 16 ran 1.5 / 4.5 us slower on
+// 11 warps than on 12) and saves the switches.
+int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
+  const int cw = decode_warps_at(K, I, E, T, topk, max_smem);
+  int t_max = kDecodeMaxTokens;
+  if (t_max * topk > kDecodeMaxRoutes) t_max = kDecodeMaxRoutes / topk;
+  if (cw == 0 || t_max <= T) return cw;
+  const int cw_max = decode_warps_at(K, I, E, t_max, topk, max_smem);
+  return cw_max >= 10 && cw_max < cw ? cw_max : cw;
 }
 
 bool decode_fits(int K, int I, int E, int T, int topk, int max_smem) {
