@@ -14,10 +14,12 @@
 //   combine:       y [T, K] = bf16 of the slot-order sum of each token's route
 //                  outputs.
 //
-// One CTA per SM; every warp is a consumer: 10 to 12 warps with 3-deep rings
-// when the activation rows a CTA is expected to need fit in shared memory
-// next to the rings, else 8 warps, which leave the most room for rows
-// (decode_warps).
+// One CTA per SM: 10 to 12 consumer warps with 3-deep rings when the
+// activation rows a CTA is expected to need fit in shared memory next to the
+// rings, else 7 consumer warps and a producer warp, which leave the most room
+// for rows (decode_warps). In the 10- to 12-warp forms each consumer warp's
+// lane 0 issues its own stages; in the 7 + 1 form the producer's lanes issue
+// them for all consumer warps.
 //  * Work item = 16 weight rows of one touched expert over the whole
 //    reduction (phase 1: gate rows i0..i0+7 and the matching up rows; phase 2:
 //    16 w2 rows) times up to 32 of the expert's routes. A phase's items are
@@ -68,6 +70,12 @@ constexpr int kMaxGroups = kBatch / kGroup;
 constexpr int kBarConsumers = 1;             // named barrier of the consumer warps
 constexpr int kRowBars = 16;                 // barriers of the staged activation rows
 constexpr uint32_t kRowBarBytes = 32768;     // bytes tracked by one of them (at most)
+// The form with 7 consumer warps has a producer warp besides them (8 warps in
+// all): its lanes issue the consumers' weight stages and scale rows, which the
+// consumers hand back through per-slot barriers. Only that form has one.
+__host__ __device__ constexpr bool has_producer(int cw) { return cw == 7; }
+// polls (32 ns apart) without a copy issued before the producer warp gives up
+constexpr uint32_t kProducerIdleLimit = 1u << 24;
 
 
 __host__ __device__ inline size_t round_up(size_t n, size_t a) { return (n + a - 1) / a * a; }
@@ -90,7 +98,8 @@ __host__ __device__ inline DecodeSmem decode_smem_plan(int cw, int K, int I, int
   m.scales = o;
   o += (size_t)2 * cw * m.slot_bytes;
   m.bars = o;
-  o += round_up((size_t)(cw * ring_depth(cw) + 2 * cw + kRowBars) * 8, 16);
+  o += round_up((size_t)((has_producer(cw) ? 2 : 1) * (cw * ring_depth(cw) + 2 * cw) + kRowBars) * 8,
+                16);
   m.flags = o;
   o += 64;   // int flags[16]
   m.ints = o;
@@ -538,7 +547,7 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
                                             int lane, const uint8_t* sc, int ng, const BRows& br,
                                             const uint8_t* xs, StageIssuer& is, const DecodeParams& P,
                                             const PhaseView& v1, const PhaseView& v2, int n1,
-                                            int n2, const int* eb, int cw) {
+                                            int n2, const int* eb, int cw, uint64_t* empty_w) {
   constexpr int KD = ring_depth(CW);
   const int g = lane >> 2, t = lane & 3;
   // scale rows of MMA rows g (gate / w2 row g) and g + 8 (up / w2 row g + 8)
@@ -547,7 +556,8 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
   for (int c = 0; c < v.nc; ++c, ring_advance<KD>(s)) {
     // keep KD - 1 stages ahead: the slot refilled now held stage s - 1, which
     // every lane has finished reading (fenced below)
-    if (lane == 0) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
+    if constexpr (!has_producer(CW))
+      if (lane == 0) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, const_cast<uint8_t*>(ring_w), full_w);
     const int slot = s.slot;
     if (!__all_sync(0xffffffffu, mbar_wait(&full_w[slot], s.par))) return false;
     const uint8_t* stg = ring_w + slot * kStageBytes;
@@ -596,9 +606,11 @@ __device__ __forceinline__ bool item_stages(float (&acc)[kMaxGroups][4], const i
         block_mma<FAST, GLOB>(acc, stg, b, g, t, sc_g, sc_g8, bg + b, ng, br, xs);
     }
     // the slot is refilled by tensor copies (async proxy): order the generic
-    // reads of it before that write
+    // reads of it before that write (and hand it back to a producer warp)
     fence_proxy_async_smem();
     __syncwarp();
+    if constexpr (has_producer(CW))
+      if (lane == 0) mbar_arrive(&empty_w[slot]);
   }
   return true;
 }
@@ -620,7 +632,8 @@ __device__ __forceinline__ void issue_rows(int phase, const PhaseView& v, const 
 // CW warps, all of them consumers; warp 0's lane 0 also stages the activation
 // rows and waits for the grid between the phases.
 template <int CW>
-__global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constant__ DecodeParams P) {
+__global__ void __launch_bounds__((CW + (has_producer(CW) ? 1 : 0)) * 32, 1)
+    decode_kernel(const __grid_constant__ DecodeParams P) {
   constexpr int kThreadsCW = CW * 32;
   constexpr int KD = ring_depth(CW);
   extern __shared__ uint8_t smem_raw[];
@@ -632,9 +645,11 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   const DecodeSmem M = decode_smem_plan(CW, a.K, a.I, E, R, P.xs_rows_cap, P.xs_stride);
   uint8_t* ring = smem + M.ring;
   uint8_t* scales = smem + M.scales;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + M.bars);  // [CW][KD]
-  uint64_t* sfull = wfull + CW * KD;                              // [CW][2]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + M.bars);  // [CW][KD] stage landed
+  uint64_t* sfull = wfull + CW * KD;                              // [CW][2] scale rows landed
   uint64_t* xfull = sfull + 2 * CW;                               // [kRowBars]
+  uint64_t* wempty = xfull + kRowBars;                            // producer form: [CW][KD] consumed
+  uint64_t* sempty = wempty + CW * KD;                            // producer form: [CW][2] consumed
   int* flags = reinterpret_cast<int*>(smem + M.flags);
   RouteTables tb;
   tb.cnt = reinterpret_cast<int*>(smem + M.ints);
@@ -661,6 +676,10 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   if (tid == 0) {
     for (int i = 0; i < CW * KD; ++i) mbar_init(&wfull[i], 1);
     for (int i = 0; i < 2 * CW; ++i) mbar_init(&sfull[i], 1);
+    if constexpr (has_producer(CW)) {
+      for (int i = 0; i < CW * KD; ++i) mbar_init(&wempty[i], 1);
+      for (int i = 0; i < 2 * CW; ++i) mbar_init(&sempty[i], 1);
+    }
     for (int i = 0; i < kRowBars; ++i) mbar_init(&xfull[i], 1);
     fence_barrier_init();
     prefetch_tensormap(&P.tmap1q);
@@ -701,7 +720,81 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   const RowPlan rp2 = row_plan(v2, P.xs_rows_cap);
   int* gbar = a.gbar;   // [0] phase arrivals (two per CTA and call), [1] CTAs done
 
-  // ======================= all warps: consumers =======================
+  if constexpr (has_producer(CW)) {
+    if (warp == CW) {
+      // ===================== producer warp =====================
+      // Lane w issues consumer warp w's weight stages into its KD-stage ring
+      // and its items' scale rows into its two scale slots, in the order the
+      // warp consumes them, refilling a slot as soon as the warp hands it back
+      // (one warp instruction issues for all consumer warps). Phase-2 stages
+      // go out before h exists.
+      const bool live = lane < CW;
+      const int w = live ? lane : 0;
+      const int pn1 = warp_items<CW>(w, v1.n), pn2 = warp_items<CW>(w, v2.n);
+      uint8_t* ring_p = ring + (size_t)w * KD * kStageBytes;
+      uint64_t* full_p = wfull + w * KD;
+      uint64_t* empty_p = wempty + w * KD;
+      uint8_t* scale_p = scales + (size_t)w * 2 * M.slot_bytes;
+      uint64_t* sfull_p = sfull + w * 2;
+      uint64_t* sempty_p = sempty + w * 2;
+      StageIssuer is;
+      is.cur.phase = live ? 1 : 3;
+      is.cur.k = 0;
+      is.c = 0;
+      is.q = {0, 0, 0u};
+      is.row0 = is.row1 = 0;
+      is.cur.j = is.cur.rb = 0;
+      cursor_locate<CW>(is.cur, v1, v2, w);
+      cursor_skip_empty<CW>(is.cur, pn1, pn2, v1, v2, w);
+      ItemCursor scc = is.cur;   // next item whose scale rows are to be issued
+      int nsc = 0;               // scale copies issued
+      bool pfail = false;
+      uint32_t idle = 0;
+      for (;;) {
+        bool progress = false;
+        if (is.cur.phase <= 2) {   // stage n into slot n % KD once stage n - KD was consumed
+          const int n = is.q.n;
+          if (n < KD || mbar_test(&empty_p[is.q.slot], (uint32_t)(n / KD - 1) & 1u)) {
+            issue_stage<CW>(is, P, v1, v2, pn1, pn2, eb, w, ring_p, full_p);
+            progress = true;
+          }
+        }
+        if (scc.phase <= 2) {      // scale copy n into slot n & 1 once item n - 2 is done
+          const int x = nsc & 1;
+          if (nsc < 2 || mbar_test(&sempty_p[x], (uint32_t)((nsc >> 1) - 1) & 1u)) {
+            issue_scales(scc, a, v1, v2, eb, w, scale_p + x * M.slot_bytes, &sfull_p[x]);
+            ++nsc;
+            cursor_next<CW>(scc, pn1, pn2, v1, v2, w);
+            progress = true;
+          }
+        }
+        if (__all_sync(0xffffffffu, is.cur.phase > 2 && scc.phase > 2)) break;
+        if (__any_sync(0xffffffffu, progress)) {
+          idle = 0;
+        } else {
+          __nanosleep(32);
+          if (++idle > kProducerIdleLimit) {   // the consumers stopped taking stages
+            pfail = true;
+            break;
+          }
+        }
+      }
+      // every copy issued lands before the CTA can exit
+      if (live) {
+        for (int n = max(0, is.q.n - KD); n < is.q.n; ++n)
+          mbar_wait(&full_p[n % KD], (uint32_t)(n / KD) & 1u);
+        for (int n = max(0, nsc - 2); n < nsc; ++n)
+          mbar_wait(&sfull_p[n & 1], (uint32_t)(n >> 1) & 1u);
+      }
+      if (pfail && lane == 0 && a.status != nullptr) {
+        atomicOr(&a.status[2], 1);
+        atomicCAS(&a.status[3], 0, blockIdx.x + 1);
+      }
+      return;
+    }
+  }
+
+  // ======================= consumer warps =======================
   const int cw = warp;
   const int ctid = tid;
   if (ctid == 0) issue_rows(1, v1, rp1, a, tb, xs, xs_stride, xfull);
@@ -711,7 +804,9 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   for (int u = 0; u < 8; ++u) xo[u] = g * 128 + (((u ^ g) << 4) + (t << 2));
   uint8_t* ring_w = ring + (size_t)cw * KD * kStageBytes;
   uint64_t* full_w = wfull + cw * KD;
+  uint64_t* empty_w = wempty + cw * KD;   // (producer form)
   uint64_t* sfull_w = sfull + cw * 2;
+  uint64_t* sempty_w = sempty + cw * 2;   // (producer form)
   uint8_t* scale_w = scales + (size_t)cw * 2 * M.slot_bytes;
   const int n1 = warp_items<CW>(cw, v1.n), n2 = warp_items<CW>(cw, v2.n);
   bool ok = true;
@@ -731,7 +826,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   cursor_skip_empty<CW>(is.cur, n1, n2, v1, v2, cw);
   ItemCursor sc_next = is.cur;   // next item whose scale rows are to be issued
   int sc_count = 0;              // scale copies issued (lane 0)
-  if (lane == 0) {
+  if (!has_producer(CW) && lane == 0) {
     for (int i = 0; i < KD - 1; ++i) issue_stage<CW>(is, P, v1, v2, n1, n2, eb, cw, ring_w, full_w);
     if (sc_next.phase <= 2) {
       issue_scales(sc_next, a, v1, v2, eb, cw, scale_w, &sfull_w[0]);
@@ -836,7 +931,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       const int sx = kitems & 1;
       // the next item's scale rows go to the other slot, which the previous
       // item (finished and fenced) no longer reads
-      if (lane == 0 && sc_next.phase <= 2) {
+      if (!has_producer(CW) && lane == 0 && sc_next.phase <= 2) {
         issue_scales(sc_next, a, v1, v2, eb, cw, scale_w + (sx ^ 1) * M.slot_bytes, &sfull_w[sx ^ 1]);
         ++sc_count;
       }
@@ -885,16 +980,16 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
         for (int q = 0; q < 4; ++q) acc[gr][q] = 0.f;
       if (!special && !glob)
         ok = item_stages<CW, true, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is, P,
-                                          v1, v2, n1, n2, eb, cw);
+                                          v1, v2, n1, n2, eb, cw, empty_w);
       else if (special && !glob)
         ok = item_stages<CW, false, false>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is, P,
-                                           v1, v2, n1, n2, eb, cw);
+                                           v1, v2, n1, n2, eb, cw, empty_w);
       else if (!special)
         ok = item_stages<CW, true, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is,
-                                              P, v1, v2, n1, n2, eb, cw);
+                                              P, v1, v2, n1, n2, eb, cw, empty_w);
       else
         ok = item_stages<CW, false, true>(acc, xo, ring_w, full_w, s, v, lane, sc, ng, br, xs, is,
-                                               P, v1, v2, n1, n2, eb, cw);
+                                               P, v1, v2, n1, n2, eb, cw, empty_w);
       if (!ok) {
         fail |= 16;
         break;
@@ -938,6 +1033,8 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
       // the scale slot is refilled by a bulk copy (async proxy)
       fence_proxy_async_smem();
       __syncwarp();
+      if constexpr (has_producer(CW))
+        if (lane == 0) mbar_arrive(&sempty_w[sx]);
       ++kitems;
     }
     // -- grid arrival: this CTA's outputs of the phase are written
@@ -967,7 +1064,7 @@ __global__ void __launch_bounds__(CW * 32, 1) decode_kernel(const __grid_constan
   }
   // stages issued ahead but never consumed (only after a failed wait) must
   // land before the CTA exits
-  if (lane == 0) {
+  if (!has_producer(CW) && lane == 0) {
     for (int n = s.n; n < is.q.n; ++n) mbar_wait(&full_w[n % KD], (uint32_t)(n / KD) & 1u);
     for (int n = kitems; n < sc_count; ++n) mbar_wait(&sfull_w[n & 1], (uint32_t)(n >> 1) & 1u);
   }
@@ -1004,11 +1101,12 @@ static int routes_per_expert_p99(int T, int topk, int E) {
 // most 2 m99 (m99 from routes_per_expert_p99), and 3 rho + 3 covered the
 // largest need of every CTA on the workload shapes (rho = R / (E (1 - (1 -
 // 1/E)^R)), the expected routes per touched expert). When those rows do not
-// fit next to any of them: 8 warps, the form with the most room for rows
+// fit next to any of them: 7 consumer warps and a producer, the form with the
+// most room for rows
 // (and batched paths for rows read from the f16 scratch and for items with
 // several token groups) -- an item whose rows are not all staged reads them
 // through L2 on every block and runs about 1.5x longer, which decides the
-// call's time through the slowest CTA. 0 when even 8 warps do not fit. Rows
+// call's time through the slowest CTA. 0 when even that form does not fit. Rows
 // beyond the staged ones are read from the f16 scratch in global memory
 // (correct for any routing, only slower).
 static int decode_warps_at(int K, int I, int E, int T, int topk, int max_smem) {
@@ -1021,7 +1119,7 @@ static int decode_warps_at(int K, int I, int E, int T, int topk, int max_smem) {
   if (want > R) want = R;
   for (int cw = 12; cw >= 10; --cw)
     if (decode_smem_bytes(cw, K, I, E, R, want, stride) <= (size_t)max_smem) return cw;
-  if (decode_smem_bytes(8, K, I, E, R, 1, stride) <= (size_t)max_smem) return 8;
+  if (decode_smem_bytes(7, K, I, E, R, 1, stride) <= (size_t)max_smem) return 7;
   return 0;
 }
 
@@ -1061,12 +1159,13 @@ static cudaError_t launch_cw(const DecodeParams& p, size_t smem, int num_sms, cu
   }
   // every CTA must be resident at once (grid barriers): one per SM, cooperative launch
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<CW>, CW * 32, smem);
+  constexpr int kThreads = (CW + (has_producer(CW) ? 1 : 0)) * 32;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<CW>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms);
-  cfg.blockDim = dim3(CW * 32);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1099,7 +1198,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const C
   if (cw == 12) return launch_cw<12>(p, smem, num_sms, stream);
   if (cw == 11) return launch_cw<11>(p, smem, num_sms, stream);
   if (cw == 10) return launch_cw<10>(p, smem, num_sms, stream);
-  return launch_cw<8>(p, smem, num_sms, stream);
+  return launch_cw<7>(p, smem, num_sms, stream);
 }
 
 }  // namespace mxmoe
