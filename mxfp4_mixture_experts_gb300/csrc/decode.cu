@@ -1125,11 +1125,13 @@ static int decode_warps_at(int K, int I, int E, int T, int topk, int max_smem) {
 
 // The form of a call: the one its own T needs, except that when the largest
 // decode T of the layer shape runs one of the 10- to 12-warp forms, every T of
-// the shape runs that form. Each form is its own code, and a sequence of
-// calls whose T move between forms pays for the switch at every change (about
-// 8 us a switch on gptoss128, in a step of T = 1, 4, 16, 32); one form for the
-// shape costs the small calls a little (T = 4 / 16 ran 1.5 / 4.5 us slower on
-// 11 warps than on 12) and saves the switches.
+// the shape runs that form. Serving interleaves calls of different T, and on
+// gptoss128 a sequence of T = 1, 4, 16, 32 whose calls moved between the 12-
+// and 11-warp forms took about 8 us more per change than the same calls on
+// one form; the 11-warp form costs the small calls a little on their own
+// (T = 4 / 16 ran 1.5 / 4.5 us slower than on 12 warps). (All T on the 12-warp
+// form, with one staged row fewer at T = 32, was slower still in such
+// sequences.)
 int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
   const int cw = decode_warps_at(K, I, E, T, topk, max_smem);
   int t_max = kDecodeMaxTokens;
