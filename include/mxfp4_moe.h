@@ -321,6 +321,16 @@ void mxfp4_moe_set_phase_events(void* const* events, int n);
  * reporting without faulting or hanging a GPU. Not thread-safe. */
 void mxfp4_moe_test_skip_grid_arrival(int cta);
 
+/* Test only: the warps per CTA of the decode kernel form that a decode call of
+ * this shape and T would run on a device with max_smem bytes of opt-in shared
+ * memory per block: 12, 11 or 10 (every warp a consumer), 7 (7 consumer warps
+ * and a producer warp), or 0 when no form fits. The form is the one the call's
+ * own T needs, except that every T of a layer shape runs the form of its
+ * largest decode T when that is a 10- to 12-warp form. Host only; no device
+ * is touched. -1 for shapes the decode path does not take (T outside 1..32,
+ * T * topk > 1024, K or I not a multiple of 64, E or topk out of range). */
+int mxfp4_moe_test_decode_form(int T, int K, int I, int E, int topk, int max_smem);
+
 /* Static description of an error code (never NULL). */
 const char* mxfp4_moe_strerror(int code);
 

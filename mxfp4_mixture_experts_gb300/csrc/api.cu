@@ -496,6 +496,13 @@ void mxfp4_moe_set_phase_events(void* const* events, int n) {
 
 void mxfp4_moe_test_skip_grid_arrival(int cta) { g_test_skip_arrival = cta < 0 ? -1 : cta; }
 
+int mxfp4_moe_test_decode_form(int T, int K, int I, int E, int topk, int max_smem) {
+  if (T < 1 || T > kDecodeMaxT || topk < 1 || topk > 32 || topk > E || E < 1 || E > kMaxExperts ||
+      T * topk > kDecodeMaxRoutes || K < 64 || I < 64 || K % 64 || I % 64 || max_smem < 0)
+    return -1;
+  return mxmoe::decode_warps(K, I, E, T, topk, max_smem);
+}
+
 const char* mxfp4_moe_strerror(int code) {
   switch (code) {
     case MXFP4_MOE_OK: return "ok";

@@ -61,6 +61,8 @@ size_t workspace_zero_kept_bytes();
 
 // Whether the decode kernel's shared-memory plan fits for these sizes.
 bool decode_fits(int K, int I, int E, int T, int topk, int max_smem);
+// Warps per CTA of the decode form a call would run (7: 7 consumers + producer).
+int decode_warps(int K, int I, int E, int T, int topk, int max_smem);
 
 // One cooperative launch (one CTA per SM, all resident) per decode call.
 cudaError_t launch_decode(const DecodeArgs& a, const CUtensorMap& tmap1, const CUtensorMap& tmap2,

@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_dequant_form.restype = i32
     L.mxfp4_moe_test_skip_grid_arrival.argtypes = [i32]
     L.mxfp4_moe_test_skip_grid_arrival.restype = None
+    L.mxfp4_moe_test_decode_form.argtypes = [i32] * 6
+    L.mxfp4_moe_test_decode_form.restype = i32
     L.mxfp4_moe_set_phase_events.argtypes = [vp, i32]
     L.mxfp4_moe_set_phase_events.restype = None
     L.mxfp4_moe_strerror.argtypes = [i32]
@@ -76,6 +78,13 @@ def lib() -> ctypes.CDLL:
     L.mxfp4_moe_version.restype = i32
     _lib = L
     return L
+
+
+def decode_form(T: int, K: int, I: int, E: int, topk: int, max_smem: int = 232448) -> int:
+    """Warps per CTA of the decode form a call of this shape and T runs (7: seven
+    consumer warps and a producer), 0 when none fits, -1 for shapes the decode
+    path does not take. Host only (227 KB of shared memory per block by default)."""
+    return lib().mxfp4_moe_test_decode_form(T, K, I, E, topk, max_smem)
 
 
 def strerror(code: int) -> str:
