@@ -1130,8 +1130,8 @@ static int decode_warps_at(int K, int I, int E, int T, int topk, int max_smem) {
 // and 11-warp forms took about 8 us more per change than the same calls on
 // one form; the 11-warp form costs the small calls a little on their own
 // (T = 4 / 16 ran 1.5 / 4.5 us slower than on 12 warps). (All T on the 12-warp
-// form, with one staged row fewer at T = 32, was slower still in such
-// sequences.)
+// form, with one staged row fewer at T = 32, was slower: T = 32 routings whose
+// CTAs need more rows than 12 warps leave room for read them through L2.)
 int decode_warps(int K, int I, int E, int T, int topk, int max_smem) {
   const int cw = decode_warps_at(K, I, E, T, topk, max_smem);
   int t_max = kDecodeMaxTokens;
