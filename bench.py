@@ -21,8 +21,9 @@ from a second pass at each T: a chain of 8 calls (one cooperative decode
 launch each: w13 + SwiGLU, w2, combine) on 8 distinct layers captured in one
 graph, median replay time / 8 (the pages' protocol), against the touched
 experts' packed bytes. ``e2e`` repeats the metric through the C-ABI
-with host buffers (pinned host -> device copies of each call's activations and
-routing, device -> host copy of its output, inside the timed region).
+with host buffers: every step copies its calls' activations and routing up
+from one pinned host buffer (one copy) and their outputs down (one copy),
+inside the timed region.
 ``--impl reference`` times the CPU oracle on the same workload instead.
 """
 from __future__ import annotations
@@ -177,13 +178,65 @@ class DecodeWorkload:
             ly = dict(T=T, hidden=hidden.to(dev), ids=ids.to(dev), w=w.to(dev), w13=w13, s13=s13,
                       w2=w2, s2=s2, out=torch.empty(T, s.K, dtype=torch.bfloat16, device=dev),
                       host_hidden=hidden.pin_memory(), host_ids=ids.pin_memory(),
-                      host_w=w.pin_memory(),
-                      host_out=torch.empty(T, s.K, dtype=torch.bfloat16).pin_memory())
+                      host_w=w.pin_memory())
             ly["D"] = touched_experts(ly["ids"], s.E)
             self.L.append(ly)
         Tmax = max(self.tokens)
         self.ws = moe.new_workspace(Tmax, s.K, s.I, s.E, s.topk, dev)
         self.calls_per_step = len(self.tokens)
+        self._pack_steps()
+
+    def _pack_steps(self):
+        """The end-to-end pass moves a step the way a serving loop does: the
+        step's inputs (every call's hidden rows, routing ids and weights) sit
+        in one pinned host buffer and go up in one copy, and the step's outputs
+        come back in one copy. Each call reads and writes views of the two
+        device buffers."""
+        def align(n):
+            return (n + 255) // 256 * 256
+        self.packs = []
+        n = self.calls_per_step
+        for g in range(self.layers // n):
+            lys = self.L[g * n:(g + 1) * n]
+            srcs = [t for ly in lys for t in (ly["host_hidden"], ly["host_ids"], ly["host_w"])]
+            offs, o = [], 0
+            for t in srcs:
+                offs.append(o)
+                o += align(t.numel() * t.element_size())
+            host_in = torch.zeros(o, dtype=torch.uint8).pin_memory()
+            for t, off in zip(srcs, offs):
+                nb = t.numel() * t.element_size()
+                host_in[off:off + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+            dev_in = torch.empty(o, dtype=torch.uint8, device=self.dev)
+            views = []
+            for t, off in zip(srcs, offs):
+                nb = t.numel() * t.element_size()
+                views.append(dev_in[off:off + nb].view(t.dtype).view(t.shape))
+            out_offs, oo = [], 0
+            for ly in lys:
+                out_offs.append(oo)
+                oo += align(ly["out"].numel() * 2)
+            dev_out = torch.empty(oo, dtype=torch.uint8, device=self.dev)
+            host_out = torch.empty(oo, dtype=torch.uint8).pin_memory()
+            outs = [dev_out[off:off + ly["out"].numel() * 2].view(torch.bfloat16).view(ly["out"].shape)
+                    for ly, off in zip(lys, out_offs)]
+            calls = [(ly, views[3 * i], views[3 * i + 1], views[3 * i + 2], outs[i])
+                     for i, ly in enumerate(lys)]
+            h2d = sum(t.numel() * t.element_size() for t in srcs)
+            d2h = sum(ly["out"].numel() * 2 for ly in lys)
+            self.packs.append(dict(host_in=host_in, dev_in=dev_in, dev_out=dev_out,
+                                   host_out=host_out, calls=calls, h2d=h2d, d2h=d2h))
+
+    def step_e2e(self, step: int, stream):
+        """One step end to end: its inputs up in one copy, its calls, its
+        outputs down in one copy. Returns the bytes moved each way."""
+        pk = self.packs[step % len(self.packs)]
+        pk["dev_in"].copy_(pk["host_in"], non_blocking=True)
+        for ly, hidden, ids, w, out in pk["calls"]:
+            self.moe.forward(hidden, ids, w, ly["w13"], ly["s13"], ly["w2"], ly["s2"], out=out,
+                             workspace=self.ws, stream=stream)
+        pk["host_out"].copy_(pk["dev_out"], non_blocking=True)
+        return pk["h2d"], pk["d2h"]
 
     def step_layers(self, step: int):
         n = self.calls_per_step
@@ -192,17 +245,6 @@ class DecodeWorkload:
     def call(self, ly, stream=None):
         self.moe.forward(ly["hidden"], ly["ids"], ly["w"], ly["w13"], ly["s13"], ly["w2"],
                          ly["s2"], out=ly["out"], workspace=self.ws, stream=stream)
-
-    def call_e2e(self, ly, stream):
-        ly["hidden"].copy_(ly["host_hidden"], non_blocking=True)
-        ly["ids"].copy_(ly["host_ids"], non_blocking=True)
-        ly["w"].copy_(ly["host_w"], non_blocking=True)
-        self.call(ly, stream)
-        ly["host_out"].copy_(ly["out"], non_blocking=True)
-
-    def e2e_bytes(self, ly):
-        T, K, k = ly["T"], self.shape.K, self.shape.topk
-        return T * K * 2 + 2 * T * k * 4, T * K * 2
 
     def alg_bytes(self, ly):
         s = self.shape
@@ -707,22 +749,22 @@ def recorded_traffic(kind: str):
 
 
 def time_e2e(wl, steps: int, warmup: int):
+    """End to end through the C ABI from pinned host buffers: every step copies
+    its inputs up (one copy), runs its calls and copies its outputs down (one
+    copy), all inside the timed region."""
     stream = torch.cuda.Stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     h2d = d2h = 0
     with torch.cuda.stream(stream):
         for s in range(warmup):
-            for ly in wl.step_layers(s):
-                wl.call_e2e(ly, stream)
+            wl.step_e2e(s, stream)
         stream.synchronize()
         e0.record(stream)
         for s in range(steps):
-            for ly in wl.step_layers(s):
-                wl.call_e2e(ly, stream)
-                a, b = wl.e2e_bytes(ly)
-                h2d += a
-                d2h += b
+            a, b = wl.step_e2e(s, stream)
+            h2d += a
+            d2h += b
         e1.record(stream)
     stream.synchronize()
     return e0.elapsed_time(e1), h2d // steps, d2h // steps
